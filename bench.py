@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark of the Flint-shape W4A16 (NVFP4) MoE decode layer on one GB300.
+
+Metric: microseconds per MoE decode layer at batch 1 (lower is better), with
+the achieved HBM bandwidth over the unique weight bytes the layer touches.
+A step is one decode of one layer (router, sigmoid top-6, gate/up + SiLU*up,
+down + combine, shared expert) for one batch of synthetic tokens. Steps rotate
+through a pool of distinct seeded layers (47 by default, the MoE layer count
+of the Flint stack), launched back to back on one stream with programmatic
+dependent launch and replayed from a CUDA graph: each layer's weights are
+touched once per rotation, 631 MB per rotation at batch 1 against a 129 MB
+L2, so inputs are larger than L2.
+
+One JSON line is printed by rank 0. --impl reference times the CPU oracle on
+the same workload instead (a bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FLINT = dict(hidden=2048, num_experts=256, top_k=6, inter=512, n_shared=1)
+WORKLOAD = ("Flint-shape NVFP4 W4A16 MoE decode layer: hidden 2048, 256 experts, sigmoid top-6 renormalised "
+            "+ 1 shared expert, intermediate 512, SwiGLU, bf16 router and activations")
+METRIC = "us per MoE decode layer (batch 1) and achieved HBM GB/s"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--batch", type=int, default=1)
+    p.add_argument("--layers", type=int, default=47)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--quick", action="store_true", help="skip the batch-8, isolated, e2e and CPU legs")
+    p.add_argument("--oracle-leg", type=int, default=0, help=argparse.SUPPRESS)
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_leg(n_steps: int, batch: int, seed: int, budget_s: float) -> dict:
+    """Times the oracle's decode of one Flint-shape layer, n_steps times (or
+    fewer if the time budget runs out). Weights of the experts the routing
+    selects are generated and quantised before timing starts."""
+    import numpy as np  # noqa: F401
+
+    import synth
+    from oracle import moe, nvfp4
+    d = FLINT
+    cfg = moe.Config(**d)
+    x = moe.bf16_bits_to_f64(synth.x_bf16(seed, 0, batch, d["hidden"]))
+    router = moe.bf16_bits_to_f64(synth.router_bf16(seed, 0, d["num_experts"], d["hidden"]))
+    routing = moe.route(x, router, cfg)
+    cache = {}
+    for e in sorted(set(routing.idx.ravel().tolist()) | {d["num_experts"] + s for s in range(d["n_shared"])}):
+        mats = synth.expert_f32(seed, 0, e, d["hidden"], d["inter"])
+        cache[e] = tuple(moe.NVFP4Matrix(*nvfp4.quantize(m)) for m in mats)
+    times = []
+    t_start = time.perf_counter()
+    for _ in range(max(1, n_steps)):
+        t0 = time.perf_counter()
+        moe.moe_layer(x, router, cache.__getitem__, cfg)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    return {"us_per_layer": 1e6 * statistics.mean(times), "steps_timed": len(times),
+            "seconds": time.perf_counter() - t_start}
+
+
+def run_oracle_subprocess(n_steps: int, batch: int, seed: int, budget_s: float) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.oracle_leg(%d, %d, %d, %f)))" % (ROOT, n_steps, batch, seed, budget_s))
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+    if res.returncode != 0:
+        raise RuntimeError("oracle leg failed: " + res.stderr[-2000:])
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    budget = 150.0
+    warm = run_oracle_subprocess(min(args.warmup, 1), args.batch, args.seed, budget)
+    res = run_oracle_subprocess(args.steps, args.batch, args.seed, budget)
+    sample = (f"oracle decode of one Flint-shape layer at batch {args.batch} per step (float64 numpy, 1 thread), "
+              f"{res['steps_timed']} of {args.steps} requested steps timed within a {budget:.0f} s budget; "
+              f"expert weights generated and quantised before timing")
+    v = res["us_per_layer"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/layer", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1000.0, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": args.batch},
+            "cpu_baseline": {"value": v, "unit": "us/layer", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "warmup_us": warm["us_per_layer"]}
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed work runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peak_gbs() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(batch: int):
+    """DRAM bytes per decode from the committed ncu summary, if it was taken on
+    the current kernel sources (the summary records their hash)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "w4a16_moe_decode_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", "traffic_b%d.txt" % batch)
+    try:
+        with open(path) as f:
+            kv = dict(line.strip().split("=", 1) for line in f if "=" in line and not line.startswith("#"))
+        if kv.get("csrc_sha256_16") == digest:
+            return float(kv["dram_bytes_per_layer"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+def gpu_arm(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import synth  # noqa: F401  (the CPU generator is the definition the device one follows)
+    from w4a16_moe_decode_gb300 import binding as fb
+    from w4a16_moe_decode_gb300 import layers
+    from w4a16_moe_decode_gb300.build import build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+    fb.lib()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    cfg = fb.make_config(**FLINT)
+    P = args.layers
+
+    def build_pool(B):
+        pool = [layers.synth_layer(cfg, args.seed + 1000 * rank, L, dev) for L in range(P)]
+        xs = [layers.synth_x(B, cfg.hidden, args.seed + 1000 * rank, L, dev) for L in range(P)]
+        outs = [torch.empty_like(x) for x in xs]
+        ws = layers.workspace(cfg, B, dev)
+        return pool, xs, outs, ws
+
+    def distinct_per_layer(pool, xs, outs, ws, B):
+        idx = torch.empty(B, cfg.top_k, dtype=torch.int32, device=dev)
+        w = torch.empty(B, cfg.top_k, dtype=torch.float32, device=dev)
+        ds = []
+        for L in range(P):
+            fb.flint_moe_decode(pool[L].handle, xs[L], B, outs[L], ws)
+            fb.flint_moe_debug_routing(cfg, ws, B, idx, w)
+            ds.append(len(set(idx.cpu().numpy().ravel().tolist())))
+        st, bits = fb.flint_moe_read_status(ws)
+        if st != fb.OK or bits:
+            raise RuntimeError(f"device status {bits} during setup")
+        return ds
+
+    def unique_bytes(D, B):
+        per_matrix = cfg.inter * cfg.hidden // 2 + cfg.inter * cfg.hidden // 16 + 4
+        return cfg.num_experts * cfg.hidden * 2 + (D + cfg.n_shared) * 3 * per_matrix + 2 * B * cfg.hidden * 2
+
+    def timed_graph(pool, xs, outs, ws, B, steps, warmup, sample_clocks=False):
+        stream = torch.cuda.Stream(device=dev)
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            for s in range(warmup):
+                L = s % P
+                fb.flint_moe_decode(pool[L].handle, xs[L], B, outs[L], ws, stream)
+            cycle = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(cycle, stream=stream):
+                for L in range(P):
+                    fb.flint_moe_decode(pool[L].handle, xs[L], B, outs[L], ws, stream)
+            rem = steps % P
+            tail = None
+            if rem:
+                tail = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(tail, stream=stream):
+                    for L in range(rem):
+                        fb.flint_moe_decode(pool[L].handle, xs[L], B, outs[L], ws, stream)
+            cycle.replay()
+            stream.synchronize()
+            clocks = None
+            if sample_clocks:
+                sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                                       else 0)
+                sampler.start()
+                t_end = time.time() + 1.5  # sustained load so the sampler sees the clocks under this work
+                while time.time() < t_end:
+                    for _ in range(50):
+                        cycle.replay()
+                    stream.synchronize()
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps // P):
+                cycle.replay()
+            if tail is not None:
+                tail.replay()
+            e1.record(stream)
+            stream.synchronize()
+            barrier()
+            if sample_clocks:
+                clocks = sampler.stop()
+        ms = e0.elapsed_time(e1)
+        st, bits = fb.flint_moe_read_status(ws, stream)
+        if st != fb.OK or bits:
+            raise RuntimeError(f"device status {bits} after the timed region")
+        return max_over_ranks(ms), clocks
+
+    def isolated(pool, xs, outs, ws, B, reps=40):
+        """One layer at a time with L2 flushed before each (256 MB write)."""
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream()
+        times = []
+        for r in range(reps):
+            L = r % P
+            flush.fill_(float(r))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fb.flint_moe_decode(pool[L].handle, xs[L], B, outs[L], ws, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1000.0)
+        return statistics.median(times)
+
+    def e2e(pool, B, steps):
+        """Through the C ABI with host buffers: each step copies x from pinned
+        host memory, decodes, and copies out back to pinned host memory."""
+        xh = [layers.synth_x(B, cfg.hidden, args.seed, L, dev).cpu().pin_memory() for L in range(P)]
+        oh = [torch.empty(B, cfg.hidden, dtype=torch.int16).pin_memory() for _ in range(P)]
+        xd = torch.empty(B, cfg.hidden, dtype=torch.int16, device=dev)
+        od = torch.empty_like(xd)
+        ws = layers.workspace(cfg, B, dev)
+        stream = torch.cuda.current_stream()
+        for s in range(min(steps, 50)):
+            L = s % P
+            xd.copy_(xh[L], non_blocking=True)
+            fb.flint_moe_decode(pool[L].handle, xd, B, od, ws, stream)
+            oh[L].copy_(od, non_blocking=True)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(steps):
+            L = s % P
+            xd.copy_(xh[L], non_blocking=True)
+            fb.flint_moe_decode(pool[L].handle, xd, B, od, ws, stream)
+            oh[L].copy_(od, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return max_over_ranks(e0.elapsed_time(e1)) * 1000.0 / steps
+
+    K, W, B = args.steps, max(args.warmup, 3), args.batch
+    pool, xs, outs, ws = build_pool(B)
+    ds = distinct_per_layer(pool, xs, outs, ws, B)
+    bytes_per_step = statistics.mean(unique_bytes(D, B) for D in ds)
+    ms, clocks = timed_graph(pool, xs, outs, ws, B, K, W, sample_clocks=True)
+    us = ms * 1000.0 / K / world
+    us_rank = ms * 1000.0 / K
+    gbs = bytes_per_step / (us_rank * 1e-6) / 1e9
+    peak, peak_kind = measured_peak_gbs()
+    extra = {}
+    if not args.quick:
+        extra["isolated_l2_flushed_us"] = isolated(pool, xs, outs, ws, B)
+        e2e_us = e2e(pool, B, min(K, 4000))
+    else:
+        e2e_us = None
+    del pool, xs, outs, ws
+    torch.cuda.empty_cache()
+    if not args.quick and B == 1:
+        pool8, xs8, outs8, ws8 = build_pool(8)
+        ds8 = distinct_per_layer(pool8, xs8, outs8, ws8, 8)
+        b8 = statistics.mean(unique_bytes(D, 8) for D in ds8)
+        ms8, _ = timed_graph(pool8, xs8, outs8, ws8, 8, min(K, 4700), W)
+        us8 = ms8 * 1000.0 / min(K, 4700)
+        extra["batch8"] = {"us_per_layer": us8, "gbs": b8 / (us8 * 1e-6) / 1e9, "frac": b8 / (us8 * 1e-6) / 1e9 / peak,
+                           "mean_distinct_experts": statistics.mean(ds8), "unique_bytes_per_layer": b8,
+                           "isolated_l2_flushed_us": isolated(pool8, xs8, outs8, ws8, 8)}
+        del pool8, xs8, outs8, ws8
+        torch.cuda.empty_cache()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.quick and world == 1:
+        try:
+            r = run_oracle_subprocess(30, B, args.seed, 25.0)
+            cpu = {"value": r["us_per_layer"], "unit": "us/layer", "cores": 1, "kind": "oracle",
+                   "sample": f"{r['steps_timed']} oracle decodes of one Flint-shape layer at batch {B} "
+                             f"(float64 numpy, 1 thread, {r['seconds']:.1f} s); weights of the selected experts "
+                             f"generated before timing"}
+        except Exception as exc:  # the GPU number stands without the CPU leg
+            cpu = {"value": None, "unit": "us/layer", "cores": 1, "kind": "oracle", "sample": f"failed: {exc}"}
+    line = {
+        "metric": METRIC, "value": us, "unit": "us/layer", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": us_rank / 1000.0, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 x bf16 -> f16 tensor-core products, f32 accumulate", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "layers_in_rotation": P,
+                   "l2": f"inputs larger than L2: {P} distinct layers rotated, "
+                         f"{P * bytes_per_step / 1e6:.0f} MB touched per rotation",
+                   "launch": "3 kernels per layer, programmatic dependent launch, CUDA graph replay"},
+        "gbs": gbs,
+        "unique_bytes_per_layer": bytes_per_step,
+        "mean_distinct_experts": statistics.mean(ds),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_kind": peak_kind, "kernel": "flint_moe_decode (k_router + k_gateup + k_down)",
+                     "traffic": recorded_traffic(B)},
+        "clocks": clocks,
+        "e2e": None if e2e_us is None else {"value": e2e_us, "unit": "us/layer",
+                                            "h2d_bytes_per_step": B * cfg.hidden * 2,
+                                            "d2h_bytes_per_step": B * cfg.hidden * 2},
+        "gpu_launches": 3 * K,
+        "cpu_baseline": cpu,
+    }
+    line.update(extra)
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

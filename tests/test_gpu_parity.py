@@ -1,0 +1,239 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Pass rules, fixed in advance: expert indices and dequantised weights
+bit-exact (ties to the lower index); tokens whose top-k / top-(k+1) key gap
+is below 1e-6 are reported and excluded; routing weights within 1e-6;
+outputs within 2^-7 * max(1, |ref|) per element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import moe, nvfp4
+from w4a16_moe_decode_gb300 import binding as fb
+from w4a16_moe_decode_gb300 import layers
+from w4a16_moe_decode_gb300.build import build
+
+from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, oracle_config, oracle_experts,
+                     oracle_inputs)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+    fb.lib()
+
+
+def cfg_of(d, fmt=fb.NVFP4, **kw):
+    return fb.make_config(hidden=d["hidden"], num_experts=d["num_experts"], top_k=d["top_k"], inter=d["inter"],
+                          n_shared=d["n_shared"], weight_fmt=fmt, **kw)
+
+
+def gpu_decode(cfg, dl, B, seed, layer, ws=None):
+    x = layers.synth_x(B, cfg.hidden, seed, layer, DEV)
+    out = torch.full_like(x, 0x7FC0)  # bf16 NaN pattern: every element must be written
+    ws = layers.workspace(cfg, B, DEV) if ws is None else ws
+    fb.flint_moe_decode(dl.handle, x, B, out, ws)
+    idx = torch.empty(B, cfg.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(B, cfg.top_k, dtype=torch.float32, device=DEV)
+    fb.flint_moe_debug_routing(cfg, ws, B, idx, w)
+    st, bits = fb.flint_moe_read_status(ws)
+    assert st == fb.OK and bits == 0
+    return x, out, idx.cpu().numpy(), w.cpu().numpy()
+
+
+def run_parity(d, B, seed=0, layer=0, fmt=fb.NVFP4, tokens=None, bias=None, renormalize=True, routed_scale=1.0):
+    cfg = cfg_of(d, fmt, renormalize=renormalize, routed_scale=routed_scale)
+    bias_t = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).to(DEV)
+    dl = layers.synth_layer(cfg, seed, layer, DEV, bias=bias_t)
+    x, out, idx, w = gpu_decode(cfg, dl, B, seed, layer)
+    xo, router = oracle_inputs(d, seed, layer, B)
+    assert np.array_equal(bits_to_f64(x), xo)  # both generators drew the same activations
+    oc = oracle_config(d, renormalize, routed_scale)
+    tokens = list(range(B)) if tokens is None else tokens
+    ref, routing = moe.moe_layer(xo, router, oracle_experts(d, seed, layer, fmt == fb.BF16), oc, bias, tokens)
+    excluded = check_routing(routing, idx, w, tokens)
+    keep = [i for i, t in enumerate(tokens) if t not in excluded]
+    got = bits_to_f64(out)[tokens]
+    worst = check_out(ref[keep], got[keep], f"B={B} seed={seed}")
+    return worst, excluded, routing
+
+
+# ---------------------------------------------------------------- inputs and formats
+
+def test_synth_gpu_matches_cpu_generator():
+    for key, start, n, sigma in [(synth.stream_key(0, 0, synth.GATE, 3), 0, 4099, 0.02),
+                                 (synth.stream_key(7, 46, synth.X, 31), 123456789, 1000, 1.0)]:
+        f = torch.empty(n, dtype=torch.float32, device=DEV)
+        fb.flint_synth_normal(key, start, n, sigma, False, f)
+        assert np.array_equal(f.cpu().numpy(), synth.normal_scaled_f32(key, start, n, sigma))
+        b = torch.empty(n, dtype=torch.int16, device=DEV)
+        fb.flint_synth_normal(key, start, n, sigma, True, b)
+        assert np.array_equal(b.cpu().numpy().view(np.uint16),
+                              synth.f32_to_bf16_bits(synth.normal_scaled_f32(key, start, n, sigma)))
+
+
+def _gpu_quantize(w):
+    n_mat, rows, cols = w.shape
+    wd = torch.from_numpy(np.ascontiguousarray(w)).to(DEV)
+    codes = torch.empty(n_mat, rows, cols // 2, dtype=torch.uint8, device=DEV)
+    scales = torch.empty(n_mat, rows, cols // 16, dtype=torch.uint8, device=DEV)
+    g = torch.empty(n_mat, dtype=torch.float32, device=DEV)
+    fb.flint_moe_quantize_nvfp4(wd, n_mat, rows, cols, codes, scales, g)
+    return codes.cpu().numpy(), scales.cpu().numpy(), g.cpu().numpy()
+
+
+def test_quantizer_gpu_matches_oracle():
+    mats = [synth.matrix_f32(0, 0, synth.GATE, e, 512, 2048, 0.02) for e in (0, 255)]
+    special = synth.matrix_f32(1, 0, synth.UP, 0, 32, 256, 0.02)
+    special[0] = 0.0                                   # an all-zero row: zero scales and codes
+    special[1, :16] = 0.0                              # one zero block
+    grid = np.array([0, .25, .5, .75, 1, 1.25, 1.5, 1.75, 2, 2.5, 3, 3.5, 4, 5, 6, 7], np.float32)
+    special[2, :16] = grid * np.float32(special.__abs__().max() / 6)   # values near E2M1 midpoints
+    special[3, :16] = -special[2, :16]
+    for w in mats + [special]:
+        c, s, g = _gpu_quantize(w[None])
+        oc, os_, og = nvfp4.quantize(w)
+        assert np.array_equal(s[0], os_)
+        assert np.array_equal(c[0], oc)
+        assert g[0] == og
+    zero = np.zeros((1, 16, 32), np.float32)
+    c, s, g = _gpu_quantize(zero)
+    assert not c.any() and not s.any() and g[0] == 0
+
+
+@pytest.mark.parametrize("d,fmt", [(TINY, fb.NVFP4), (TINY, fb.BF16), (FLINT, fb.NVFP4)])
+def test_pack_is_a_bijection(d, fmt):
+    cfg = cfg_of(d, fmt)
+    canon = layers.synth_canonical(cfg, 3, 0, DEV)
+    packed = torch.empty(fb.flint_moe_packed_bytes(cfg), dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fb.flint_moe_pack(cfg, canon, packed, status)
+    back = {k: torch.full_like(v, 0x5A if v.dtype != torch.float32 else 7.0) for k, v in canon.items()}
+    fb.flint_moe_unpack_debug(cfg, packed, back)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for k in canon:
+        assert torch.equal(canon[k], back[k]), k
+
+
+def test_pack_flags_nan_scales():
+    cfg = cfg_of(TINY)
+    canon = layers.synth_canonical(cfg, 0, 0, DEV)
+    canon["down_scales"][3, 5, 1] = 0x7F
+    packed = torch.empty(fb.flint_moe_packed_bytes(cfg), dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fb.flint_moe_pack(cfg, canon, packed, status)
+    assert int(status.item()) & fb.DEV_ERR_NAN_SCALE
+
+
+@pytest.mark.parametrize("d,experts", [(TINY, range(17)), (FLINT, (0, 77, 256))])
+def test_dequantised_weights_bit_exact(d, experts):
+    cfg = cfg_of(d)
+    dl = layers.synth_layer(cfg, 0, 0, DEV)
+    shapes = [(d["inter"], d["hidden"]), (d["inter"], d["hidden"]), (d["hidden"], d["inter"])]
+    get = oracle_experts(d, 0, 0)
+    for e in experts:
+        mats = get(e)
+        for m in range(3):
+            out = torch.empty(shapes[m], dtype=torch.float32, device=DEV)
+            fb.flint_moe_debug_dequant(cfg, dl.packed, e, m, out)
+            ref = (mats[m].c().astype(np.float32) * np.float32(mats[m].G)).astype(np.float32)
+            assert np.array_equal(out.cpu().numpy(), ref), (e, m)
+
+
+# ---------------------------------------------------------------- the decode layer
+
+@pytest.mark.parametrize("B,seed", [(1, 0), (1, 1), (3, 2), (8, 3), (9, 4), (32, 5)])
+def test_decode_tiny(B, seed):
+    run_parity(TINY, B, seed)
+
+
+def test_decode_flint_batch1():
+    worst, excluded, routing = run_parity(FLINT, 1, seed=0)
+    assert not excluded
+
+
+def test_decode_flint_batch8_sampled():
+    run_parity(FLINT, 8, seed=0, tokens=[0, 3, 7])
+
+
+def test_decode_flint_batch2_and_4_sampled():
+    run_parity(FLINT, 2, seed=1, tokens=[1])
+    run_parity(FLINT, 4, seed=2, tokens=[0, 2])
+
+
+def test_decode_bf16_weights():
+    run_parity(FLINT, 1, seed=0, fmt=fb.BF16)
+    run_parity(FLINT, 8, seed=0, fmt=fb.BF16, tokens=[5])
+    run_parity(TINY, 5, seed=1, fmt=fb.BF16)
+
+
+def test_decode_all_experts_routed_no_renorm_scaled():
+    d = dict(TINY, top_k=16)
+    run_parity(d, 4, seed=6, renormalize=False, routed_scale=2.5)
+
+
+def test_decode_without_shared_expert():
+    run_parity(dict(TINY, n_shared=0), 3, seed=7)
+    run_parity(dict(TINY, n_shared=2), 2, seed=8)
+
+
+def test_decode_selection_bias():
+    bias = np.zeros(16, np.float32)
+    bias[[2, 9]] = 1.0
+    _, _, routing = run_parity(TINY, 4, seed=9, bias=bias)
+    assert all(set(routing.idx[t]) == {2, 9} for t in range(4))
+
+
+def test_decode_batch0_is_a_noop():
+    cfg = cfg_of(TINY)
+    dl = layers.synth_layer(cfg, 0, 0, DEV)
+    out = torch.full((1, cfg.hidden), 123, dtype=torch.int16, device=DEV)
+    ws = layers.workspace(cfg, 1, DEV)
+    fb.flint_moe_decode(dl.handle, out, 0, out, ws)
+    torch.cuda.synchronize()
+    assert int(out[0, 0]) == 123
+
+
+def test_decode_deterministic_and_chained_through_a_graph():
+    """Three layers chained (out of one is x of the next), launched with PDL,
+    captured in a CUDA graph and replayed twice: both replays are bit-identical
+    to the same decodes run one at a time with a full synchronisation between
+    them, and the first layer matches the oracle."""
+    d = TINY
+    cfg = cfg_of(d)
+    B = 2
+    dls = [layers.synth_layer(cfg, 11, L, DEV) for L in range(3)]
+    ws = layers.workspace(cfg, B, DEV)
+    x0 = layers.synth_x(B, cfg.hidden, 11, 0, DEV)
+    bufs = [x0] + [torch.empty_like(x0) for _ in range(3)]
+    serial = [x0] + [torch.empty_like(x0) for _ in range(3)]
+    for L in range(3):
+        fb.flint_moe_decode(dls[L].handle, serial[L], B, serial[L + 1], ws)
+        torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for L in range(3):
+                fb.flint_moe_decode(dls[L].handle, bufs[L], B, bufs[L + 1], ws, s)
+    s.synchronize()
+    for _ in range(2):
+        for b in bufs[1:]:
+            b.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(serial[1:], bufs[1:]):
+            assert torch.equal(a, b)
+    xo, router = oracle_inputs(d, 11, 0, B)
+    ref, routing = moe.moe_layer(xo, router, oracle_experts(d, 11, 0), oracle_config(d))
+    keep = [t for t in range(B) if routing.gap[t] >= 1e-6]
+    check_out(ref[keep], bits_to_f64(serial[1])[keep], "layer 0")
+    st, bits = fb.flint_moe_read_status(ws)
+    assert st == fb.OK and bits == 0

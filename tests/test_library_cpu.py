@@ -1,0 +1,123 @@
+"""The C-ABI library builds, loads and validates arguments on the host (no GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from w4a16_moe_decode_gb300 import binding as fb
+from w4a16_moe_decode_gb300.build import INCLUDE, build
+
+DECL = re.compile(r"^[A-Za-z_][\w\s\*]*?\b(flint_\w+)\s*\(", re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return fb.lib()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(INCLUDE, "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"typedef struct.*?\}\s*\w+;", "", src, flags=re.S)
+        names.update(DECL.findall(src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"flint_moe_decode", "flint_moe_pack", "flint_synth_normal"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def test_no_oracle_in_product_path():
+    root = os.path.dirname(INCLUDE)
+    pkg = os.path.join(root, "w4a16_moe_decode_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            text = open(path).read()
+            assert "import oracle" not in text and "from oracle" not in text, path
+
+
+def flint_cfg(**kw):
+    return fb.make_config(**kw)
+
+
+def test_config_checks(lib):
+    assert fb.flint_moe_check_config(flint_cfg()) == fb.OK
+    assert fb.flint_moe_check_config(flint_cfg(hidden=256, num_experts=16, top_k=2, inter=64)) == fb.OK
+    assert fb.flint_moe_check_config(flint_cfg(hidden=300)) == fb.EUNSUPPORTED
+    assert fb.flint_moe_check_config(flint_cfg(hidden=2304)) == fb.EUNSUPPORTED
+    assert fb.flint_moe_check_config(flint_cfg(inter=100)) == fb.EUNSUPPORTED
+    assert fb.flint_moe_check_config(flint_cfg(top_k=0)) == fb.EUNSUPPORTED
+    assert fb.flint_moe_check_config(flint_cfg(top_k=17)) == fb.EUNSUPPORTED
+    assert fb.flint_moe_check_config(flint_cfg(num_experts=4, top_k=5)) == fb.EUNSUPPORTED
+    assert fb.flint_moe_check_config(flint_cfg(num_experts=513)) == fb.EUNSUPPORTED
+    assert fb.flint_moe_check_config(flint_cfg(n_shared=5)) == fb.EUNSUPPORTED
+    assert fb.flint_moe_check_config(flint_cfg(weight_fmt=2)) == fb.EUNSUPPORTED
+
+
+def test_packed_bytes_is_the_nvfp4_and_bf16_byte_count(lib):
+    # NVFP4: per [rows, cols] matrix rows*cols/2 code bytes + rows*cols/16 scale
+    # bytes; per expert 3 matrices; float32 tensor scales after the experts.
+    c = flint_cfg()
+    per_expert = 3 * (512 * 2048 // 2 + 512 * 2048 // 16)
+    assert per_expert == 1769472
+    n = fb.flint_moe_packed_bytes(c)
+    assert n >= 257 * per_expert + 257 * 12 and n < 257 * per_expert + 257 * 16 + 256
+    b = fb.flint_moe_packed_bytes(flint_cfg(weight_fmt=fb.BF16))
+    assert b >= 257 * 3 * 512 * 2048 * 2
+    assert fb.flint_moe_packed_bytes(flint_cfg(hidden=300)) == 0
+
+
+def test_workspace_bytes(lib):
+    c = flint_cfg()
+    assert fb.flint_moe_workspace_bytes(c, 0) == 0
+    assert fb.flint_moe_workspace_bytes(c, 33) == 0
+    w1, w8, w32 = (fb.flint_moe_workspace_bytes(c, b) for b in (1, 8, 32))
+    assert 0 < w1 < w8 < w32
+    # the bf16 h rows dominate: one per (token, selected or shared expert)
+    assert w32 >= 32 * 7 * 512 * 2
+
+
+def test_decode_rejects_bad_arguments_on_the_host(lib):
+    c = flint_cfg()
+    layer = fb.flint_moe_layer()
+    layer.cfg = c
+    layer.packed = 0x10000
+    layer.router = 0x20000
+    x, out, ws = 0x30000, 0x40000, 0x50000
+    L = fb.lib()
+    assert L.flint_moe_decode(ctypes.byref(layer), x, 0, out, ws, None) == fb.OK      # B = 0: nothing to do
+    assert L.flint_moe_decode(ctypes.byref(layer), x, 33, out, ws, None) == fb.EINVAL
+    assert L.flint_moe_decode(ctypes.byref(layer), x, -1, out, ws, None) == fb.EINVAL
+    assert L.flint_moe_decode(ctypes.byref(layer), None, 1, out, ws, None) == fb.EINVAL
+    assert L.flint_moe_decode(ctypes.byref(layer), x + 2, 1, out, ws, None) == fb.EALIGN
+    assert L.flint_moe_decode(ctypes.byref(layer), x, 1, out + 8, ws, None) == fb.EALIGN
+    assert L.flint_moe_decode(None, x, 1, out, ws, None) == fb.EINVAL
+    layer.cfg.hidden = 300
+    assert L.flint_moe_decode(ctypes.byref(layer), x, 1, out, ws, None) == fb.EUNSUPPORTED
+
+
+def test_layer_init_and_pack_validate(lib):
+    c = flint_cfg()
+    layer = fb.flint_moe_layer()
+    L = fb.lib()
+    assert L.flint_moe_layer_init(ctypes.byref(c), 0x10000, 0x20000, None, ctypes.byref(layer)) == fb.OK
+    assert layer.cfg.hidden == 2048 and layer.packed == 0x10000
+    assert L.flint_moe_layer_init(ctypes.byref(c), 0x10004, 0x20000, None, ctypes.byref(layer)) == fb.EALIGN
+    assert L.flint_moe_layer_init(ctypes.byref(c), None, 0x20000, None, ctypes.byref(layer)) == fb.EINVAL
+    src = fb.flint_moe_src()
+    assert L.flint_moe_pack(ctypes.byref(c), ctypes.byref(src), 0x10000, 10, None, None) == fb.EINVAL
+    assert L.flint_moe_quantize_nvfp4(0x1000, 1, 4, 24, 0x2000, 0x3000, 0x4000, None) == fb.EINVAL
+
+
+def test_synth_stream_key_matches_cpu_generator(lib):
+    import synth
+    for args in [(0, 0, 1, 0), (12345, 3, 4, 200), (2**63 + 5, 46, 2, 256)]:
+        assert fb.flint_synth_stream_key(*args) == synth.stream_key(*args)

@@ -1,0 +1,313 @@
+// Shared device helpers of the Flint-style W4A16 MoE decode library (sm_103a).
+//
+// Contents: the packed weight layout, the workspace layout, inline PTX for
+// bulk copies, mbarriers, programmatic dependent launch and mma.sync, and the
+// NVFP4 -> f16 tensor-core fragment dequantiser.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "flint_moe.h"
+
+namespace flint {
+
+// ---------------------------------------------------------------------------
+// Packed layout (the result of flint_moe_pack).
+//
+// A "tile" is 16 matrix rows by the full reduction length, cut into k-groups of
+// 64 columns (4 tensor-core k-steps of 16). Within a k-group (NVFP4, 576 B):
+//   bytes [0, 512): lane L = 4g + t of the consuming warp owns bytes
+//     [16L, 16L + 16): for k-step ks = 0..3 the four A-fragment bytes
+//     b = 0..3 of mma.m16n8k16, byte b holding rows r = g + 8 (b & 1),
+//     columns c = 2t + 8 (b >> 1) and c + 1 of that k-step (low nibble = c).
+//   bytes [512, 576): the E4M3 scales, [row 16][ks 4].
+// BF16 k-groups (2048 B): lane L owns 64 B = for ks 0..3, registers a0..a3
+//   (2 bf16 each, lower column in the lower half) with the same row/column map.
+// Per expert: I/8 gate/up tiles (rows 0..7 gate rows, 8..15 up rows of the
+// same 8 intermediate indices; reduction length H), then H/16 down tiles
+// (reduction length I). After all E + S experts: float32 globals [E+S][4] =
+// {G_gate, G_up, G_down, 0}.
+// ---------------------------------------------------------------------------
+constexpr int KG_COLS = 64;
+constexpr int KG_NVFP4 = 576;
+constexpr int KG_BF16 = 2048;
+constexpr int KG_CODE_BYTES = 512;
+constexpr int MAX_BATCH = 32;
+constexpr int MAX_TOPK = 16;
+constexpr int MAX_EXPERTS = 512;
+constexpr int MAX_SHARED = 4;
+
+struct Layout {
+  int64_t kg_bytes;      // 576 (NVFP4) or 2048 (BF16)
+  int64_t gu_tile;       // bytes of one gate/up tile
+  int64_t dn_tile;       // bytes of one down tile
+  int64_t gu_bytes;      // all gate/up tiles of one expert
+  int64_t expert_bytes;  // one expert
+  int64_t globals_off;   // offset of the float32 globals
+  int64_t total;         // packed bytes of the layer
+};
+
+__host__ __device__ inline Layout make_layout(int H, int I, int E, int S, int fmt) {
+  Layout L;
+  L.kg_bytes = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  L.gu_tile = (int64_t)(H / KG_COLS) * L.kg_bytes;
+  L.dn_tile = (int64_t)(I / KG_COLS) * L.kg_bytes;
+  L.gu_bytes = (int64_t)(I / 8) * L.gu_tile;
+  L.expert_bytes = L.gu_bytes + (int64_t)(H / 16) * L.dn_tile;
+  L.globals_off = (int64_t)(E + S) * L.expert_bytes;
+  L.total = L.globals_off + (((int64_t)(E + S) * 16 + 255) / 256) * 256;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout. Header words, then 256-byte aligned regions.
+// ---------------------------------------------------------------------------
+enum : int { HDR_COUNTER = 0, HDR_STATUS = 1, HDR_NSLOTS = 2, HDR_NROWS = 3, HDR_BATCH = 4 };
+
+struct WsLayout {
+  size_t logits, topk_idx, topk_w, slot_expert, slot_off, row_tok, row_w, hmax, h, total;
+  int max_slots, max_rows;
+};
+
+__host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__host__ __device__ inline WsLayout make_ws_layout(int E, int k, int I, int S, int maxB) {
+  WsLayout W;
+  W.max_slots = S + (E < maxB * k ? E : maxB * k);
+  W.max_rows = maxB * (k + S);
+  size_t o = 256;
+  W.logits = o;      o = ws_align(o + sizeof(float) * maxB * E);
+  W.topk_idx = o;    o = ws_align(o + sizeof(int) * maxB * k);
+  W.topk_w = o;      o = ws_align(o + sizeof(float) * maxB * k);
+  W.slot_expert = o; o = ws_align(o + sizeof(int) * W.max_slots);
+  W.slot_off = o;    o = ws_align(o + sizeof(int) * (W.max_slots + 1));
+  W.row_tok = o;     o = ws_align(o + sizeof(int) * W.max_rows);
+  W.row_w = o;       o = ws_align(o + sizeof(float) * W.max_rows);
+  W.hmax = o;        o = ws_align(o + sizeof(unsigned) * W.max_rows);
+  W.h = o;           o = ws_align(o + (size_t)2 * W.max_rows * I);
+  W.total = o;
+  return W;
+}
+
+// ---------------------------------------------------------------------------
+// Inline PTX.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Makes initialised mbarriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Bulk (non-tensor) copy global -> this CTA's shared memory, completing on bar.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~limit_ns of wall time,
+// setting FLINT_MOE_DEV_ERR_TIMEOUT in *status. Never spins forever.
+constexpr uint64_t WAIT_LIMIT_NS = 200ull * 1000ull * 1000ull;  // 200 ms
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 63 && global_ns() - t0 > WAIT_LIMIT_NS) {
+      atomicOr(status, FLINT_MOE_DEV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// After a failed wait the CTA may still have bulk copies in flight into its
+// shared memory; give them a second bounded wait before the CTA exits.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > WAIT_LIMIT_NS) return;
+  }
+}
+
+// Programmatic dependent launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Loads. Weights never change during a decode: non-coherent, no L1 allocation.
+// Data written by the previous kernel of the stream: L2 (".cg").
+__device__ __forceinline__ uint4 ld_weights_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int ld_cg_s32(const int* p) { return __ldcg(p); }
+__device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)));
+  return v;
+}
+
+// D += A * B, m16n8k16, f16 inputs, f32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 dequantisation into mma.m16n8k16 A fragments (f16).
+//
+// codes: the 4 fragment bytes of one k-step (byte b -> register a[b]);
+// scales: low byte = E4M3 scale of row g, high byte = scale of row g + 8.
+// a[b] = E2M1 pair * scale, an exact f16 product: |E2M1| <= 6 and
+// E4M3 in [2^-9, 448] give at most 6 significant bits in [2^-10, 2688], all
+// f16 normals, so the tensor core sees the exact dequantised weight c.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void e2m1x4_to_f16x2(uint32_t w, uint32_t (&q)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  uint16_t s = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(s));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_bcast_lo(uint32_t q, uint32_t s) {
+  __half2 qq = *reinterpret_cast<__half2*>(&q);
+  __half2 ss = *reinterpret_cast<__half2*>(&s);
+  __half2 r = __hmul2(qq, __low2half2(ss));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2_bcast_hi(uint32_t q, uint32_t s) {
+  __half2 qq = *reinterpret_cast<__half2*>(&q);
+  __half2 ss = *reinterpret_cast<__half2*>(&s);
+  __half2 r = __hmul2(qq, __high2half2(ss));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// codes_word: the 4 fragment bytes of one k-step; sg, sg8: the 4-byte scale
+// words of rows g and g + 8 in this k-group; ks selects the k-step's byte.
+__device__ __forceinline__ void nvfp4_afrag(uint32_t codes_word, uint32_t sg, uint32_t sg8, int ks,
+                                            uint32_t (&a)[4]) {
+  const uint32_t pair = __byte_perm(sg, sg8, (uint32_t)ks | ((uint32_t)(ks + 4) << 4));
+  const uint32_t s = e4m3x2_to_f16x2(pair);  // lo half: row g, hi half: row g + 8
+  uint32_t q[4];
+  e2m1x4_to_f16x2(codes_word, q);
+  a[0] = hmul2_bcast_lo(q[0], s);
+  a[1] = hmul2_bcast_hi(q[1], s);
+  a[2] = hmul2_bcast_lo(q[2], s);
+  a[3] = hmul2_bcast_hi(q[3], s);
+}
+
+// ---------------------------------------------------------------------------
+// Activation fragments. Per token row, per k-group of 64 columns: 128 bytes,
+// [t 4][ks 4][4 halves] with halves (2t, 2t+1, 2t+8, 2t+9) of the k-step, so
+// thread (g, t) of mma.m16n8k16 reads its B fragments for 4 k-steps as 32
+// contiguous bytes. Row strides in shared memory are padded by 16 bytes.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline int frag_offset_elems(int col) {
+  const int kg = col >> 6, ks = (col >> 4) & 3, c = col & 15;
+  const int t = (c & 7) >> 1, idx = (c & 1) | ((c >> 3) << 1);
+  return kg * 64 + t * 16 + ks * 4 + idx;
+}
+
+// Power-of-two prescale that maps the largest magnitude m into [2^14, 2^15),
+// so values fit f16 without overflow and keep full precision down to 2^-29 m.
+__device__ __forceinline__ int prescale_exp(float maxabs) {
+  const int e = (int)((__float_as_uint(maxabs) >> 23) & 0xFF) - 127;
+  int k = maxabs > 0.f ? 14 - e : 0;
+  k = k > 126 ? 126 : (k < -126 ? -126 : k);
+  return k;
+}
+__device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace flint
