@@ -16,7 +16,8 @@ namespace flint {
 // come from four canonical bytes (src_idx[0..3]); for scale and BF16 words the
 // four bytes are one aligned canonical word (src_idx[0], whole = true).
 struct WordSrc {
-  int mat;          // 0 gate, 1 up, 2 down, 3 = globals (handled separately)
+  int mat;          // 0 gate, 1 up, 2 down (of byte 0; a code word mixes gate and up rows)
+  int mat_b[4];     // matrix of each byte of a code word
   int64_t expert;
   bool is_scale;
   bool whole;
@@ -63,11 +64,11 @@ __host__ __device__ inline void map_word(const Layout& L, int H, int I, int fmt,
       s.is_scale = false;
       s.whole = false;
       for (int b = 0; b < 4; ++b) {
-        const int r = g + 8 * (b & 1);
+        const int r = g + 8 * (b & 1);  // b & 1 selects row g + 8: the up row in a gate/up tile
         const int c = kg * KG_COLS + ks * 16 + 2 * t + 8 * (b >> 1);
         int mat;
         const int row = row_of(r, mat);
-        s.mat = mat;
+        s.mat_b[b] = mat;
         s.idx[b] = (int64_t)row * (cols / 2) + c / 2;
       }
     } else {
@@ -118,9 +119,11 @@ __global__ void k_pack(PackArgs a) {
         for (int b = 0; b < 4; ++b) nan |= ((v >> (8 * b)) & 0x7F) == 0x7F;
         if (nan && a.status) atomicOr(a.status, FLINT_MOE_DEV_ERR_NAN_SCALE);
       } else {
-        const uint8_t* base = a.codes[s.mat] + s.expert * a.codes_per_expert[s.mat];
-        v = (uint32_t)base[s.idx[0]] | ((uint32_t)base[s.idx[1]] << 8) | ((uint32_t)base[s.idx[2]] << 16) |
-            ((uint32_t)base[s.idx[3]] << 24);
+        v = 0;
+        for (int b = 0; b < 4; ++b) {
+          const int m = s.mat_b[b];
+          v |= (uint32_t)a.codes[m][s.expert * a.codes_per_expert[m] + s.idx[b]] << (8 * b);
+        }
       }
     } else {
       const uint8_t* p = a.bf16[s.mat] + s.expert * a.bf16_per_expert[s.mat] + s.idx[0];
@@ -167,8 +170,10 @@ __global__ void k_unpack(UnpackArgs a) {
         uint8_t* p = a.scales[s.mat] + s.expert * a.scales_per_expert[s.mat] + s.idx[0];
         for (int b = 0; b < 4; ++b) p[b] = (uint8_t)(v >> (8 * b));
       } else {
-        uint8_t* base = a.codes[s.mat] + s.expert * a.codes_per_expert[s.mat];
-        for (int b = 0; b < 4; ++b) base[s.idx[b]] = (uint8_t)(v >> (8 * b));
+        for (int b = 0; b < 4; ++b) {
+          const int m = s.mat_b[b];
+          a.codes[m][s.expert * a.codes_per_expert[m] + s.idx[b]] = (uint8_t)(v >> (8 * b));
+        }
       }
     } else {
       uint8_t* p = a.bf16[s.mat] + s.expert * a.bf16_per_expert[s.mat] + s.idx[0];
