@@ -192,6 +192,29 @@ flint_moe_status flint_moe_debug_dequant(const flint_moe_config* cfg, const void
 flint_moe_status flint_moe_read_status(const void* workspace, int32_t* host_status,
                                        cudaStream_t stream);
 
+/* Bytes of the scratch array behind flint_moe_decode_noalloc. */
+#define FLINT_MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* flint_moe_decode for callers that cannot allocate device memory for a
+ * workspace: a plugin whose host application owns every device allocation and
+ * offers it no allocator, or a latency-critical loop in which cudaMalloc and
+ * cudaFree could synchronise the device. No counterpart on the pages: it is a
+ * variant of flint_moe_decode with the same arguments minus the workspace.
+ * The scratch is one array of FLINT_MOE_NOALLOC_SCRATCH_BYTES bytes (1 MiB)
+ * in this library's device memory, held by every GPU that loads the library
+ * until the process exits. It allocates nothing and calls no allocating
+ * routine. The first call on a device looks up the array's device address
+ * (with that device current); make that first call before any stream capture.
+ * Every call shares the array and leaves its contents behind; the call clears
+ * what must start at zero. Calls whose work overlaps on the GPU (other streams,
+ * other threads) race on the array: serialise them. Returns
+ * FLINT_MOE_EUNSUPPORTED when the workspace this shape and batch need
+ * (flint_moe_workspace_bytes) exceeds FLINT_MOE_NOALLOC_SCRATCH_BYTES (the
+ * Flint-shape layer needs about 0.3 MiB at B = 32). Device status bits are not
+ * reported; use flint_moe_decode with a workspace to read them. */
+flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* layer, const uint16_t* x_bf16,
+                                          int32_t B, uint16_t* out_bf16, cudaStream_t stream);
+
 /* ---- loading helpers (checkpoint side, off the decode path) ---- */
 
 /* Quantises n_mat float32 matrices [n_mat][rows][cols] to canonical NVFP4

@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "flint_moe_unpack_debug": (c_int32, [P(flint_moe_config), c_void_p, P(flint_moe_src), c_void_p]),
             "flint_moe_layer_init": (c_int32, [P(flint_moe_config), c_void_p, c_void_p, c_void_p, P(flint_moe_layer)]),
             "flint_moe_decode": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
+            "flint_moe_decode_noalloc": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p]),
             "flint_moe_debug_routing": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
             "flint_moe_debug_dequant": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
             "flint_moe_read_status": (c_int32, [c_void_p, P(c_int32), c_void_p]),
@@ -171,6 +172,13 @@ def flint_moe_layer_init(cfg, packed, router, sel_bias=None) -> flint_moe_layer:
 def flint_moe_decode(layer: flint_moe_layer, x, B: int, out, workspace, stream=None) -> None:
     _check("flint_moe_decode", lib().flint_moe_decode(ctypes.byref(layer), _ptr(x), B, _ptr(out), _ptr(workspace),
                                                       _stream(stream)))
+
+
+def flint_moe_decode_noalloc(layer: flint_moe_layer, x, B: int, out, stream=None) -> None:
+    """flint_moe_decode with the library's own 1 MiB device scratch array in
+    place of a workspace, for callers that cannot allocate device memory."""
+    _check("flint_moe_decode_noalloc", lib().flint_moe_decode_noalloc(ctypes.byref(layer), _ptr(x), B, _ptr(out),
+                                                                      _stream(stream)))
 
 
 def flint_moe_debug_routing(cfg, workspace, B, idx, w, stream=None) -> None:

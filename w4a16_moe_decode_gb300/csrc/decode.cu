@@ -870,3 +870,59 @@ extern "C" flint_moe_status flint_moe_read_status(const void* ws, int32_t* host_
   *host_status = v;
   return (v & FLINT_MOE_DEV_ERR_TIMEOUT) ? FLINT_MOE_ETIMEOUT : FLINT_MOE_OK;
 }
+
+// ===========================================================================
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory for a workspace: a plugin whose
+// host application owns every device allocation and exposes no allocator, or
+// a latency-critical loop where cudaMalloc / cudaFree could synchronise the
+// device and stall other work. For them the decode's scratch lives in one
+// file-scope device array instead. Every GPU that loads this library keeps
+// the array (FLINT_MOE_NOALLOC_SCRATCH_BYTES bytes) until the process exits.
+// ===========================================================================
+#include <mutex>
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[FLINT_MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. The host-side
+// symbol is only a stand-in; the address is looked up once per device.
+flint_moe_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FLINT_MOE_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FLINT_MOE_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return FLINT_MOE_OK;
+}
+
+}  // namespace
+
+extern "C" flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* layer, const uint16_t* x, int32_t B,
+                                                     uint16_t* out, cudaStream_t stream) {
+  if (!layer) return FLINT_MOE_EINVAL;
+  const flint_moe_config* c = &layer->cfg;
+  const flint_moe_status st = flint_moe_check_config(c);
+  if (st != FLINT_MOE_OK) return st;
+  if (B < 0 || B > MAX_BATCH) return FLINT_MOE_EINVAL;
+  if (B == 0) return FLINT_MOE_OK;
+  if (make_ws_layout(c->num_experts, c->top_k, c->inter, c->n_shared, B).total > FLINT_MOE_NOALLOC_SCRATCH_BYTES)
+    return FLINT_MOE_EUNSUPPORTED;
+  void* scratch = nullptr;
+  const flint_moe_status sst = noalloc_scratch(&scratch);
+  if (sst != FLINT_MOE_OK) return sst;
+  // The routing counter must start at zero; the status word is not reported
+  // by this entry point, so both header words are cleared on every call.
+  if (cudaMemsetAsync(scratch, 0, 256, stream) != cudaSuccess) return FLINT_MOE_ECUDA;
+  return flint_moe_decode(layer, x, B, out, scratch, stream);
+}
