@@ -186,6 +186,19 @@ flint_moe_status flint_moe_debug_dequant(const flint_moe_config* cfg, const void
                                          int32_t expert, int32_t mat, float* out,
                                          cudaStream_t stream);
 
+/* Phase trace of the decode kernels, for profiling. Only a library built with
+ * -DFLINT_MOE_TRACE records it; otherwise returns FLINT_MOE_EUNSUPPORTED.
+ * op 0: clear the trace (asynchronous on stream). op 1: copy it to
+ * host_events, uint64 [64 calls][24 events][2] = earliest and latest
+ * %globaltimer (ns) over all blocks, and SYNCHRONISE the stream. Call n of
+ * flint_moe_decode records into slot n % 64. Events: router start 0, after
+ * its wait 1, x arrived 2, end 3; gate/up start 8, after its wait 9, routed
+ * 10, operands arrived 11, products done 12, end 13, routing scan done 14,
+ * routing rows done 15, logits loaded 21, top-k selected 22, top-k written
+ * 23; down start 16, routed 17, after its wait 18, first item ready 19,
+ * end 20. */
+flint_moe_status flint_moe_trace(int32_t op, uint64_t* host_events, cudaStream_t stream);
+
 /* Reads the workspace status word into *host_status and clears it.
  * SYNCHRONISES the stream. Returns FLINT_MOE_ETIMEOUT if the timeout bit
  * was set, FLINT_MOE_OK otherwise (other bits are reported in *host_status). */

@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
             "flint_moe_debug_routing": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
             "flint_moe_debug_dequant": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
             "flint_moe_read_status": (c_int32, [c_void_p, P(c_int32), c_void_p]),
+            "flint_moe_trace": (c_int32, [c_int32, c_void_p, c_void_p]),
             "flint_moe_quantize_nvfp4": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                                    c_void_p]),
             "flint_synth_stream_key": (ctypes.c_uint64, [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
@@ -198,6 +199,17 @@ def flint_moe_read_status(workspace, stream=None) -> tuple[int, int]:
     if st not in (OK, ETIMEOUT):
         raise FlintMoeError("flint_moe_read_status", st)
     return st, v.value
+
+
+def flint_moe_trace(op: int, stream=None):
+    """op 0 clears the phase trace; op 1 returns it as a numpy uint64 array
+    [64 calls][24 events][2] (earliest, latest ns over blocks). Needs the trace
+    build of the library (FLINT_MOE_LIB pointing at it)."""
+    import numpy as np
+    buf = np.zeros((64, 24, 2), dtype=np.uint64) if op == 1 else None
+    st = lib().flint_moe_trace(op, None if buf is None else buf.ctypes.data, _stream(stream))
+    _check("flint_moe_trace", st)
+    return buf
 
 
 def flint_moe_quantize_nvfp4(w, n_mat, rows, cols, codes, scales, global_, stream=None) -> None:

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-LIB = os.path.join(PKG, "libflint_moe.so")
+LIB = os.environ.get("FLINT_MOE_LIB") or os.path.join(PKG, "libflint_moe.so")
 SOURCES = ["decode.cu", "pack.cu", "synth.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -28,10 +28,11 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libflint_moe.so")
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, verbose_ptxas: bool, defines=()) -> str:
+    suffix = ("_" + "_".join(d.lower() for d in defines)) if defines else ""
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + suffix + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-           "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
+           "-I", INCLUDE, "-I", CSRC, *("-D" + d for d in defines), "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -51,20 +52,24 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compiles the library if a source is newer than it; returns its path."""
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose_ptxas: bool = False, trace: bool = False, out: str | None = None) -> str:
+    """Compiles the library if a source is newer than it; returns its path.
+    trace=True builds the phase-trace variant (flint_moe_trace records) into
+    `out` (default libflint_moe_trace.so beside the normal library)."""
+    lib = out or (os.path.join(PKG, "libflint_moe_trace.so") if trace else LIB)
+    if not force and not trace and not _stale():
+        return lib
     os.makedirs(BUILD, exist_ok=True)
+    defines = ("FLINT_MOE_TRACE",) if trace else ()
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, defines), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

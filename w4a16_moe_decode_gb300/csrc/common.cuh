@@ -68,27 +68,29 @@ __host__ __device__ inline Layout make_layout(int H, int I, int E, int S, int fm
 // ---------------------------------------------------------------------------
 enum : int { HDR_COUNTER = 0, HDR_STATUS = 1, HDR_NSLOTS = 2, HDR_NROWS = 3, HDR_BATCH = 4 };
 
+constexpr int MAX_SLOTS = MAX_SHARED + MAX_EXPERTS;
+constexpr int MAX_ROWS = MAX_BATCH * (MAX_TOPK + MAX_SHARED);
+
+// Regions: router logits [B][E]; the routing of the last decode ([B][k]
+// indices and weights, for read-back); the largest |h| per (slot, token) row;
+// h in bf16 [rows][I] in fragment order.
 struct WsLayout {
-  size_t logits, topk_idx, topk_w, slot_expert, slot_off, row_tok, row_w, hmax, h, total;
+  size_t logits, topk_idx, topk_w, hmax, h, total;
   int max_slots, max_rows;
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~(size_t)255; }
 
-__host__ __device__ inline WsLayout make_ws_layout(int E, int k, int I, int S, int maxB) {
+__host__ __device__ inline WsLayout make_ws_layout(int H, int E, int k, int I, int S, int maxB) {
   WsLayout W;
   W.max_slots = S + (E < maxB * k ? E : maxB * k);
   W.max_rows = maxB * (k + S);
   size_t o = 256;
-  W.logits = o;      o = ws_align(o + sizeof(float) * maxB * E);
-  W.topk_idx = o;    o = ws_align(o + sizeof(int) * maxB * k);
-  W.topk_w = o;      o = ws_align(o + sizeof(float) * maxB * k);
-  W.slot_expert = o; o = ws_align(o + sizeof(int) * W.max_slots);
-  W.slot_off = o;    o = ws_align(o + sizeof(int) * (W.max_slots + 1));
-  W.row_tok = o;     o = ws_align(o + sizeof(int) * W.max_rows);
-  W.row_w = o;       o = ws_align(o + sizeof(float) * W.max_rows);
-  W.hmax = o;        o = ws_align(o + sizeof(unsigned) * W.max_rows);
-  W.h = o;           o = ws_align(o + (size_t)2 * W.max_rows * I);
+  W.logits = o;   o = ws_align(o + sizeof(float) * maxB * E);
+  W.topk_idx = o; o = ws_align(o + sizeof(int) * maxB * k);
+  W.topk_w = o;   o = ws_align(o + sizeof(float) * maxB * k);
+  W.hmax = o;     o = ws_align(o + sizeof(unsigned) * W.max_rows);
+  W.h = o;        o = ws_align(o + (size_t)2 * W.max_rows * I);
   W.total = o;
   return W;
 }

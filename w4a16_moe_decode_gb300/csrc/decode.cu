@@ -1,23 +1,32 @@
 // Decode step of the Flint-style W4A16 MoE layer on sm_103a: three kernels
-// chained with programmatic dependent launch.
+// chained with programmatic dependent launch (PDL).
 //
-//   k_router   logits = x Wr^T (FP32 accumulation), then the last block to
-//              finish computes sigmoid, top-k, the routing weights and the
-//              "slots": the distinct experts the batch selected (ascending
-//              expert id) after the always-on shared experts, each with its
-//              list of (token, weight) rows.
-//   k_gateup   one block per (slot, 8 intermediate rows): bulk-copies the
-//              slot's packed gate/up tile into shared memory, dequantises it
-//              into tensor-core fragments and writes h = bf16(silu(g) * u).
-//   k_down     one block per 16 output rows: for every slot, bulk-copies the
-//              down tile and the slot's h rows, multiplies, and accumulates
-//              w * y in a fixed slot order; writes out = bf16(sum).
+//   k_router   logits = x Wr^T (FP32 accumulation); also writes the
+//              activations once in tensor-core fragment order.
+//   k_gateup   one block per (slot, 8 intermediate rows). A slot is one of the
+//              always-on shared experts or one of the distinct experts the
+//              batch selected (ascending id). Every block derives the routing
+//              itself from the 1 KB-per-token logits, bulk-copies its packed
+//              gate/up tile and the slot's activation rows into shared memory,
+//              dequantises into mma fragments and writes h = bf16(silu(g) * u).
+//   k_down     one block per 16 output rows: derives the routing *before*
+//              waiting for k_gateup and prefetches the down tiles it needs,
+//              then, once h exists, multiplies and accumulates w * y in a fixed
+//              slot order; writes out = bf16(sum).
+//
+// Launch order inside a layer and across layers (same stream):
+//   k_router waits for the previous layer, then lets k_gateup launch;
+//   k_gateup fetches the shared expert before its wait and lets k_down launch
+//   right after its wait (so the router has finished when k_down starts);
+//   k_down routes and fetches its weights while k_gateup runs, and waits only
+//   for h. Each kernel's routing-independent bytes therefore move while the
+//   previous kernel runs.
 //
 // "Day-0 Support for Flint on vLLM", section "Optimisation": the small-batch
 // MoE kernels read only the selected experts' weights; routing and the expert
-// combine are fused into the adjacent GEMV kernels; every kernel is launched
-// with programmatic dependent launch so it fetches its routing-independent
-// weights (router rows, shared expert) while the previous kernel still runs.
+// combine are fused into the adjacent GEMV kernels; every kernel uses PDL so it
+// loads its weights while the previous kernel still runs.
+#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -36,18 +45,38 @@ struct DecodeArgs {
   Layout L;
   uint8_t* ws;
   WsLayout W;
+  int gu_nb;      // gate/up weight buffers in flight per warp group (1..3)
+  int trace_seq;  // decode call number, used only by trace builds
 };
 
 __device__ __forceinline__ int* ws_hdr(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws); }
 __device__ __forceinline__ float* ws_logits(const DecodeArgs& a) { return reinterpret_cast<float*>(a.ws + a.W.logits); }
 __device__ __forceinline__ int* ws_topk_idx(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws + a.W.topk_idx); }
 __device__ __forceinline__ float* ws_topk_w(const DecodeArgs& a) { return reinterpret_cast<float*>(a.ws + a.W.topk_w); }
-__device__ __forceinline__ int* ws_slot_expert(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws + a.W.slot_expert); }
-__device__ __forceinline__ int* ws_slot_off(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws + a.W.slot_off); }
-__device__ __forceinline__ int* ws_row_tok(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws + a.W.row_tok); }
-__device__ __forceinline__ float* ws_row_w(const DecodeArgs& a) { return reinterpret_cast<float*>(a.ws + a.W.row_w); }
 __device__ __forceinline__ unsigned* ws_hmax(const DecodeArgs& a) { return reinterpret_cast<unsigned*>(a.ws + a.W.hmax); }
 __device__ __forceinline__ uint16_t* ws_h(const DecodeArgs& a) { return reinterpret_cast<uint16_t*>(a.ws + a.W.h); }
+
+// ---------------------------------------------------------------------------
+// Optional phase trace (built with -DFLINT_MOE_TRACE): per decode call, the
+// earliest and latest %globaltimer over all blocks at each phase boundary of
+// each kernel. Off by default; it adds no work to the decode itself.
+// ---------------------------------------------------------------------------
+#ifdef FLINT_MOE_TRACE
+constexpr int TRACE_CALLS = 64, TRACE_EVENTS = 24;
+__device__ unsigned long long g_trace[TRACE_CALLS][TRACE_EVENTS][2];
+#define FLINT_TRACE(a, ev)                                                          \
+  do {                                                                              \
+    if (threadIdx.x == 0 && (ev) >= 0) {                                            \
+      const unsigned long long t_ = global_ns();                                    \
+      atomicMin(&g_trace[(a).trace_seq % TRACE_CALLS][(ev)][0], t_);                \
+      atomicMax(&g_trace[(a).trace_seq % TRACE_CALLS][(ev)][1], t_);                \
+    }                                                                               \
+  } while (0)
+#else
+#define FLINT_TRACE(a, ev) \
+  do {                     \
+  } while (0)
+#endif
 
 __device__ __forceinline__ float dot8_bf16(const uint4 w, const uint4 x, float acc) {
   acc = fmaf(bf16lo(w.x), bf16lo(x.x), acc);
@@ -62,179 +91,353 @@ __device__ __forceinline__ float dot8_bf16(const uint4 w, const uint4 x, float a
 }
 
 // ===========================================================================
-// Routing: sigmoid, top-k, weights and slots. Run by the last router block.
+// Routing: sigmoid, top-k, renormalised weights, slots and rows. Computed by
+// every block that needs it from the logits in the workspace; the result is
+// a deterministic function of the logits, so all blocks agree.
 // ===========================================================================
-struct RouteSmem {
-  uint32_t mask[MAX_EXPERTS];   // token bitmask per expert
-  int rank[MAX_EXPERTS];        // slot rank of a used expert
-  int rowoff[MAX_EXPERTS];      // first row of its token list (relative)
-  int idx[MAX_BATCH * MAX_TOPK];
+constexpr int MAX_WARPS = 8;
+
+struct __align__(16) RouteSmem {
+  int idx[MAX_BATCH * MAX_TOPK];  // per token, in (key desc, index asc) order
   float w[MAX_BATCH * MAX_TOPK];
-  int scan[4];
+  uint32_t mask[MAX_EXPERTS];     // token bitmask per expert
+  int rowoff[MAX_EXPERTS];        // first row of a used expert's token list
+  int slot_expert[MAX_SLOTS];
+  int slot_off[MAX_SLOTS + 1];
+  int row_tok[MAX_ROWS];
+  float row_w[MAX_ROWS];
+  int sel_e[MAX_WARPS][MAX_TOPK];  // per warp: the winners of the current token
+  float sel_l[MAX_WARPS][MAX_TOPK];
+  float sel_s[MAX_WARPS][MAX_TOPK];
+  float sel_k[MAX_WARPS][MAX_TOPK];
+  int n_slots, n_rows;
 };
 
-__device__ void route_and_slots(const DecodeArgs& a, RouteSmem& sm) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = a.B, E = a.E, k = a.k, S = a.S;
-  for (int i = threadIdx.x; i < E; i += blockDim.x) sm.mask[i] = 0;
-  __syncthreads();
-  const float* lg = ws_logits(a);
-  for (int t = warp; t < B; t += 4) {
-    float key[MAX_EXPERTS / 32], sc[MAX_EXPERTS / 32];
-#pragma unroll
-    for (int j = 0; j < MAX_EXPERTS / 32; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = -INFINITY;
-      sc[j] = 0.f;
-      if (e < E) {
-        const float l = __ldcg(lg + t * E + e);
-        const float s = 1.0f / (1.0f + expf(-l));
-        sc[j] = s;
-        key[j] = a.bias ? s + a.bias[e] : s;
-      }
-    }
-    int my_e = 0;
-    float my_s = 0.f, ssum = 0.f;
-    for (int r = 0; r < k; ++r) {
-      float bk = -INFINITY, bs = 0.f;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < MAX_EXPERTS / 32; ++j) {
-        if (key[j] > bk) {  // strictly greater: the lowest index wins ties
-          bk = key[j];
-          be = lane + 32 * j;
-          bs = sc[j];
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-        if (ok > bk || (ok == bk && oe < be)) {
-          bk = ok;
-          be = oe;
-          bs = os;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < MAX_EXPERTS / 32; ++j)
-        if (lane + 32 * j == be) key[j] = -INFINITY;
-      if (be >= E) {  // only reachable with non-finite logits; keep every index in range
-        if (lane == 0) atomicOr(ws_hdr(a) + HDR_STATUS, FLINT_MOE_DEV_ERR_SLOTS);
-        be = r;
-        bs = 0.f;
-      }
-      if (lane == r) {
-        my_e = be;
-        my_s = bs;
-      }
-      ssum += bs;
-    }
-    if (lane < k) {
-      float w = a.renorm ? my_s / ssum : my_s;
-      w *= a.routed_scale;
-      ws_topk_idx(a)[t * k + lane] = my_e;
-      ws_topk_w(a)[t * k + lane] = w;
-      sm.idx[t * k + lane] = my_e;
-      sm.w[t * k + lane] = w;
-      atomicOr(&sm.mask[my_e], 1u << t);
-    }
-  }
-  __syncthreads();
+// Order-preserving map of a float key to an unsigned integer; 0 means "none".
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
 
-  // Exclusive scan over experts of (used << 16 | token count): slot rank and row offset.
-  const int ept = (E + blockDim.x - 1) / blockDim.x;
-  const int e0 = threadIdx.x * ept;
-  int local = 0;
-  for (int e = e0; e < e0 + ept && e < E; ++e) {
-    const uint32_t m = sm.mask[e];
-    local += m ? (1 << 16) | __popc(m) : 0;
-  }
-  int incl = local;
+__device__ __forceinline__ float sigmoid_f32(float l) { return 1.0f / (1.0f + expf(-l)); }
+
+// Arg-max of two (key, index) pairs whose indices increase left to right: the
+// right one wins only when strictly greater, so equal keys keep the lower index.
+__device__ __forceinline__ void argmax2(uint32_t k0, int j0, uint32_t k1, int j1, uint32_t& k, int& j) {
+  const bool hi = k1 > k0;
+  k = hi ? k1 : k0;
+  j = hi ? j1 : j0;
+}
+
+// Top-k of one token by one warp, any E <= 512. Lane l holds experts l, l+32,
+// ... Without a selection bias the selection runs on the logits (the sigmoid
+// is monotone); the k winners are then ordered by (sigmoid + bias) descending,
+// ties to the lower expert index.
+__device__ void topk_token_wide(const DecodeArgs& a, int t, int warp, int lane, RouteSmem& R, bool write_debug,
+                                int tb) {
+  constexpr int EPL = MAX_EXPERTS / 32;
+  static_assert(EPL == 16, "the arg-max tree below is written for 16 keys per lane");
+  const float* lg = ws_logits(a) + (size_t)t * a.E;
+  const bool biased = a.bias != nullptr;
+  float lv[EPL], bv[EPL];
+  // Every load is issued before any is used, so they are in flight together.
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) sm.scan[warp] = incl;
-  __syncthreads();
-  int warp_off = 0;
-  for (int w2 = 0; w2 < warp; ++w2) warp_off += sm.scan[w2];
-  const int total = sm.scan[0] + sm.scan[1] + sm.scan[2] + sm.scan[3];
-  int run = warp_off + incl - local;
-  int* slot_expert = ws_slot_expert(a);
-  int* slot_off = ws_slot_off(a);
-  for (int e = e0; e < e0 + ept && e < E; ++e) {
-    const uint32_t m = sm.mask[e];
-    if (m) {
-      const int rank = run >> 16, roff = run & 0xFFFF;
-      sm.rank[e] = rank;
-      sm.rowoff[e] = roff;
-      slot_expert[S + rank] = e;
-      slot_off[S + rank] = S * B + roff;
-      run += (1 << 16) | __popc(m);
+  for (int j = 0; j < EPL; ++j) {
+    lv[j] = 0.f;
+    bv[j] = 0.f;
+    if (32 * j < a.E) {
+      const int e = min(lane + 32 * j, a.E - 1);
+      lv[j] = __ldcg(lg + e);
+      if (biased) bv[j] = __ldg(a.bias + e);
     }
   }
-  const int D = total >> 16, R = total & 0xFFFF;
-  const int n_slots = S + D, n_rows = S * B + R;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      slot_expert[s] = E + s;
-      slot_off[s] = s * B;
+  uint32_t key[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = e < a.E ? ordered_key(biased ? sigmoid_f32(lv[j]) + bv[j] : lv[j]) : 0u;
+  }
+  if (t == 0) FLINT_TRACE(a, tb);
+  for (int r = 0; r < a.k; ++r) {
+    uint32_t k8[8], k4[4], k2[2], best;
+    int j8[8], j4[4], j2[2], bj;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) argmax2(key[2 * p], 2 * p, key[2 * p + 1], 2 * p + 1, k8[p], j8[p]);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) argmax2(k8[2 * p], j8[2 * p], k8[2 * p + 1], j8[2 * p + 1], k4[p], j4[p]);
+#pragma unroll
+    for (int p = 0; p < 2; ++p) argmax2(k4[2 * p], j4[2 * p], k4[2 * p + 1], j4[2 * p + 1], k2[p], j2[p]);
+    argmax2(k2[0], j2[0], k2[1], j2[1], best, bj);
+    const uint32_t wmax = __reduce_max_sync(0xffffffffu, best);
+    const int cand = (best == wmax && best != 0u) ? lane + 32 * bj : 0x7fffffff;
+    int win = __reduce_min_sync(0xffffffffu, cand);
+    if (win == 0x7fffffff) {  // only with non-finite logits: keep every index in range
+      if (lane == 0) atomicOr(ws_hdr(a) + HDR_STATUS, FLINT_MOE_DEV_ERR_SLOTS);
+      win = r;
     }
-    slot_off[n_slots] = n_rows;
-    int* hdr = ws_hdr(a);
-    hdr[HDR_NSLOTS] = n_slots;
-    hdr[HDR_NROWS] = n_rows;
-    hdr[HDR_BATCH] = B;
+    if (lane == (win & 31)) {
+      const int wj = win >> 5;
+      float l = 0.f;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (j == wj) {
+          l = lv[j];
+          key[j] = 0u;
+        }
+      R.sel_e[warp][r] = win;
+      R.sel_l[warp][r] = l;
+    }
+  }
+  __syncwarp();
+  if (t == 0) FLINT_TRACE(a, tb < 0 ? -1 : tb + 1);
+  const bool act = lane < a.k;
+  int my_e = 0;
+  float s = 0.f, kf = 0.f;
+  if (act) {
+    my_e = R.sel_e[warp][lane];
+    s = sigmoid_f32(R.sel_l[warp][lane]);
+    kf = biased ? s + __ldg(a.bias + my_e) : s;
+    R.sel_s[warp][lane] = s;
+    R.sel_k[warp][lane] = kf;
+  }
+  __syncwarp();
+  if (act) {
+    int rank = 0;
+    float ssum = 0.f;
+    for (int q = 0; q < a.k; ++q) {
+      const float kq = R.sel_k[warp][q];
+      const int eq = R.sel_e[warp][q];
+      ssum += R.sel_s[warp][q];  // selection order, the same in every lane and block
+      rank += (kq > kf || (kq == kf && eq < my_e)) ? 1 : 0;
+    }
+    float w = a.renorm ? s / ssum : s;
+    w *= a.routed_scale;
+    R.idx[t * a.k + rank] = my_e;
+    R.w[t * a.k + rank] = w;
+    atomicOr(&R.mask[my_e], 1u << t);
+    if (write_debug) {
+      ws_topk_idx(a)[t * a.k + rank] = my_e;
+      ws_topk_w(a)[t * a.k + rank] = w;
+    }
+  }
+  __syncwarp();  // the warp's selection scratch is reused by its next token
+  if (t == 0) FLINT_TRACE(a, tb < 0 ? -1 : tb + 2);
+}
+
+// Inverse of ordered_key.
+__device__ __forceinline__ float unordered_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ void ce_desc(uint64_t& x, uint64_t& y) {  // x >= y afterwards
+  const uint64_t hi = x > y ? x : y, lo = x > y ? y : x;
+  x = hi;
+  y = lo;
+}
+
+// Top-k of one token by one warp for E <= 256 (the Flint shape), same result
+// as topk_token_wide with a fraction of the instructions. Lane l holds experts
+// 8l .. 8l+7, each as one 64-bit word (order-preserving key << 32 | 0xFFFF - e,
+// so a larger word is a larger key or, on equal keys, a lower index), sorts
+// them once with a 19-comparator network, and each round is two warp
+// reductions and a shift of the winning lane's list.
+__device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane, RouteSmem& R, bool write_debug,
+                                  int tb) {
+  constexpr int EPL = 8;
+  const float* lg = ws_logits(a) + (size_t)t * a.E;
+  const bool biased = a.bias != nullptr;
+  const int e0 = lane * EPL;
+  float lv[EPL], bv[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {  // clamped addresses: every load issues at once
+    const int e = min(e0 + j, a.E - 1);
+    lv[j] = __ldcg(lg + e);
+    bv[j] = biased ? __ldg(a.bias + e) : 0.f;
+  }
+  uint64_t v[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = e0 + j;
+    const uint32_t key = ordered_key(biased ? sigmoid_f32(lv[j]) + bv[j] : lv[j]);
+    v[j] = e < a.E ? ((uint64_t)key << 32) | (uint32_t)(0xFFFF - e) : 0ull;
+  }
+  ce_desc(v[0], v[2]); ce_desc(v[1], v[3]); ce_desc(v[4], v[6]); ce_desc(v[5], v[7]);
+  ce_desc(v[0], v[4]); ce_desc(v[1], v[5]); ce_desc(v[2], v[6]); ce_desc(v[3], v[7]);
+  ce_desc(v[0], v[1]); ce_desc(v[2], v[3]); ce_desc(v[4], v[5]); ce_desc(v[6], v[7]);
+  ce_desc(v[2], v[4]); ce_desc(v[3], v[5]);
+  ce_desc(v[1], v[4]); ce_desc(v[3], v[6]);
+  ce_desc(v[1], v[2]); ce_desc(v[3], v[4]); ce_desc(v[5], v[6]);
+  if (t == 0) FLINT_TRACE(a, tb);
+  uint32_t my_hi = 0u, my_lo = 0xFFFFu;
+  for (int r = 0; r < a.k; ++r) {
+    const uint32_t hi = (uint32_t)(v[0] >> 32), lo = (uint32_t)v[0];
+    const uint32_t whi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t wlo = __reduce_max_sync(0xffffffffu, hi == whi ? lo : 0u);
+    if (hi == whi && lo == wlo) {  // the winning lane drops its head
+#pragma unroll
+      for (int j = 0; j < EPL - 1; ++j) v[j] = v[j + 1];
+      v[EPL - 1] = 0ull;
+    }
+    if (lane == r) {
+      my_hi = whi;
+      my_lo = wlo;
+    }
+  }
+  if (t == 0) FLINT_TRACE(a, tb < 0 ? -1 : tb + 1);
+  const bool act = lane < a.k;
+  int my_e = min(0xFFFF - (int)my_lo, a.E - 1);
+  if (act && my_hi == 0u) {  // fewer than k finite keys: only with non-finite logits
+    atomicOr(ws_hdr(a) + HDR_STATUS, FLINT_MOE_DEV_ERR_SLOTS);
+    my_e = lane;
+  }
+  // The winner's logit is its key unless a bias was added to it.
+  const float l = act ? (biased ? __ldcg(lg + my_e) : unordered_key(my_hi)) : 0.f;
+  const float s = act ? sigmoid_f32(l) : 0.f;
+  const float kf = act ? (biased ? s + __ldg(a.bias + my_e) : s) : -INFINITY;
+  // Selection order is (key desc, index asc) already, except that distinct
+  // logits can give equal sigmoids: then reorder by (sigmoid desc, index asc).
+  int rank = lane;
+  const float kprev = __shfl_up_sync(0xffffffffu, kf, 1);
+  if (__any_sync(0xffffffffu, act && lane > 0 && kprev == kf)) {
+    R.sel_e[warp][lane] = my_e;
+    R.sel_k[warp][lane] = kf;
+    __syncwarp();
+    if (act) {
+      rank = 0;
+      for (int q = 0; q < a.k; ++q) {
+        const float kq = R.sel_k[warp][q];
+        const int eq = R.sel_e[warp][q];
+        rank += (kq > kf || (kq == kf && eq < my_e)) ? 1 : 0;
+      }
+    }
+    __syncwarp();
+  }
+  // Sum of the k scores in selection order (a fixed order: deterministic).
+  float ssum = 0.f;
+  for (int q = 0; q < a.k; ++q) ssum += __shfl_sync(0xffffffffu, s, q);
+  if (act) {
+    float w = a.renorm ? s / ssum : s;
+    w *= a.routed_scale;
+    R.idx[t * a.k + rank] = my_e;
+    R.w[t * a.k + rank] = w;
+    atomicOr(&R.mask[my_e], 1u << t);
+    if (write_debug) {
+      ws_topk_idx(a)[t * a.k + rank] = my_e;
+      ws_topk_w(a)[t * a.k + rank] = w;
+    }
+  }
+  if (t == 0) FLINT_TRACE(a, tb < 0 ? -1 : tb + 2);
+}
+
+// Whole block. Slots: the S shared experts first, then the distinct selected
+// experts in ascending id. Rows: each slot's tokens in ascending order, shared
+// rows first (S * B of them). tb: first trace event id, or -1.
+__device__ void compute_routing(const DecodeArgs& a, RouteSmem& R, bool write_debug, int tb) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int B = a.B, E = a.E, k = a.k, S = a.S;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) R.mask[i] = 0;
+  __syncthreads();
+  if (E <= 256) {
+    for (int t = warp; t < B; t += nw) topk_token_narrow(a, t, warp, lane, R, write_debug, tb);
+  } else {
+    for (int t = warp; t < B; t += nw) topk_token_wide(a, t, warp, lane, R, write_debug, tb);
   }
   __syncthreads();
-  int* row_tok = ws_row_tok(a);
-  float* row_w = ws_row_w(a);
-  for (int p = threadIdx.x; p < B * k; p += blockDim.x) {
-    const int t = p / k, e = sm.idx[p];
-    const int pos = __popc(sm.mask[e] & ((1u << t) - 1u));
-    const int row = S * B + sm.rowoff[e] + pos;
-    row_tok[row] = t;
-    row_w[row] = sm.w[p];
+  if (warp == 0) {
+    // Exclusive scan over experts of (used << 16 | token count); lane l owns a
+    // contiguous range of experts so the ranks come out in ascending id. Warp 0
+    // also writes the rows, so the block needs a single barrier afterwards.
+    const int ept = (E + 31) >> 5;
+    const int e0 = lane * ept, e1 = min(E, e0 + ept);
+    int local = 0;
+    if (ept == 8 && E == 256) {  // the Flint shape: two 16-byte loads, no bank conflicts
+      const uint4 m0 = *reinterpret_cast<const uint4*>(&R.mask[e0]);
+      const uint4 m1 = *reinterpret_cast<const uint4*>(&R.mask[e0 + 4]);
+      const uint32_t mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) local += mm[q] ? (1 << 16) | __popc(mm[q]) : 0;
+    } else {
+      for (int e = e0; e < e1; ++e) {
+        const uint32_t m = R.mask[e];
+        local += m ? (1 << 16) | __popc(m) : 0;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int run = incl - local;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t m = R.mask[e];
+      if (m) {
+        const int rank = run >> 16, roff = S * B + (run & 0xFFFF);
+        R.rowoff[e] = roff;
+        R.slot_expert[S + rank] = e;
+        R.slot_off[S + rank] = roff;
+        run += (1 << 16) | __popc(m);
+      }
+    }
+    const int n_slots = S + (total >> 16), n_rows = S * B + (total & 0xFFFF);
+    for (int s = lane; s < S; s += 32) {
+      R.slot_expert[s] = E + s;
+      R.slot_off[s] = s * B;
+    }
+    if (lane == 0) {
+      R.slot_off[n_slots] = n_rows;
+      R.n_slots = n_slots;
+      R.n_rows = n_rows;
+    }
+    __syncwarp();
+    FLINT_TRACE(a, tb < 0 ? -1 : 14);
+    for (int p = lane; p < B * k; p += 32) {
+      const int t = p / k, e = R.idx[p];
+      const int row = R.rowoff[e] + __popc(R.mask[e] & ((1u << t) - 1u));
+      R.row_tok[row] = t;
+      R.row_w[row] = R.w[p];
+    }
+    for (int p = lane; p < S * B; p += 32) {
+      R.row_tok[p] = p % B;
+      R.row_w[p] = 1.0f;
+    }
   }
-  for (int p = threadIdx.x; p < S * B; p += blockDim.x) {
-    row_tok[p] = p % B;
-    row_w[p] = 1.0f;
-  }
-  unsigned* hmax = ws_hmax(a);
-  for (int p = threadIdx.x; p < n_rows; p += blockDim.x) hmax[p] = 0u;
-  if (threadIdx.x == 0) ws_hdr(a)[HDR_COUNTER] = 0;
+  __syncthreads();
+  FLINT_TRACE(a, tb < 0 ? -1 : 15);
 }
 
 // ===========================================================================
-// K1: router GEMV (+ routing by the last block).
+// K1: router GEMV (logits in the workspace); also clears the per-row |h|
+// maxima that k_gateup accumulates.
 // NCH: 16-byte chunks of a router row per lane per pass (H / 256 capped at 8).
 // ===========================================================================
 template <int NCH>
 __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t dsm[];  // x chunk: up to 8 tokens x H bf16
-  __shared__ RouteSmem rs;
   __shared__ __align__(8) uint64_t bar;
-  __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 4 + warp;
   const int passes = a.H / (256 * NCH);
+  FLINT_TRACE(a, 0);
   uint4 w[NCH];
-  if (e < a.E) {
-    const uint8_t* row = reinterpret_cast<const uint8_t*>(a.router + (size_t)e * a.H);
+  auto load_pass = [&](int p) {
+    const uint8_t* row = reinterpret_cast<const uint8_t*>(a.router + (size_t)e * a.H) + (size_t)p * NCH * 512;
 #pragma unroll
     for (int c = 0; c < NCH; ++c) w[c] = ld_weights_v4(row + (size_t)(lane + 32 * c) * 16);
-  }
+  };
+  if (e < a.E) load_pass(0);  // routing-independent: before waiting for x
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
+  pdl_wait();  // x is the previous kernel's output
   pdl_trigger();
-  pdl_wait();
+  FLINT_TRACE(a, 1);
   __syncthreads();
   int* status = ws_hdr(a) + HDR_STATUS;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < a.W.max_rows; i += blockDim.x) ws_hmax(a)[i] = 0u;
   float* lg = ws_logits(a);
   uint32_t phase = 0;
   for (int t0 = 0; t0 < a.B; t0 += 8) {
@@ -244,322 +447,401 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
       mbar_arrive_expect_tx(&bar, bytes);
       bulk_g2s(dsm, a.x + (size_t)t0 * a.H, bytes, &bar);
     }
-    const bool ok = mbar_wait(&bar, phase, status);
+    const bool ok = __syncthreads_and(mbar_wait(&bar, phase, status));  // block-uniform
     phase ^= 1;
-    if (e < a.E && ok) {
-      for (int t = 0; t < nt; ++t) {
-        const uint8_t* xr = dsm + (size_t)t * a.H * 2;
-        float acc = 0.f;
-        for (int p = 0; p < passes; ++p) {
-          if (p > 0) {
-            const uint8_t* row = reinterpret_cast<const uint8_t*>(a.router + (size_t)e * a.H) + (size_t)p * NCH * 512;
+    if (!ok) break;
+    FLINT_TRACE(a, 2);
+    if (e < a.E) {
+      // All tokens of the chunk at once: independent sums give the FMA and
+      // shuffle latencies something to overlap with.
+      float acc[8];
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) w[c] = ld_weights_v4(row + (size_t)(lane + 32 * c) * 16);
+      for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+      for (int p = 0; p < passes; ++p) {
+        if (p > 0 || (t0 > 0 && passes > 1)) load_pass(p);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (t < nt) {
+            const uint8_t* xr = dsm + (size_t)t * a.H * 2 + (size_t)p * NCH * 512;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) acc[t] = dot8_bf16(w[c], lds128(xr + (lane + 32 * c) * 16), acc[t]);
           }
-#pragma unroll
-          for (int c = 0; c < NCH; ++c)
-            acc = dot8_bf16(w[c], lds128(xr + (size_t)p * NCH * 512 + (lane + 32 * c) * 16), acc);
         }
-        acc = warp_sum(acc);
-        if (lane == 0) lg[(t0 + t) * a.E + e] = acc;
-        if (passes > 1 && t + 1 < nt) {  // reload the first pass for the next token
-          const uint8_t* row = reinterpret_cast<const uint8_t*>(a.router + (size_t)e * a.H);
+      }
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) w[c] = ld_weights_v4(row + (size_t)(lane + 32 * c) * 16);
+      for (int t = 0; t < 8; ++t) {
+        if (t < nt) {
+          const float v = warp_sum(acc[t]);
+          if (lane == 0) lg[(t0 + t) * a.E + e] = v;
         }
       }
     }
-    __syncthreads();  // the x chunk is reused by the next copy
+    __syncthreads();  // the x chunk buffer is reused by the next copy
   }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int ticket = atomicAdd(ws_hdr(a) + HDR_COUNTER, 1);
-    s_last = ticket == (int)gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  route_and_slots(a, rs);
+  FLINT_TRACE(a, 3);
 }
 
-// ===========================================================================
-// Activation rows -> fragment order in shared memory.
-// NVFP4 path: f16 with a per-row power-of-two prescale (exact for values
-// within 2^29 of the row's largest magnitude); *inv gets 2^-prescale.
-// BF16 path: bf16 unchanged, *inv = 1.
-// ===========================================================================
-template <int FMT>
-__device__ __forceinline__ void stage_x_row(const uint16_t* src, int len, uint8_t* dst, float* inv, int lane) {
-  float mx = 0.f;
-  if (FMT == FLINT_MOE_NVFP4) {
-    for (int c = lane; c < len / 8; c += 32) {
-      const uint4 v = ld_cg_v4(src + 8 * c);
-      const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int p = 0; p < 4; ++p) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(ws[p])), fabsf(bf16hi(ws[p]))));
-    }
-    mx = warp_max(mx);
-  }
-  const int kx = FMT == FLINT_MOE_NVFP4 ? prescale_exp(mx) : 0;
-  const float sc = exp2i(kx);
-  for (int c = lane; c < len / 8; c += 32) {
-    const uint4 v = ld_cg_v4(src + 8 * c);
-    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      uint32_t bits = ws[p];
-      if (FMT == FLINT_MOE_NVFP4) {
-        const __half2 hv = __floats2half2_rn(bf16lo(ws[p]) * sc, bf16hi(ws[p]) * sc);
-        bits = *reinterpret_cast<const uint32_t*>(&hv);
-      }
-      *reinterpret_cast<uint32_t*>(dst + 2 * frag_offset_elems(8 * c + 2 * p)) = bits;
-    }
-  }
-  if (lane == 0) *inv = exp2i(-kx);
-}
-
-// ===========================================================================
-// K2: gate/up GEMV + SiLU * up for one (slot, tile of 8 intermediate rows).
-// 4 warps split the reduction (H) into contiguous k-group ranges.
-// ===========================================================================
+// One k-group (64 columns) of a 16-row tile against NTMAX token tiles.
+// Even and odd k-groups accumulate into separate registers (cs) so that
+// consecutive mma.sync need not wait for one another.
 template <int FMT, int NTMAX>
-__global__ void __launch_bounds__(128) k_gateup(DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-  const int tile = blockIdx.x, slot = blockIdx.y;
-  const int KGW = a.H / (KG_COLS * 4);
-  const int kslice = KGW * KGB;
-  const int xstride = a.H * 2 + 16;
-  uint8_t* wbuf = smem + warp * kslice;
-  uint8_t* xs = smem + 4 * kslice;
-  float* red = reinterpret_cast<float*>(xs + (size_t)a.B * xstride);
-  float* s_inv = red + 3 * NTMAX * 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_inv + MAX_BATCH);
-
-  if (threadIdx.x < 4) mbar_init(&bars[threadIdx.x], 1);
-  fence_mbar_init();
-  __syncthreads();
-  const bool shared_slot = slot < a.S;
-  auto issue = [&](int expert) {
-    if (lane == 0) {
-      const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + (int64_t)tile * a.L.gu_tile +
-                           (int64_t)warp * kslice;
-      mbar_arrive_expect_tx(&bars[warp], (uint32_t)kslice);
-      bulk_g2s(wbuf, src, (uint32_t)kslice, &bars[warp]);
-    }
-  };
-  if (shared_slot) issue(a.E + slot);  // routing-independent: fetch before waiting
-  pdl_trigger();
-  pdl_wait();
-  int* hdr = ws_hdr(a);
-  const int n_slots = __ldcg(hdr + HDR_NSLOTS);
-  if (slot >= n_slots) return;  // a routed slot this batch does not use; nothing in flight
-  const int expert = __ldcg(ws_slot_expert(a) + slot);
-  const int off = __ldcg(ws_slot_off(a) + slot);
-  const int T = __ldcg(ws_slot_off(a) + slot + 1) - off;
-  if (expert < 0 || expert >= a.E + a.S || T < 1 || T > a.B || off < 0 || off + T > a.W.max_rows) {
-    if (threadIdx.x == 0) atomicOr(hdr + HDR_STATUS, FLINT_MOE_DEV_ERR_SLOTS);
-    if (shared_slot) mbar_drain(&bars[warp], 0);
-    return;
-  }
-  if (!shared_slot) issue(expert);
-  for (int n = warp; n < T; n += 4) {
-    const int tok = __ldcg(ws_row_tok(a) + off + n);
-    stage_x_row<FMT>(a.x + (size_t)tok * a.H, a.H, xs + (size_t)n * xstride, s_inv + n, lane);
-  }
-  __syncthreads();
-
-  float acc[NTMAX][4];
+__device__ __forceinline__ void tile_kgroup(const uint8_t* kp, const uint4 (&bx)[NTMAX][2], int nt_used, int lane,
+                                            float (&acc)[NTMAX][4]) {
+  const int g = lane >> 2;
+  if (FMT == FLINT_MOE_NVFP4) {
+    const uint4 codes = lds128(kp + lane * 16);
+    const uint32_t sg = lds32(kp + KG_CODE_BYTES + g * 4);
+    const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (g + 8) * 4);
+    const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
 #pragma unroll
-  for (int nt = 0; nt < NTMAX; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-  const int nt_used = (T + 7) >> 3;
-  const bool ok = mbar_wait(&bars[warp], 0, hdr + HDR_STATUS);
-  if (ok) {
-    for (int kl = 0; kl < KGW; ++kl) {
-      const int kg = warp * KGW + kl;
-      const uint8_t* kp = wbuf + kl * KGB;
-      uint4 bx[NTMAX][2];
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t af[4];
+      nvfp4_afrag(cw[ks], sg, sg8, ks, af);
 #pragma unroll
       for (int nt = 0; nt < NTMAX; ++nt) {
         if (nt < nt_used) {
-          int n = nt * 8 + g;
-          n = n < T ? n : T - 1;  // columns past the slot's tokens repeat a valid row
-          const uint8_t* rp = xs + (size_t)n * xstride + kg * 128 + t4 * 32;
-          bx[nt][0] = lds128(rp);
-          bx[nt][1] = lds128(rp + 16);
-        }
-      }
-      if (FMT == FLINT_MOE_NVFP4) {
-        const uint4 codes = lds128(kp + lane * 16);
-        const uint32_t sg = lds32(kp + KG_CODE_BYTES + g * 4);
-        const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (g + 8) * 4);
-        const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          uint32_t af[4];
-          nvfp4_afrag(cw[ks], sg, sg8, ks, af);
-#pragma unroll
-          for (int nt = 0; nt < NTMAX; ++nt) {
-            if (nt < nt_used) {
-              const uint4& q = bx[nt][ks >> 1];
-              mma_f16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint4 v = lds128(kp + lane * 64 + ks * 16);
-          const uint32_t af[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int nt = 0; nt < NTMAX; ++nt) {
-            if (nt < nt_used) {
-              const uint4& q = bx[nt][ks >> 1];
-              mma_bf16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
-            }
-          }
+          const uint4& q = bx[nt][ks >> 1];
+          mma_f16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
         }
       }
     }
   } else {
-    mbar_drain(&bars[warp], 0);
-  }
-  if (warp > 0) {
 #pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt)
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint4 v = lds128(kp + lane * 64 + ks * 16);
+      const uint32_t af[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) red[((warp - 1) * NTMAX + nt) * 128 + lane * 4 + i] = acc[nt][i];
-  }
-  __syncthreads();
-  if (warp != 0) return;
-#pragma unroll
-  for (int w2 = 0; w2 < 3; ++w2)
-#pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[nt][i] += red[(w2 * NTMAX + nt) * 128 + lane * 4 + i];
-
-  const float Gg = a.globals[expert * 4 + 0];
-  const float Gu = a.globals[expert * 4 + 1];
-  const int i_row = tile * 8 + g;
-  const int hoff = frag_offset_elems(i_row);
-  uint16_t* h = ws_h(a);
-  unsigned* hmax = ws_hmax(a);
-#pragma unroll
-  for (int nt = 0; nt < NTMAX; ++nt) {
-    if (nt >= nt_used) break;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int n = nt * 8 + 2 * t4 + hh;
-      float hv = 0.f;
-      if (n < T) {
-        const float inv = s_inv[n];
-        const float gv = (acc[nt][hh] * inv) * Gg;
-        const float uv = (acc[nt][2 + hh] * inv) * Gu;
-        const float sv = gv / (1.0f + expf(-gv));
-        const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
-        h[(size_t)(off + n) * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hb);
-        hv = fabsf(__bfloat162float(hb));
+      for (int nt = 0; nt < NTMAX; ++nt) {
+        if (nt < nt_used) {
+          const uint4& q = bx[nt][ks >> 1];
+          mma_bf16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
+        }
       }
-      hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 4));
-      hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 8));
-      hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 16));
-      if (g == 0 && n < T && hv > 0.f) atomicMax(hmax + off + n, __float_as_uint(hv));
     }
   }
 }
 
 // ===========================================================================
+// K2: gate/up GEMV + SiLU * up. A unit is (slot, tile of 8 intermediate rows);
+// units are numbered slot-major. A block has ng groups of 4 warps; group gi
+// works through units blockIdx.x + (gi + ng * jj) * gridDim.x, jj = 0, 1, ...,
+// with nb of them in flight, and synchronises on its own named barrier, so the
+// groups of a block proceed independently. The 4 warps of a group split a
+// unit's reduction (H) into contiguous k-group ranges.
+//
+// Before waiting for the router the block copies the bf16 activations of all
+// tokens, prescales them and stores them in fragment order: they are the
+// previous layer's output, which had completed before the router (which lets
+// this kernel launch only after its own wait) started.
+// ===========================================================================
+constexpr int GU_MAX_GROUPS = 3;
+
+struct GateupPlan {
+  size_t wbuf_off, xstage_off, xs_off, red_off, inv_off, bar_off, total;
+};
+
+__host__ __device__ inline GateupPlan gateup_plan(int H, int B, int fmt, int ntmax, int ng, int nb) {
+  const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  const size_t kslice = (size_t)(H / 256) * kgb;
+  GateupPlan p;
+  size_t o = 0;
+  p.wbuf_off = o;   o += (size_t)ng * nb * 4 * kslice;
+  p.xstage_off = o; o += (size_t)B * H * 2;
+  p.xs_off = o;     o += (size_t)B * (H * 2 + 16);
+  p.red_off = o;    o += sizeof(float) * ng * 2 * 3 * ntmax * 128;
+  p.inv_off = o;    o += sizeof(float) * MAX_BATCH;
+  o = (o + 15) & ~(size_t)15;
+  p.bar_off = o;    o += sizeof(uint64_t) * (ng * nb * 4 + 1);
+  p.total = o;
+  return p;
+}
+
+// Barrier of one 4-warp group (named barrier 1 + gi); returns the AND of v.
+__device__ __forceinline__ bool group_sync_and(int gi, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(gi + 1)
+      : "memory");
+  return r != 0;
+}
+
+template <int FMT, int NTMAX>
+__global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 leaves room for k_down
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ RouteSmem R;
+  constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  const int NG = blockDim.x >> 7, NB = a.gu_nb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int gi = warp >> 2, gw = warp & 3;
+  const int TILES = a.I / 8;
+  const int KGW = a.H / (KG_COLS * 4);
+  const int kslice = KGW * KGB;
+  const int xstride = a.H * 2 + 16;
+  const GateupPlan P = gateup_plan(a.H, a.B, FMT, NTMAX, NG, NB);
+  uint8_t* xstage = smem + P.xstage_off;
+  uint8_t* xs = smem + P.xs_off;
+  // Cross-warp partial sums of a group, double-buffered by unit parity: warp 0
+  // of the group reads one buffer while warps 1..3 fill the other.
+  float* red = reinterpret_cast<float*>(smem + P.red_off) + gi * 2 * 3 * NTMAX * 128;
+  float* s_inv = reinterpret_cast<float*>(smem + P.inv_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);  // [NG][NB][4] weights, then x
+  uint64_t* xbar = bars + NG * NB * 4;
+  auto wbar = [&](int b) { return &bars[(gi * NB + b) * 4 + gw]; };
+  auto wbuf = [&](int b) { return smem + P.wbuf_off + ((size_t)(gi * NB + b) * 4 + gw) * kslice; };
+  int* status = ws_hdr(a) + HDR_STATUS;
+  const int G = gridDim.x;
+  auto unit_of = [&](int jj) { return (int)blockIdx.x + (gi + NG * jj) * G; };
+
+  FLINT_TRACE(a, 8);
+  if (threadIdx.x < NG * NB * 4 + 1) mbar_init(&bars[threadIdx.x], 1);
+  fence_mbar_init();
+  __syncthreads();
+  auto issue_w = [&](int b, int expert, int tile) {
+    if (lane == 0) {
+      const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + (int64_t)tile * a.L.gu_tile +
+                           (int64_t)gw * kslice;
+      mbar_arrive_expect_tx(wbar(b), (uint32_t)kslice);
+      bulk_g2s(wbuf(b), src, (uint32_t)kslice, wbar(b));
+    }
+  };
+  // The shared experts' units come first and need no routing: fetch them now.
+  int pre = 0;
+  while (pre < NB && unit_of(pre) < a.S * TILES) {
+    const int u = unit_of(pre);
+    issue_w(pre, a.E + u / TILES, u % TILES);
+    ++pre;
+  }
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(xbar, (uint32_t)(a.B * a.H * 2));
+    bulk_g2s(xstage, a.x, (uint32_t)(a.B * a.H * 2), xbar);
+  }
+  const bool okx = __syncthreads_and(mbar_wait(xbar, 0, status));
+  if (okx) {  // warp w prescales and reorders tokens w, w + nwarps, ...
+    for (int t = warp; t < a.B; t += blockDim.x >> 5) {
+      const uint8_t* src = xstage + (size_t)t * a.H * 2;
+      float mx = 0.f;
+      if (FMT == FLINT_MOE_NVFP4) {
+        for (int c = lane; c < a.H / 8; c += 32) {
+          const uint4 v = lds128(src + c * 16);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(w4[q])), fabsf(bf16hi(w4[q]))));
+        }
+        mx = warp_max(mx);
+      }
+      const int kx = FMT == FLINT_MOE_NVFP4 ? prescale_exp(mx) : 0;
+      const float sc = exp2i(kx);
+      uint8_t* dst = xs + (size_t)t * xstride;
+      for (int c = lane; c < a.H / 8; c += 32) {
+        const uint4 v = lds128(src + c * 16);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t bits = w4[q];
+          if (FMT == FLINT_MOE_NVFP4) {
+            const __half2 hv = __floats2half2_rn(bf16lo(w4[q]) * sc, bf16hi(w4[q]) * sc);
+            bits = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          *reinterpret_cast<uint32_t*>(dst + 2 * frag_offset_elems(8 * c + 2 * q)) = bits;
+        }
+      }
+      if (lane == 0) s_inv[t] = exp2i(-kx);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  FLINT_TRACE(a, 9);
+  compute_routing(a, R, blockIdx.x == 0, 21);  // its barriers also publish xs and s_inv
+  FLINT_TRACE(a, 10);
+  const int n_units = R.n_slots * TILES;
+  for (int jj = pre; jj < NB; ++jj) {
+    const int u = unit_of(jj);
+    if (u < n_units) issue_w(jj, R.slot_expert[u / TILES], u % TILES);
+  }
+  const float* glob = a.globals;
+  for (int jj = 0;; ++jj) {
+    const int u = unit_of(jj);
+    if (u >= n_units) break;  // the same for the 4 warps of the group
+    const int b = jj % NB;
+    const uint32_t par = (uint32_t)((jj / NB) & 1);
+    const int slot = u / TILES, tile = u % TILES;
+    const int expert = R.slot_expert[slot], off = R.slot_off[slot], T = R.slot_off[slot + 1] - off;
+    const int nt_used = (T + 7) >> 3;
+    float acc[2][NTMAX][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int nt = 0; nt < NTMAX; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
+    const bool ok = mbar_wait(wbar(b), par, status) && okx;
+    if (jj == 0) FLINT_TRACE(a, 11);
+    if (ok) {
+      int tok[NTMAX];
+#pragma unroll
+      for (int nt = 0; nt < NTMAX; ++nt) tok[nt] = R.row_tok[off + min(nt * 8 + g, T - 1)];
+      const uint8_t* wb = wbuf(b);
+#pragma unroll 4
+      for (int kl = 0; kl < KGW; ++kl) {
+        const int kg = gw * KGW + kl;
+        uint4 bx[NTMAX][2];
+#pragma unroll
+        for (int nt = 0; nt < NTMAX; ++nt) {
+          if (nt < nt_used) {  // columns past the slot's tokens repeat a valid row
+            const uint8_t* rp = xs + (size_t)tok[nt] * xstride + kg * 128 + t4 * 32;
+            bx[nt][0] = lds128(rp);
+            bx[nt][1] = lds128(rp + 16);
+          }
+        }
+        if (kl & 1)
+          tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[1]);
+        else
+          tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[0]);
+      }
+    } else {
+      mbar_drain(wbar(b), par);
+    }
+    float* rb = red + (jj & 1) * 3 * NTMAX * 128;
+    if (gw > 0) {
+#pragma unroll
+      for (int nt = 0; nt < NTMAX; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rb[((gw - 1) * NTMAX + nt) * 128 + lane * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
+    }
+    if (!group_sync_and(gi, ok)) {  // a copy timed out: let the next buffer's copies land, then stop
+      if (unit_of(jj + 1) < n_units && NB > 1) mbar_drain(wbar((jj + 1) % NB), (uint32_t)(((jj + 1) / NB) & 1));
+      break;
+    }
+    if (jj == 0) FLINT_TRACE(a, 12);
+    // This warp's weight slice is free again: fetch its slice of unit jj + NB.
+    {
+      const int u2 = unit_of(jj + NB);
+      if (u2 < n_units) issue_w(b, R.slot_expert[u2 / TILES], u2 % TILES);
+    }
+    if (gw != 0) continue;
+    float sum[NTMAX][4];
+#pragma unroll
+    for (int nt = 0; nt < NTMAX; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float v = acc[0][nt][i] + acc[1][nt][i];
+#pragma unroll
+        for (int w2 = 0; w2 < 3; ++w2) v += rb[(w2 * NTMAX + nt) * 128 + lane * 4 + i];
+        sum[nt][i] = v;
+      }
+    const float Gg = glob[expert * 4 + 0];
+    const float Gu = glob[expert * 4 + 1];
+    const int hoff = frag_offset_elems(tile * 8 + g);
+    uint16_t* h = ws_h(a);
+    unsigned* hmax = ws_hmax(a);
+#pragma unroll
+    for (int nt = 0; nt < NTMAX; ++nt) {
+      if (nt >= nt_used) break;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int n = nt * 8 + 2 * t4 + hh;
+        float hv = 0.f;
+        if (n < T) {
+          const float inv = s_inv[R.row_tok[off + n]];
+          const float gv = (sum[nt][hh] * inv) * Gg;
+          const float uv = (sum[nt][2 + hh] * inv) * Gu;
+          const float sv = gv / (1.0f + expf(-gv));
+          const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
+          h[(size_t)(off + n) * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hb);
+          hv = fabsf(__bfloat162float(hb));
+        }
+        hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 4));
+        hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 8));
+        hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 16));
+        if (g == 0 && n < T && hv > 0.f) atomicMax(hmax + off + n, __float_as_uint(hv));
+      }
+    }
+  }
+  FLINT_TRACE(a, 13);
+}
+
+// ===========================================================================
 // K3: down GEMV + routing-weighted combine for one tile of 16 output rows.
-// Work items are (slot, chunk of up to 8 of its rows); warp w takes items
-// w, w+4, ... in order, NBUF of them in flight; per-warp partial sums are
-// added in warp order at the end, so the result does not depend on timing.
+// Work items are (slot, chunk of up to 8 of its rows); warp w of nw takes
+// items w, w+nw, ... in order, NBUF of them in flight; per-warp partial sums
+// are added in warp order at the end, so the result does not depend on timing.
 // ===========================================================================
 struct DownSmemPlan {
   int buf_bytes, hrows, hstride;
-  size_t acc_off, off_off, rowtok_off, roww_off, items_off, inv_off, bar_off, total;
+  size_t acc_off, items_off, hmax_off, inv_off, bar_off, total;
 };
 
-__host__ __device__ inline DownSmemPlan down_plan(int H, int I, int B, int max_slots, int max_rows, int fmt, int nbuf) {
+__host__ __device__ inline DownSmemPlan down_plan(int H, int I, int B, int max_slots, int max_rows, int fmt, int nbuf,
+                                                  int nw) {
   DownSmemPlan p;
   const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
   p.hrows = B < 8 ? B : 8;
   p.hstride = I * 2 + 16;
   p.buf_bytes = (I / KG_COLS) * kgb + p.hrows * p.hstride;
-  size_t o = (size_t)4 * nbuf * p.buf_bytes;
-  p.acc_off = o;     o += sizeof(float) * 4 * B * 16;
-  p.off_off = o;     o += sizeof(int) * (max_slots + 1);
-  p.rowtok_off = o;  o += sizeof(int) * max_rows;
-  p.roww_off = o;    o += sizeof(float) * max_rows;
-  p.items_off = o;   o += sizeof(int) * (max_slots + max_rows / 8 + 8);
+  size_t o = (size_t)nw * nbuf * p.buf_bytes;
+  p.acc_off = o;    o += sizeof(float) * nw * B * 16;
+  p.items_off = o;  o += sizeof(int) * (max_slots + max_rows / 8 + 8);
+  p.hmax_off = o;   o += sizeof(float) * max_rows;
   o = (o + 15) & ~(size_t)15;
-  p.inv_off = o;     o += sizeof(float) * 4 * nbuf * 8;
+  p.inv_off = o;    o += sizeof(float) * nw * nbuf * 8;
   o = (o + 15) & ~(size_t)15;
-  p.bar_off = o;     o += sizeof(uint64_t) * 4 * nbuf;
+  p.bar_off = o;    o += sizeof(uint64_t) * nw * nbuf;
   p.total = o;
   return p;
 }
 
 template <int FMT, int NBUF>
-__global__ void __launch_bounds__(128) k_down(DecodeArgs a) {
+__global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ RouteSmem R;
+  __shared__ int s_wsum[MAX_WARPS];
   constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int nw = blockDim.x >> 5;
   const int tile = blockIdx.x;
-  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, a.W.max_rows, FMT, NBUF);
+  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, a.W.max_rows, FMT, NBUF, nw);
   const int dn_bytes = (int)a.L.dn_tile;
   float* acc_s = reinterpret_cast<float*>(smem + P.acc_off);
-  int* s_off = reinterpret_cast<int*>(smem + P.off_off);
-  int* s_rowtok = reinterpret_cast<int*>(smem + P.rowtok_off);
-  float* s_roww = reinterpret_cast<float*>(smem + P.roww_off);
   int* s_items = reinterpret_cast<int*>(smem + P.items_off);
+  float* s_hmax = reinterpret_cast<float*>(smem + P.hmax_off);
   float* s_inv = reinterpret_cast<float*>(smem + P.inv_off) + warp * NBUF * 8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off) + warp * NBUF;
   auto buf = [&](int b) { return smem + (size_t)(warp * NBUF + b) * P.buf_bytes; };
-  __shared__ int s_wsum[4];
+  int* status = ws_hdr(a) + HDR_STATUS;
 
+  FLINT_TRACE(a, 16);
   if (lane < NBUF) mbar_init(&bars[lane], 2);  // one arrival for the weights, one for the h rows
   fence_mbar_init();
-  for (int i = threadIdx.x; i < 4 * a.B * 16; i += blockDim.x) acc_s[i] = 0.f;
+  for (int i = threadIdx.x; i < nw * a.B * 16; i += blockDim.x) acc_s[i] = 0.f;
   __syncthreads();
 
-  // Items of the shared slots are known before routing: T = B for each.
-  const int cps = (a.B + 7) / 8;
-  int pre = 0;
-  for (int i = warp; i < a.S * cps && pre < NBUF; i += 4, ++pre) {
+  auto issue_weights = [&](int j, int expert) {
     if (lane == 0) {
-      const int s = i / cps;
-      const uint8_t* src = a.packed + (int64_t)(a.E + s) * a.L.expert_bytes + a.L.gu_bytes + (int64_t)tile * dn_bytes;
-      mbar_arrive_expect_tx(&bars[pre], (uint32_t)dn_bytes);
-      bulk_g2s(buf(pre), src, (uint32_t)dn_bytes, &bars[pre]);
+      const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + a.L.gu_bytes + (int64_t)tile * dn_bytes;
+      mbar_arrive_expect_tx(&bars[j % NBUF], (uint32_t)dn_bytes);
+      bulk_g2s(buf(j % NBUF), src, (uint32_t)dn_bytes, &bars[j % NBUF]);
     }
-  }
-  pdl_trigger();
-  pdl_wait();
+  };
+  // The shared experts' items come first and are known before routing (T = B).
+  const int cps = (a.B + 7) / 8;
+  int w_issued = 0;
+  for (int i = warp; i < a.S * cps && w_issued < NBUF; i += nw, ++w_issued) issue_weights(w_issued, a.E + i / cps);
 
-  int* hdr = ws_hdr(a);
-  int n_slots = __ldcg(hdr + HDR_NSLOTS);
-  int n_rows = __ldcg(hdr + HDR_NROWS);
-  if (n_slots < a.S || n_slots > a.W.max_slots || n_rows < 0 || n_rows > a.W.max_rows) {
-    if (threadIdx.x == 0) atomicOr(hdr + HDR_STATUS, FLINT_MOE_DEV_ERR_SLOTS);
-    for (int j = 0; j < pre; ++j) mbar_drain(&bars[j], 0);  // let pre-issued copies land, then stop
-    return;
-  }
-  for (int i = threadIdx.x; i <= n_slots; i += blockDim.x) s_off[i] = __ldcg(ws_slot_off(a) + i);
-  for (int i = threadIdx.x; i < n_rows; i += blockDim.x) {
-    s_rowtok[i] = __ldcg(ws_row_tok(a) + i);
-    s_roww[i] = __ldcg(ws_row_w(a) + i);
-  }
-  __syncthreads();
-  // Item list: slot s contributes ceil(T_s / 8) items; exclusive prefix over slots.
+  // k_gateup lets this kernel launch only after its own wait, so the router has
+  // finished: route now and fetch the routed down tiles while k_gateup runs.
+  compute_routing(a, R, false, -1);
+  FLINT_TRACE(a, 17);
   {
+    const int n_slots = R.n_slots;
     const int spt = (n_slots + blockDim.x - 1) / blockDim.x;
     const int s0 = threadIdx.x * spt;
     int local = 0;
-    for (int s = s0; s < s0 + spt && s < n_slots; ++s) local += (s_off[s + 1] - s_off[s] + 7) >> 3;
+    for (int s = s0; s < s0 + spt && s < n_slots; ++s) local += (R.slot_off[s + 1] - R.slot_off[s] + 7) >> 3;
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -571,64 +853,61 @@ __global__ void __launch_bounds__(128) k_down(DecodeArgs a) {
     int run = incl - local;
     for (int w2 = 0; w2 < warp; ++w2) run += s_wsum[w2];
     for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
-      const int nc = (s_off[s + 1] - s_off[s] + 7) >> 3;
+      const int nc = (R.slot_off[s + 1] - R.slot_off[s] + 7) >> 3;
       for (int c = 0; c < nc; ++c) s_items[run + c] = (s << 8) | c;
       run += nc;
     }
   }
   __syncthreads();
-  const int n_items = s_wsum[0] + s_wsum[1] + s_wsum[2] + s_wsum[3];
-  const int* slot_expert = ws_slot_expert(a);
+  int n_items = 0;
+  for (int w2 = 0; w2 < nw; ++w2) n_items += s_wsum[w2];
+  auto item_of = [&](int j, int& s, int& r0, int& Tc) {
+    const int it = s_items[warp + nw * j];
+    s = it >> 8;
+    r0 = R.slot_off[s] + 8 * (it & 0xFF);
+    Tc = min(8, R.slot_off[s + 1] - r0);
+  };
+  for (int j = w_issued; j < NBUF && warp + nw * j < n_items; ++j) {
+    int s, r0, Tc;
+    item_of(j, s, r0, Tc);
+    issue_weights(j, R.slot_expert[s]);
+  }
 
-  // Issue item j of this warp into buffer j % NBUF.
-  auto issue = [&](int j) {
-    const int item = warp + 4 * j;
-    if (item >= n_items) return;
-    const int s = s_items[item] >> 8, c = s_items[item] & 0xFF;
-    const int r0 = s_off[s] + 8 * c;
-    const int Tc = min(8, s_off[s + 1] - r0);
+  pdl_wait();  // h comes from k_gateup
+  pdl_trigger();
+  FLINT_TRACE(a, 18);
+
+  auto issue_h = [&](int j) {
+    int s, r0, Tc;
+    item_of(j, s, r0, Tc);
     const int b = j % NBUF;
-    if (lane == 0) {
-      if (j >= pre) {
-        int expert = __ldcg(slot_expert + s);
-        if (expert < 0 || expert >= a.E + a.S) {
-          atomicOr(hdr + HDR_STATUS, FLINT_MOE_DEV_ERR_SLOTS);
-          expert = 0;
-        }
-        const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + a.L.gu_bytes + (int64_t)tile * dn_bytes;
-        mbar_arrive_expect_tx(&bars[b], (uint32_t)dn_bytes);
-        bulk_g2s(buf(b), src, (uint32_t)dn_bytes, &bars[b]);
-      }
-      mbar_arrive_expect_tx(&bars[b], (uint32_t)(Tc * a.I * 2));
-    }
+    if (lane == 0) mbar_arrive_expect_tx(&bars[b], (uint32_t)(Tc * a.I * 2));
     __syncwarp();
     if (lane < Tc)
       bulk_g2s(buf(b) + dn_bytes + lane * P.hstride, ws_h(a) + (size_t)(r0 + lane) * a.I, (uint32_t)(a.I * 2),
                &bars[b]);
   };
-  for (int j = 0; j < NBUF; ++j) issue(j);
+  for (int j = 0; j < NBUF && warp + nw * j < n_items; ++j) issue_h(j);
+  for (int i = threadIdx.x; i < R.n_rows; i += blockDim.x) s_hmax[i] = __uint_as_float(__ldcg(ws_hmax(a) + i));
+  __syncthreads();
 
   const int KG = a.I / KG_COLS;
-  for (int j = 0;; ++j) {
-    const int item = warp + 4 * j;
-    if (item >= n_items) break;
-    const int s = s_items[item] >> 8, c = s_items[item] & 0xFF;
-    const int r0 = s_off[s] + 8 * c;
-    const int Tc = min(8, s_off[s + 1] - r0);
+  for (int j = 0; warp + nw * j < n_items; ++j) {
+    int s, r0, Tc;
+    item_of(j, s, r0, Tc);
     const int b = j % NBUF;
     const uint32_t parity = (uint32_t)((j / NBUF) & 1);
-    if (!mbar_wait(&bars[b], parity, hdr + HDR_STATUS)) {
-      // give every copy this warp has in flight a bounded chance to land
-      for (int jj = j; jj < j + NBUF && warp + 4 * jj < n_items; ++jj)
+    if (!mbar_wait(&bars[b], parity, status)) {
+      for (int jj = j; jj < j + NBUF && warp + nw * jj < n_items; ++jj)
         mbar_drain(&bars[jj % NBUF], (uint32_t)((jj / NBUF) & 1));
       break;
     }
+    if (j == 0) FLINT_TRACE(a, 19);
     uint8_t* wb = buf(b);
     uint8_t* hb = wb + dn_bytes;
     if (FMT == FLINT_MOE_NVFP4) {
       for (int n = 0; n < Tc; ++n) {
-        const float mx = __uint_as_float(__ldcg(ws_hmax(a) + r0 + n));
-        const int kh = prescale_exp(mx);
+        const int kh = prescale_exp(s_hmax[r0 + n]);
         const float sc = exp2i(kh);
         uint32_t* rowp = reinterpret_cast<uint32_t*>(hb + n * P.hstride);
         for (int q = lane; q < a.I / 2; q += 32) {
@@ -642,60 +921,54 @@ __global__ void __launch_bounds__(128) k_down(DecodeArgs a) {
       s_inv[b * 8 + lane] = 1.0f;
     }
     __syncwarp();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[2][1][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[c][0][i] = 0.f;
     const int nrow = g < Tc ? g : Tc - 1;
+#pragma unroll 4
     for (int kg = 0; kg < KG; ++kg) {
-      const uint8_t* kp = wb + kg * KGB;
       const uint8_t* rp = hb + nrow * P.hstride + kg * 128 + t4 * 32;
-      const uint4 b01 = lds128(rp), b23 = lds128(rp + 16);
-      if (FMT == FLINT_MOE_NVFP4) {
-        const uint4 codes = lds128(kp + lane * 16);
-        const uint32_t sg = lds32(kp + KG_CODE_BYTES + g * 4);
-        const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (g + 8) * 4);
-        const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          uint32_t af[4];
-          nvfp4_afrag(cw[ks], sg, sg8, ks, af);
-          const uint4& q = ks < 2 ? b01 : b23;
-          mma_f16(acc, af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint4 v = lds128(kp + lane * 64 + ks * 16);
-          const uint32_t af[4] = {v.x, v.y, v.z, v.w};
-          const uint4& q = ks < 2 ? b01 : b23;
-          mma_bf16(acc, af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
-        }
-      }
+      uint4 bx[1][2];
+      bx[0][0] = lds128(rp);
+      bx[0][1] = lds128(rp + 16);
+      if (kg & 1)
+        tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[1]);
+      else
+        tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
     }
-    const int expert = min(max(__ldcg(slot_expert + s), 0), a.E + a.S - 1);
-    const float Gd = a.globals[expert * 4 + 2];
+    const float Gd = a.globals[R.slot_expert[s] * 4 + 2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int n = 2 * t4 + hh;
       if (n < Tc) {
         const int row = r0 + n;
-        const int tok = min(max(s_rowtok[row], 0), a.B - 1);
-        const float wt = s_roww[row];
+        const int tok = R.row_tok[row];
+        const float wt = R.row_w[row];
         const float inv = s_inv[b * 8 + n];
         float* dst = acc_s + (warp * a.B + tok) * 16;
-        dst[g] += wt * ((acc[hh] * inv) * Gd);
-        dst[g + 8] += wt * ((acc[2 + hh] * inv) * Gd);
+        dst[g] += wt * (((acc[0][0][hh] + acc[1][0][hh]) * inv) * Gd);
+        dst[g + 8] += wt * (((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * inv) * Gd);
       }
     }
     __syncwarp();
-    issue(j + NBUF);
+    if (warp + nw * (j + NBUF) < n_items) {
+      int s2, r2, T2;
+      item_of(j + NBUF, s2, r2, T2);
+      issue_weights(j + NBUF, R.slot_expert[s2]);
+      issue_h(j + NBUF);
+    }
   }
   __syncthreads();
   for (int p = threadIdx.x; p < a.B * 16; p += blockDim.x) {
     const int t = p >> 4, r = p & 15;
-    const float v = acc_s[(0 * a.B + t) * 16 + r] + acc_s[(1 * a.B + t) * 16 + r] + acc_s[(2 * a.B + t) * 16 + r] +
-                    acc_s[(3 * a.B + t) * 16 + r];
+    float v = 0.f;
+    for (int w2 = 0; w2 < nw; ++w2) v += acc_s[(w2 * a.B + t) * 16 + r];
     const __nv_bfloat16 o = __float2bfloat16_rn(v);
     a.out[(size_t)t * a.H + tile * 16 + r] = *reinterpret_cast<const uint16_t*>(&o);
   }
+  FLINT_TRACE(a, 20);
 }
 
 }  // namespace flint
@@ -710,17 +983,33 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 constexpr int DOWN_NBUF = 2;
+constexpr size_t SMEM_LIMIT = 227 * 1024;
 
-size_t gateup_smem(int H, int B, int fmt, int ntmax) {
-  const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
-  return (size_t)4 * (H / 256) * kgb + (size_t)B * (H * 2 + 16) + sizeof(float) * (3 * ntmax * 128 + MAX_BATCH) +
-         sizeof(uint64_t) * 4;
+// 8 warps keep more down tiles in flight for small batches; larger batches and
+// BF16 tiles (16 KB each) need the shared memory for fewer, deeper buffers.
+int down_warps(int B, int fmt) { return (B <= 4 && fmt == FLINT_MOE_NVFP4) ? 8 : 4; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n < 1)
+    n = 148;
+  return n;
 }
 
 template <typename K>
 cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const DecodeArgs& a) {
-  if (smem > 48 * 1024) {
+  if (smem > 48 * 1024 - sizeof(RouteSmem)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  // Every decode kernel asks for the largest shared-memory carveout: an SM runs
+  // blocks of different kernels side by side only under one carveout, and the
+  // early (programmatic) launch of the next kernel is only useful if its blocks
+  // can be resident while the current kernel's blocks still run.
+  {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -736,23 +1025,53 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+// Warp groups (ng) and buffers per group (nb) of k_gateup: as many units in
+// flight as fit, and for small batches a footprint that leaves room on each SM
+// for a k_down block, which launches early and prefetches meanwhile.
+void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) {
+  const size_t route = sizeof(RouteSmem) + 1024;
+  const int ntmax = (B + 7) / 8;
+  const size_t budget = B <= 2 ? 110 * 1024 : SMEM_LIMIT;
+  const int want_nb = units_per_block <= GU_MAX_GROUPS ? 1 : 2;
+  const int cand[][2] = {{3, want_nb}, {3, 1}, {2, 2}, {2, 1}, {1, 3}, {1, 2}, {1, 1}};
+  for (const auto& c : cand) {
+    if (gateup_plan(H, B, fmt, ntmax, c[0], c[1]).total + route <= budget) {
+      ng = c[0];
+      nb = c[1];
+      return;
+    }
+  }
+  for (const auto& c : cand) {
+    if (gateup_plan(H, B, fmt, ntmax, c[0], c[1]).total + route <= SMEM_LIMIT) {
+      ng = c[0];
+      nb = c[1];
+      return;
+    }
+  }
+  ng = 0;
+  nb = 0;
+}
+
 template <int FMT>
-cudaError_t launch_gateup(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_gateup(const DecodeArgs& a, cudaStream_t stream, int ng) {
   const int ntmax = (a.B + 7) / 8;
-  const dim3 grid(a.I / 8, a.S + (a.E < a.B * a.k ? a.E : a.B * a.k));
-  const size_t smem = gateup_smem(a.H, a.B, FMT, ntmax);
+  const size_t smem = gateup_plan(a.H, a.B, FMT, ntmax, ng, a.gu_nb).total;
+  const int units = a.W.max_slots * (a.I / 8);
+  const int blocks = units < sm_count() ? units : sm_count();
+  const dim3 block(128 * ng);
   switch (ntmax) {
-    case 1: return launch_pdl(k_gateup<FMT, 1>, grid, dim3(128), smem, stream, a);
-    case 2: return launch_pdl(k_gateup<FMT, 2>, grid, dim3(128), smem, stream, a);
-    case 3: return launch_pdl(k_gateup<FMT, 3>, grid, dim3(128), smem, stream, a);
-    default: return launch_pdl(k_gateup<FMT, 4>, grid, dim3(128), smem, stream, a);
+    case 1: return launch_pdl(k_gateup<FMT, 1>, dim3(blocks), block, smem, stream, a);
+    case 2: return launch_pdl(k_gateup<FMT, 2>, dim3(blocks), block, smem, stream, a);
+    case 3: return launch_pdl(k_gateup<FMT, 3>, dim3(blocks), block, smem, stream, a);
+    default: return launch_pdl(k_gateup<FMT, 4>, dim3(blocks), block, smem, stream, a);
   }
 }
 
 template <int FMT>
 cudaError_t launch_down(const DecodeArgs& a, cudaStream_t stream) {
-  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, a.W.max_rows, FMT, DOWN_NBUF);
-  return launch_pdl(k_down<FMT, DOWN_NBUF>, dim3(a.H / 16), dim3(128), P.total, stream, a);
+  const int nw = down_warps(a.B, FMT);
+  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, a.W.max_rows, FMT, DOWN_NBUF, nw);
+  return launch_pdl(k_down<FMT, DOWN_NBUF>, dim3(a.H / 16), dim3(32 * nw), P.total, stream, a);
 }
 
 cudaError_t launch_router(const DecodeArgs& a, cudaStream_t stream) {
@@ -776,7 +1095,7 @@ cudaError_t launch_router(const DecodeArgs& a, cudaStream_t stream) {
 
 extern "C" size_t flint_moe_workspace_bytes(const flint_moe_config* c, int32_t max_batch) {
   if (flint_moe_check_config(c) != FLINT_MOE_OK || max_batch < 1 || max_batch > MAX_BATCH) return 0;
-  return make_ws_layout(c->num_experts, c->top_k, c->inter, c->n_shared, max_batch).total;
+  return make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, max_batch).total;
 }
 
 extern "C" flint_moe_status flint_moe_workspace_init(const flint_moe_config* c, int32_t max_batch, void* ws,
@@ -832,25 +1151,66 @@ extern "C" flint_moe_status flint_moe_decode(const flint_moe_layer* layer, const
   a.ws = static_cast<uint8_t*>(ws);
   // The workspace is laid out for the batch of this call; callers size it for
   // their largest batch, which is at least as large.
-  a.W = make_ws_layout(a.E, a.k, a.I, a.S, B);
-  constexpr size_t SMEM_LIMIT = 227 * 1024;
-  if (gateup_smem(a.H, B, a.fmt, (B + 7) / 8) > SMEM_LIMIT ||
-      down_plan(a.H, a.I, B, a.W.max_slots, a.W.max_rows, a.fmt, DOWN_NBUF).total > SMEM_LIMIT ||
+  a.W = make_ws_layout(a.H, a.E, a.k, a.I, a.S, B);
+#ifdef FLINT_MOE_TRACE
+  static std::atomic<int> trace_calls{0};
+  a.trace_seq = trace_calls.fetch_add(1);
+#else
+  a.trace_seq = 0;
+#endif
+  const size_t route_smem = sizeof(RouteSmem) + 64;
+  int gu_ng = 0;
+  {
+    const int units = a.W.max_slots * (a.I / 8), sms = sm_count();
+    gateup_shape(a.H, B, a.fmt, (units + sms - 1) / sms, gu_ng, a.gu_nb);
+  }
+  if (gu_ng == 0 ||
+      down_plan(a.H, a.I, B, a.W.max_slots, a.W.max_rows, a.fmt, DOWN_NBUF, down_warps(B, a.fmt)).total + route_smem >
+          SMEM_LIMIT ||
       (size_t)(B < 8 ? B : 8) * a.H * 2 > SMEM_LIMIT - 16 * 1024)
     return FLINT_MOE_EUNSUPPORTED;
   cudaError_t e = launch_router(a, stream);
-  if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_gateup<FLINT_MOE_NVFP4>(a, stream)
-                                                       : launch_gateup<FLINT_MOE_BF16>(a, stream);
+  if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_gateup<FLINT_MOE_NVFP4>(a, stream, gu_ng)
+                                                       : launch_gateup<FLINT_MOE_BF16>(a, stream, gu_ng);
   if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_down<FLINT_MOE_NVFP4>(a, stream)
                                                        : launch_down<FLINT_MOE_BF16>(a, stream);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
+}
+
+extern "C" flint_moe_status flint_moe_trace(int32_t op, uint64_t* host_events, cudaStream_t stream) {
+#ifdef FLINT_MOE_TRACE
+  if (op == 0) {
+    static unsigned long long init[TRACE_CALLS][TRACE_EVENTS][2];
+    for (int c = 0; c < TRACE_CALLS; ++c)
+      for (int e = 0; e < TRACE_EVENTS; ++e) {
+        init[c][e][0] = ~0ull;
+        init[c][e][1] = 0ull;
+      }
+    return cudaMemcpyToSymbolAsync(g_trace, init, sizeof(init), 0, cudaMemcpyHostToDevice, stream) == cudaSuccess
+               ? FLINT_MOE_OK
+               : FLINT_MOE_ECUDA;
+  }
+  if (op == 1 && host_events) {
+    if (cudaMemcpyFromSymbolAsync(host_events, g_trace, sizeof(g_trace), 0, cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+      return FLINT_MOE_ECUDA;
+    return FLINT_MOE_OK;
+  }
+  return FLINT_MOE_EINVAL;
+#else
+  (void)op;
+  (void)host_events;
+  (void)stream;
+  return FLINT_MOE_EUNSUPPORTED;
+#endif
 }
 
 extern "C" flint_moe_status flint_moe_debug_routing(const flint_moe_config* c, const void* ws, int32_t B,
                                                     int32_t* idx, float* w, cudaStream_t stream) {
   if (flint_moe_check_config(c) != FLINT_MOE_OK || !ws || !idx || !w || B < 1 || B > MAX_BATCH)
     return FLINT_MOE_EINVAL;
-  const WsLayout W = make_ws_layout(c->num_experts, c->top_k, c->inter, c->n_shared, B);
+  const WsLayout W = make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, B);
   const uint8_t* base = static_cast<const uint8_t*>(ws);
   const size_t n = (size_t)B * c->top_k;
   if (cudaMemcpyAsync(idx, base + W.topk_idx, n * sizeof(int), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
@@ -916,7 +1276,8 @@ extern "C" flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* laye
   if (st != FLINT_MOE_OK) return st;
   if (B < 0 || B > MAX_BATCH) return FLINT_MOE_EINVAL;
   if (B == 0) return FLINT_MOE_OK;
-  if (make_ws_layout(c->num_experts, c->top_k, c->inter, c->n_shared, B).total > FLINT_MOE_NOALLOC_SCRATCH_BYTES)
+  if (make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, B).total >
+      FLINT_MOE_NOALLOC_SCRATCH_BYTES)
     return FLINT_MOE_EUNSUPPORTED;
   void* scratch = nullptr;
   const flint_moe_status sst = noalloc_scratch(&scratch);
