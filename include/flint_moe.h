@@ -162,12 +162,13 @@ flint_moe_status flint_moe_layer_init(const flint_moe_config* cfg, const void* p
 /* One decode step of the MoE layer for B tokens (0 <= B <= 32; B = 0 is a
  * no-op). x: bf16 [B][H]; out: bf16 [B][H]; workspace: flint_moe_workspace_bytes
  * (cfg, >= B) bytes, initialised once with flint_moe_workspace_init, not shared
- * by decodes in flight at the same time. Three kernels: router + sigmoid +
- * top-k (last block builds the distinct-expert slots), gate/up GEMV with
- * SiLU*up over the selected and shared experts, down GEMV with the
- * routing-weighted combine. They are chained with programmatic dependent
- * launch, so each loads its routing-independent weights (the shared expert,
- * the router) while the previous kernel, or the previous layer, still runs.
+ * by decodes in flight at the same time. Three kernels: the router GEMV
+ * (logits); gate/up GEMV with SiLU*up over the selected and shared experts;
+ * down GEMV with the routing-weighted combine. Every block of the last two
+ * computes the sigmoid top-k it needs from the logits itself. They are
+ * chained with programmatic dependent launch, so each loads its
+ * routing-independent weights (the shared expert, the router) while the
+ * previous kernel, or the previous layer, still runs.
  * x and out must not overlap. Sections "Model architecture" and "Optimisation"
  * of "Day-0 Support for Flint on vLLM". */
 flint_moe_status flint_moe_decode(const flint_moe_layer* layer, const uint16_t* x_bf16,
@@ -193,11 +194,19 @@ flint_moe_status flint_moe_debug_dequant(const flint_moe_config* cfg, const void
  * %globaltimer (ns) over all blocks, and SYNCHRONISE the stream. Call n of
  * flint_moe_decode records into slot n % 64. Events: router start 0, after
  * its wait 1, x arrived 2, end 3; gate/up start 8, after its wait 9, routed
- * 10, operands arrived 11, products done 12, end 13, routing scan done 14,
- * routing rows done 15, logits loaded 21, top-k selected 22, top-k written
- * 23; down start 16, routed 17, after its wait 18, first item ready 19,
- * end 20. */
+ * 10, operands arrived 11, products done 12, end 13, routing published to
+ * the block 14, keys sorted 21, top-k selected 22, top-k written 23; down
+ * start 16, routed 17, after its wait 18, first item ready 19, end 20. */
 flint_moe_status flint_moe_trace(int32_t op, uint64_t* host_events, cudaStream_t stream);
+
+/* Self-check of the reciprocal the routing sigmoid uses (the hardware
+ * approximation refined by one Newton-Raphson step): compares it, bit for bit,
+ * with the IEEE quotient 1.0f / y for every FP32 y whose bit pattern lies in
+ * [lo_bits, hi_bits) with 1 <= y < 2^125, and writes the number of
+ * mismatches to *host_mismatches. SYNCHRONISES the stream. Returns
+ * FLINT_MOE_EINVAL for a range outside [1, 2^125). */
+flint_moe_status flint_moe_debug_rcp_check(uint32_t lo_bits, uint32_t hi_bits,
+                                           uint64_t* host_mismatches, cudaStream_t stream);
 
 /* Reads the workspace status word into *host_status and clears it.
  * SYNCHRONISES the stream. Returns FLINT_MOE_ETIMEOUT if the timeout bit
@@ -206,14 +215,14 @@ flint_moe_status flint_moe_read_status(const void* workspace, int32_t* host_stat
                                        cudaStream_t stream);
 
 /* Bytes of the scratch array behind flint_moe_decode_noalloc. */
-#define FLINT_MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define FLINT_MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 /* flint_moe_decode for callers that cannot allocate device memory for a
  * workspace: a plugin whose host application owns every device allocation and
  * offers it no allocator, or a latency-critical loop in which cudaMalloc and
  * cudaFree could synchronise the device. No counterpart on the pages: it is a
  * variant of flint_moe_decode with the same arguments minus the workspace.
- * The scratch is one array of FLINT_MOE_NOALLOC_SCRATCH_BYTES bytes (1 MiB)
+ * The scratch is one array of FLINT_MOE_NOALLOC_SCRATCH_BYTES bytes (8 MiB)
  * in this library's device memory, held by every GPU that loads the library
  * until the process exits. It allocates nothing and calls no allocating
  * routine. The first call on a device looks up the array's device address
@@ -223,7 +232,7 @@ flint_moe_status flint_moe_read_status(const void* workspace, int32_t* host_stat
  * other threads) race on the array: serialise them. Returns
  * FLINT_MOE_EUNSUPPORTED when the workspace this shape and batch need
  * (flint_moe_workspace_bytes) exceeds FLINT_MOE_NOALLOC_SCRATCH_BYTES (the
- * Flint-shape layer needs 0.25 MiB at B = 32). Device status bits are not
+ * Flint-shape layer needs 6.1 MiB at B = 32, 0.39 MiB at B = 8). Device status bits are not
  * reported; use flint_moe_decode with a workspace to read them. */
 flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* layer, const uint16_t* x_bf16,
                                           int32_t B, uint16_t* out_bf16, cudaStream_t stream);

@@ -190,6 +190,38 @@ def test_decode_selection_bias():
     assert all(set(routing.idx[t]) == {2, 9} for t in range(4))
 
 
+@pytest.mark.parametrize("E,k,B,seed", [(512, 4, 12, 12), (300, 3, 10, 13), (100, 5, 9, 14)])
+def test_decode_expert_counts_off_the_flint_shape(E, k, B, seed):
+    """More experts than one warp's 8-per-lane top-k holds (E > 256: the
+    16-per-lane path), a count that is not a multiple of 32, and one that leaves
+    the last lanes partly empty; B > 8 puts tokens on every warp of a block."""
+    run_parity(dict(TINY, num_experts=E, top_k=k), B, seed)
+
+
+def test_decode_exact_key_ties_go_to_the_lower_index():
+    """A selection bias of 2^24 makes the keys of experts 3, 5, 9, 12 exactly
+    equal in FP32 (2^24 + s rounds to 2^24 for every score s in (0, 1)), so the
+    top-2 is decided by the index alone: experts 3 and 5, in that order, for
+    every token. The pass rules exclude such tokens from the oracle comparison
+    (their gap is 0), so the choice is checked here against the definition."""
+    bias = np.zeros(16, np.float32)
+    bias[[12, 5, 9, 3]] = 2.0 ** 24
+    cfg = cfg_of(TINY)
+    dl = layers.synth_layer(cfg, 15, 0, DEV, bias=torch.from_numpy(bias).to(DEV))
+    x, out, idx, w = gpu_decode(cfg, dl, 6, 15, 0)
+    assert (idx == np.array([3, 5], np.int32)[None, :]).all()
+    xo, router = oracle_inputs(TINY, 15, 0, 6)
+    routing = moe.route(xo, router, oracle_config(TINY), bias)
+    assert (routing.idx == np.array([3, 5])[None, :]).all()
+    np.testing.assert_allclose(w, routing.w, rtol=0, atol=1e-6)
+
+
+def test_routing_reciprocal_is_the_ieee_quotient():
+    """The sigmoid's reciprocal (hardware approximation plus one Newton-Raphson
+    step) equals the IEEE quotient 1.0f / y for every FP32 y in [1, 2^125)."""
+    assert fb.flint_moe_debug_rcp_check(0x3F800000, (127 + 125) << 23) == 0
+
+
 def test_decode_batch0_is_a_noop():
     cfg = cfg_of(TINY)
     dl = layers.synth_layer(cfg, 0, 0, DEV)

@@ -81,8 +81,10 @@ def test_workspace_bytes(lib):
     assert fb.flint_moe_workspace_bytes(c, 33) == 0
     w1, w8, w32 = (fb.flint_moe_workspace_bytes(c, b) for b in (1, 8, 32))
     assert 0 < w1 < w8 < w32
-    # the bf16 h rows dominate: one per (token, selected or shared expert)
-    assert w32 >= 32 * 7 * 512 * 2
+    # the bf16 h rows dominate: every slot (the shared expert and up to B * k
+    # distinct selected experts) owns one row per token
+    assert w32 >= (1 + min(256, 32 * 6)) * 32 * 512 * 2
+    assert w32 <= fb.lib().flint_moe_workspace_bytes(ctypes.byref(c), 32)  # same call through ctypes
 
 
 def test_decode_rejects_bad_arguments_on_the_host(lib):
@@ -102,6 +104,15 @@ def test_decode_rejects_bad_arguments_on_the_host(lib):
     assert L.flint_moe_decode(None, x, 1, out, ws, None) == fb.EINVAL
     layer.cfg.hidden = 300
     assert L.flint_moe_decode(ctypes.byref(layer), x, 1, out, ws, None) == fb.EUNSUPPORTED
+
+
+def test_rcp_check_rejects_ranges_outside_its_domain(lib):
+    n = ctypes.c_uint64(7)
+    L = fb.lib()
+    assert L.flint_moe_debug_rcp_check(0x3F7FFFFF, 0x3F800010, ctypes.byref(n), None) == fb.EINVAL  # below 1.0
+    assert L.flint_moe_debug_rcp_check(0x3F800000, ((127 + 125) << 23) + 1, ctypes.byref(n), None) == fb.EINVAL
+    assert L.flint_moe_debug_rcp_check(0x3F800010, 0x3F800000, ctypes.byref(n), None) == fb.EINVAL
+    assert L.flint_moe_debug_rcp_check(0x3F800000, 0x3F800010, None, None) == fb.EINVAL
 
 
 def test_layer_init_and_pack_validate(lib):

@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
             "flint_moe_debug_dequant": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
             "flint_moe_read_status": (c_int32, [c_void_p, P(c_int32), c_void_p]),
             "flint_moe_trace": (c_int32, [c_int32, c_void_p, c_void_p]),
+            "flint_moe_debug_rcp_check": (c_int32, [ctypes.c_uint32, ctypes.c_uint32, P(ctypes.c_uint64), c_void_p]),
             "flint_moe_quantize_nvfp4": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                                    c_void_p]),
             "flint_synth_stream_key": (ctypes.c_uint64, [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
@@ -176,7 +177,7 @@ def flint_moe_decode(layer: flint_moe_layer, x, B: int, out, workspace, stream=N
 
 
 def flint_moe_decode_noalloc(layer: flint_moe_layer, x, B: int, out, stream=None) -> None:
-    """flint_moe_decode with the library's own 1 MiB device scratch array in
+    """flint_moe_decode with the library's own 8 MiB device scratch array in
     place of a workspace, for callers that cannot allocate device memory."""
     _check("flint_moe_decode_noalloc", lib().flint_moe_decode_noalloc(ctypes.byref(layer), _ptr(x), B, _ptr(out),
                                                                       _stream(stream)))
@@ -210,6 +211,15 @@ def flint_moe_trace(op: int, stream=None):
     st = lib().flint_moe_trace(op, None if buf is None else buf.ctypes.data, _stream(stream))
     _check("flint_moe_trace", st)
     return buf
+
+
+def flint_moe_debug_rcp_check(lo_bits: int, hi_bits: int, stream=None) -> int:
+    """Mismatches between the routing reciprocal and IEEE 1.0f / y over the FP32
+    bit patterns [lo_bits, hi_bits) (within [1, 2^125)); synchronises."""
+    n = ctypes.c_uint64(0)
+    _check("flint_moe_debug_rcp_check", lib().flint_moe_debug_rcp_check(lo_bits, hi_bits, ctypes.byref(n),
+                                                                        _stream(stream)))
+    return n.value
 
 
 def flint_moe_quantize_nvfp4(w, n_mat, rows, cols, codes, scales, global_, stream=None) -> None:

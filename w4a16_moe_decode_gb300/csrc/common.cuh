@@ -68,12 +68,10 @@ __host__ __device__ inline Layout make_layout(int H, int I, int E, int S, int fm
 // ---------------------------------------------------------------------------
 enum : int { HDR_COUNTER = 0, HDR_STATUS = 1, HDR_NSLOTS = 2, HDR_NROWS = 3, HDR_BATCH = 4 };
 
-constexpr int MAX_SLOTS = MAX_SHARED + MAX_EXPERTS;
-constexpr int MAX_ROWS = MAX_BATCH * (MAX_TOPK + MAX_SHARED);
-
 // Regions: router logits [B][E]; the routing of the last decode ([B][k]
 // indices and weights, for read-back); the largest |h| per (slot, token) row;
-// h in bf16 [rows][I] in fragment order.
+// h in bf16 [rows][I] in fragment order. Slot s (shared experts first, then
+// the distinct selected experts in ascending id) owns rows s * B .. s * B + B - 1.
 struct WsLayout {
   size_t logits, topk_idx, topk_w, hmax, h, total;
   int max_slots, max_rows;
@@ -84,7 +82,7 @@ __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~(size
 __host__ __device__ inline WsLayout make_ws_layout(int H, int E, int k, int I, int S, int maxB) {
   WsLayout W;
   W.max_slots = S + (E < maxB * k ? E : maxB * k);
-  W.max_rows = maxB * (k + S);
+  W.max_rows = W.max_slots * maxB;
   size_t o = 256;
   W.logits = o;   o = ws_align(o + sizeof(float) * maxB * E);
   W.topk_idx = o; o = ws_align(o + sizeof(int) * maxB * k);
@@ -112,6 +110,10 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's earlier shared-memory accesses before later bulk-copy
+// (async proxy) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                : "memory");
@@ -124,6 +126,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// The same for data read once per decode (expert weights): an L2 evict-first
+// policy, so the weight stream does not push out what the next kernels reuse
+// (logits, h, activations, router rows, code).
+__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n\t}"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
 

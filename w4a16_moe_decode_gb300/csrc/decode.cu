@@ -95,23 +95,33 @@ __device__ __forceinline__ float dot8_bf16(const uint4 w, const uint4 x, float a
 // every block that needs it from the logits in the workspace; the result is
 // a deterministic function of the logits, so all blocks agree.
 // ===========================================================================
-constexpr int MAX_WARPS = 8;
+constexpr int MAX_WARPS = 16;
+constexpr int USED_WORDS = MAX_EXPERTS / 32;
 
+// Routing result in shared memory. Slots are the S shared experts, then the
+// distinct selected experts in ascending id; slot s holds all B token rows
+// s * B .. s * B + B - 1 of h (a token that did not select the expert has a
+// row that is computed and never combined). So a consumer needs no prefix
+// sums: the r-th selected expert is the r-th set bit of `used`, and the tokens
+// of expert e are the bits of mask[e].
 struct __align__(16) RouteSmem {
-  int idx[MAX_BATCH * MAX_TOPK];  // per token, in (key desc, index asc) order
+  uint32_t mask[MAX_EXPERTS];       // bit t: token t selected expert e
+  uint32_t used[USED_WORDS];        // bit e % 32 of word e / 32: some token selected e
+  int idx[MAX_BATCH * MAX_TOPK];    // full routing only: per token, (key desc, index asc)
   float w[MAX_BATCH * MAX_TOPK];
-  uint32_t mask[MAX_EXPERTS];     // token bitmask per expert
-  int rowoff[MAX_EXPERTS];        // first row of a used expert's token list
-  int slot_expert[MAX_SLOTS];
-  int slot_off[MAX_SLOTS + 1];
-  int row_tok[MAX_ROWS];
-  float row_w[MAX_ROWS];
-  int sel_e[MAX_WARPS][MAX_TOPK];  // per warp: the winners of the current token
+  int sel_e[MAX_WARPS][MAX_TOPK];   // per warp scratch for the token being routed
   float sel_l[MAX_WARPS][MAX_TOPK];
   float sel_s[MAX_WARPS][MAX_TOPK];
   float sel_k[MAX_WARPS][MAX_TOPK];
-  int n_slots, n_rows;
 };
+static_assert(offsetof(RouteSmem, used) % 16 == 0, "slot_info reads `used` 16 bytes at a time");
+
+// Clears the selection bitmaps; the caller synchronises the block afterwards.
+// Needs nothing from the previous kernel, so it runs before the dependency wait.
+__device__ __forceinline__ void route_clear(RouteSmem& R, int E) {
+  for (int i = threadIdx.x; i < E; i += blockDim.x) R.mask[i] = 0u;
+  if (threadIdx.x < USED_WORDS) R.used[threadIdx.x] = 0u;
+}
 
 // Order-preserving map of a float key to an unsigned integer; 0 means "none".
 __device__ __forceinline__ uint32_t ordered_key(float f) {
@@ -119,7 +129,65 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-__device__ __forceinline__ float sigmoid_f32(float l) { return 1.0f / (1.0f + expf(-l)); }
+// Inverse of ordered_key.
+__device__ __forceinline__ float unordered_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// 1 / y rounded to nearest for y in [1, 2^125): the hardware approximation
+// (max error 1 ulp) refined by one Newton-Raphson step r + r (1 - y r) with
+// fused multiply-adds. An exhaustive GPU check over every FP32 y in that range
+// found it equal, bit for bit, to the IEEE quotient 1.0f / y, at a fraction of
+// the division's cost (no slow-path branch, so eight of them interleave).
+__device__ __forceinline__ float rcp_nr(float y) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+  return fmaf(r, fmaf(-y, r, 1.0f), r);
+}
+constexpr float RCP_NR_MAX = 0x1p125f;
+
+// The IEEE quotient 1 / y, out of line, for values outside rcp_nr's range:
+// the common path then carries none of the division's code.
+__device__ __noinline__ float rcp_ieee(float y) { return 1.0f / y; }
+
+// Routing score 1 / (1 + e^-l) in FP32: the IEEE quotient, computed through
+// rcp_nr except for l below about -86.6 (y >= 2^125) or NaN.
+__device__ __forceinline__ float sigmoid_f32(float l) {
+  const float y = 1.0f + expf(-l);
+  return y < RCP_NR_MAX ? rcp_nr(y) : 1.0f / y;
+}
+
+// Key of expert e: sigmoid of its logit plus its selection bias, in FP32.
+__device__ __forceinline__ float route_key(float l, const float* bias, int e) {
+  const float s = sigmoid_f32(l);
+  return bias ? s + __ldg(bias + e) : s;
+}
+
+// Publishes one token's k winners (lanes 0..k-1 hold my_e) and, for full
+// routing, their renormalised weights in (key desc, index asc) order. Lane r
+// holds the r-th winner in selection order, which is (key desc, index asc).
+__device__ __forceinline__ void route_publish(const DecodeArgs& a, RouteSmem& R, int t, int lane, int my_e, float s,
+                                              bool full, bool write_debug) {
+  const bool act = lane < a.k;
+  if (act) {
+    atomicOr(&R.mask[my_e], 1u << t);
+    atomicOr(&R.used[my_e >> 5], 1u << (my_e & 31));
+  }
+  if (!full) return;
+  // Sum of the k scores in selection order (a fixed order: deterministic).
+  float ssum = 0.f;
+  for (int q = 0; q < a.k; ++q) ssum += __shfl_sync(0xffffffffu, s, q);
+  if (act) {
+    float w = a.renorm ? s / ssum : s;
+    w *= a.routed_scale;
+    R.idx[t * a.k + lane] = my_e;
+    R.w[t * a.k + lane] = w;
+    if (write_debug) {
+      ws_topk_idx(a)[t * a.k + lane] = my_e;
+      ws_topk_w(a)[t * a.k + lane] = w;
+    }
+  }
+}
 
 // Arg-max of two (key, index) pairs whose indices increase left to right: the
 // right one wins only when strictly greater, so equal keys keep the lower index.
@@ -129,33 +197,21 @@ __device__ __forceinline__ void argmax2(uint32_t k0, int j0, uint32_t k1, int j1
   j = hi ? j1 : j0;
 }
 
-// Top-k of one token by one warp, any E <= 512. Lane l holds experts l, l+32,
-// ... Without a selection bias the selection runs on the logits (the sigmoid
-// is monotone); the k winners are then ordered by (sigmoid + bias) descending,
-// ties to the lower expert index.
-__device__ void topk_token_wide(const DecodeArgs& a, int t, int warp, int lane, RouteSmem& R, bool write_debug,
-                                int tb) {
+// Top-k of one token by one warp, any E <= 512: lane l holds experts l, l+32,
+// ...; k rounds of a 16-key arg-max tree and two warp reductions.
+__device__ void topk_token_wide(const DecodeArgs& a, int t, int warp, int lane, RouteSmem& R, bool full,
+                                bool write_debug, int tb, const float* logits) {
   constexpr int EPL = MAX_EXPERTS / 32;
   static_assert(EPL == 16, "the arg-max tree below is written for 16 keys per lane");
-  const float* lg = ws_logits(a) + (size_t)t * a.E;
-  const bool biased = a.bias != nullptr;
-  float lv[EPL], bv[EPL];
-  // Every load is issued before any is used, so they are in flight together.
+  const float* lg = logits + (size_t)t * a.E;
+  float lv[EPL];
 #pragma unroll
-  for (int j = 0; j < EPL; ++j) {
-    lv[j] = 0.f;
-    bv[j] = 0.f;
-    if (32 * j < a.E) {
-      const int e = min(lane + 32 * j, a.E - 1);
-      lv[j] = __ldcg(lg + e);
-      if (biased) bv[j] = __ldg(a.bias + e);
-    }
-  }
+  for (int j = 0; j < EPL; ++j) lv[j] = 32 * j < a.E ? __ldcg(lg + min(lane + 32 * j, a.E - 1)) : 0.f;
   uint32_t key[EPL];
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int e = lane + 32 * j;
-    key[j] = e < a.E ? ordered_key(biased ? sigmoid_f32(lv[j]) + bv[j] : lv[j]) : 0u;
+    key[j] = e < a.E ? ordered_key(route_key(lv[j], a.bias, e)) : 0u;
   }
   if (t == 0) FLINT_TRACE(a, tb);
   for (int r = 0; r < a.k; ++r) {
@@ -191,42 +247,11 @@ __device__ void topk_token_wide(const DecodeArgs& a, int t, int warp, int lane, 
   __syncwarp();
   if (t == 0) FLINT_TRACE(a, tb < 0 ? -1 : tb + 1);
   const bool act = lane < a.k;
-  int my_e = 0;
-  float s = 0.f, kf = 0.f;
-  if (act) {
-    my_e = R.sel_e[warp][lane];
-    s = sigmoid_f32(R.sel_l[warp][lane]);
-    kf = biased ? s + __ldg(a.bias + my_e) : s;
-    R.sel_s[warp][lane] = s;
-    R.sel_k[warp][lane] = kf;
-  }
-  __syncwarp();
-  if (act) {
-    int rank = 0;
-    float ssum = 0.f;
-    for (int q = 0; q < a.k; ++q) {
-      const float kq = R.sel_k[warp][q];
-      const int eq = R.sel_e[warp][q];
-      ssum += R.sel_s[warp][q];  // selection order, the same in every lane and block
-      rank += (kq > kf || (kq == kf && eq < my_e)) ? 1 : 0;
-    }
-    float w = a.renorm ? s / ssum : s;
-    w *= a.routed_scale;
-    R.idx[t * a.k + rank] = my_e;
-    R.w[t * a.k + rank] = w;
-    atomicOr(&R.mask[my_e], 1u << t);
-    if (write_debug) {
-      ws_topk_idx(a)[t * a.k + rank] = my_e;
-      ws_topk_w(a)[t * a.k + rank] = w;
-    }
-  }
-  __syncwarp();  // the warp's selection scratch is reused by its next token
+  const int my_e = act ? R.sel_e[warp][lane] : 0;
+  const float s = act ? sigmoid_f32(R.sel_l[warp][lane]) : 0.f;
+  __syncwarp();  // the warp's scratch is reused by its next token
+  route_publish(a, R, t, lane, my_e, s, full, write_debug);
   if (t == 0) FLINT_TRACE(a, tb < 0 ? -1 : tb + 2);
-}
-
-// Inverse of ordered_key.
-__device__ __forceinline__ float unordered_key(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 __device__ __forceinline__ void ce_desc(uint64_t& x, uint64_t& y) {  // x >= y afterwards
@@ -235,39 +260,64 @@ __device__ __forceinline__ void ce_desc(uint64_t& x, uint64_t& y) {  // x >= y a
   y = lo;
 }
 
-// Top-k of one token by one warp for E <= 256 (the Flint shape), same result
-// as topk_token_wide with a fraction of the instructions. Lane l holds experts
-// 8l .. 8l+7, each as one 64-bit word (order-preserving key << 32 | 0xFFFF - e,
-// so a larger word is a larger key or, on equal keys, a lower index), sorts
-// them once with a 19-comparator network, and each round is two warp
-// reductions and a shift of the winning lane's list.
-__device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane, RouteSmem& R, bool write_debug,
-                                  int tb) {
+// Top-k of one token by one warp for E <= 256 (the Flint shape), the same
+// result as topk_token_wide with a fraction of the instructions. Lane l holds
+// experts 8l .. 8l+7, each as one 64-bit word (order-preserving key << 32 |
+// 0xFFFF - e, so a larger word is a larger key or, on equal keys, a lower
+// index), sorts them once with a 19-comparator network, and each round is two
+// warp reductions and a shift of the winning lane's list. Winners come out in
+// (key desc, index asc) order.
+__device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane, RouteSmem& R, bool full,
+                                  bool write_debug, int tb, const float* logits) {
   constexpr int EPL = 8;
-  const float* lg = ws_logits(a) + (size_t)t * a.E;
-  const bool biased = a.bias != nullptr;
+  const float* lg = logits + (size_t)t * a.E;
   const int e0 = lane * EPL;
-  float lv[EPL], bv[EPL];
+  float lv[EPL];
+  if (a.E == 256) {  // 32 contiguous, 16-byte aligned bytes per lane
+    const uint4 p = ld_cg_v4(lg + e0), q = ld_cg_v4(lg + e0 + 4);
+    lv[0] = __uint_as_float(p.x); lv[1] = __uint_as_float(p.y); lv[2] = __uint_as_float(p.z);
+    lv[3] = __uint_as_float(p.w); lv[4] = __uint_as_float(q.x); lv[5] = __uint_as_float(q.y);
+    lv[6] = __uint_as_float(q.z); lv[7] = __uint_as_float(q.w);
+  } else {
 #pragma unroll
-  for (int j = 0; j < EPL; ++j) {  // clamped addresses: every load issues at once
-    const int e = min(e0 + j, a.E - 1);
-    lv[j] = __ldcg(lg + e);
-    bv[j] = biased ? __ldg(a.bias + e) : 0.f;
+    for (int j = 0; j < EPL; ++j) lv[j] = __ldcg(lg + min(e0 + j, a.E - 1));  // clamped: all issue at once
+  }
+#ifdef FLINT_MOE_TRACE
+  if (t == 0 && tb >= 0 && __float_as_uint(lv[0]) != 0x7FC00001u && __float_as_uint(lv[7]) != 0x7FC00001u)
+    FLINT_TRACE(a, 4);  // logits arrived (the condition makes the timer wait for them)
+#endif
+  // Scores of the lane's 8 experts: the fast reciprocal for all of them, the
+  // IEEE division only where its range ends (rare, out of the common path).
+  float sc[EPL], y[EPL];
+  bool slow = false;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    y[j] = 1.0f + expf(-lv[j]);
+    sc[j] = rcp_nr(y[j]);
+    slow |= !(y[j] < RCP_NR_MAX);
+  }
+  if (slow) {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+      if (!(y[j] < RCP_NR_MAX)) sc[j] = rcp_ieee(y[j]);
   }
   uint64_t v[EPL];
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int e = e0 + j;
-    const uint32_t key = ordered_key(biased ? sigmoid_f32(lv[j]) + bv[j] : lv[j]);
-    v[j] = e < a.E ? ((uint64_t)key << 32) | (uint32_t)(0xFFFF - e) : 0ull;
+    const float kf = a.bias ? sc[j] + __ldg(a.bias + min(e, a.E - 1)) : sc[j];
+    v[j] = e < a.E ? ((uint64_t)ordered_key(kf) << 32) | (uint32_t)(0xFFFF - e) : 0ull;
   }
+#ifdef FLINT_MOE_TRACE
+  if (t == 0 && tb >= 0 && v[0] != 1ull && v[7] != 1ull) FLINT_TRACE(a, 5);  // keys computed
+#endif
   ce_desc(v[0], v[2]); ce_desc(v[1], v[3]); ce_desc(v[4], v[6]); ce_desc(v[5], v[7]);
   ce_desc(v[0], v[4]); ce_desc(v[1], v[5]); ce_desc(v[2], v[6]); ce_desc(v[3], v[7]);
   ce_desc(v[0], v[1]); ce_desc(v[2], v[3]); ce_desc(v[4], v[5]); ce_desc(v[6], v[7]);
   ce_desc(v[2], v[4]); ce_desc(v[3], v[5]);
   ce_desc(v[1], v[4]); ce_desc(v[3], v[6]);
   ce_desc(v[1], v[2]); ce_desc(v[3], v[4]); ce_desc(v[5], v[6]);
-  if (t == 0) FLINT_TRACE(a, tb);
+  if (t == 0 && v[0] != 1ull) FLINT_TRACE(a, tb);
   uint32_t my_hi = 0u, my_lo = 0xFFFFu;
   for (int r = 0; r < a.k; ++r) {
     const uint32_t hi = (uint32_t)(v[0] >> 32), lo = (uint32_t)v[0];
@@ -290,194 +340,201 @@ __device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane
     atomicOr(ws_hdr(a) + HDR_STATUS, FLINT_MOE_DEV_ERR_SLOTS);
     my_e = lane;
   }
-  // The winner's logit is its key unless a bias was added to it.
-  const float l = act ? (biased ? __ldcg(lg + my_e) : unordered_key(my_hi)) : 0.f;
-  const float s = act ? sigmoid_f32(l) : 0.f;
-  const float kf = act ? (biased ? s + __ldg(a.bias + my_e) : s) : -INFINITY;
-  // Selection order is (key desc, index asc) already, except that distinct
-  // logits can give equal sigmoids: then reorder by (sigmoid desc, index asc).
-  int rank = lane;
-  const float kprev = __shfl_up_sync(0xffffffffu, kf, 1);
-  if (__any_sync(0xffffffffu, act && lane > 0 && kprev == kf)) {
-    R.sel_e[warp][lane] = my_e;
-    R.sel_k[warp][lane] = kf;
-    __syncwarp();
-    if (act) {
-      rank = 0;
-      for (int q = 0; q < a.k; ++q) {
-        const float kq = R.sel_k[warp][q];
-        const int eq = R.sel_e[warp][q];
-        rank += (kq > kf || (kq == kf && eq < my_e)) ? 1 : 0;
-      }
-    }
-    __syncwarp();
-  }
-  // Sum of the k scores in selection order (a fixed order: deterministic).
-  float ssum = 0.f;
-  for (int q = 0; q < a.k; ++q) ssum += __shfl_sync(0xffffffffu, s, q);
-  if (act) {
-    float w = a.renorm ? s / ssum : s;
-    w *= a.routed_scale;
-    R.idx[t * a.k + rank] = my_e;
-    R.w[t * a.k + rank] = w;
-    atomicOr(&R.mask[my_e], 1u << t);
-    if (write_debug) {
-      ws_topk_idx(a)[t * a.k + rank] = my_e;
-      ws_topk_w(a)[t * a.k + rank] = w;
-    }
-  }
+  float s = 0.f;
+  if (full && act) s = a.bias ? sigmoid_f32(__ldcg(lg + my_e)) : unordered_key(my_hi);  // key = score unbiased
+  route_publish(a, R, t, lane, my_e, s, full, write_debug);
   if (t == 0) FLINT_TRACE(a, tb < 0 ? -1 : tb + 2);
 }
 
-// Whole block. Slots: the S shared experts first, then the distinct selected
-// experts in ascending id. Rows: each slot's tokens in ascending order, shared
-// rows first (S * B of them). tb: first trace event id, or -1.
-__device__ void compute_routing(const DecodeArgs& a, RouteSmem& R, bool write_debug, int tb) {
+// Whole block, after route_clear and a barrier: selects every token's experts
+// (one warp per token) from logits [B][E] and ends with a barrier. Without
+// `full` only the selection bitmaps are built; with it also the weights. tb:
+// first trace event id, or -1.
+__device__ void route_select(const DecodeArgs& a, RouteSmem& R, bool full, bool write_debug, int tb,
+                             const float* logits) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const int B = a.B, E = a.E, k = a.k, S = a.S;
-  for (int i = threadIdx.x; i < E; i += blockDim.x) R.mask[i] = 0;
-  __syncthreads();
-  if (E <= 256) {
-    for (int t = warp; t < B; t += nw) topk_token_narrow(a, t, warp, lane, R, write_debug, tb);
+  if (a.E <= 256) {
+    for (int t = warp; t < a.B; t += nw) topk_token_narrow(a, t, warp, lane, R, full, write_debug, tb, logits);
   } else {
-    for (int t = warp; t < B; t += nw) topk_token_wide(a, t, warp, lane, R, write_debug, tb);
+    for (int t = warp; t < a.B; t += nw) topk_token_wide(a, t, warp, lane, R, full, write_debug, tb, logits);
   }
   __syncthreads();
-  if (warp == 0) {
-    // Exclusive scan over experts of (used << 16 | token count); lane l owns a
-    // contiguous range of experts so the ranks come out in ascending id. Warp 0
-    // also writes the rows, so the block needs a single barrier afterwards.
-    const int ept = (E + 31) >> 5;
-    const int e0 = lane * ept, e1 = min(E, e0 + ept);
-    int local = 0;
-    if (ept == 8 && E == 256) {  // the Flint shape: two 16-byte loads, no bank conflicts
-      const uint4 m0 = *reinterpret_cast<const uint4*>(&R.mask[e0]);
-      const uint4 m1 = *reinterpret_cast<const uint4*>(&R.mask[e0 + 4]);
-      const uint32_t mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  FLINT_TRACE(a, tb < 0 ? -1 : 14);
+}
+
+// Position of the n-th (from 0) set bit of m; n < popc(m).
+__device__ __forceinline__ int nth_set_bit(uint32_t m, int n) {
+  int pos = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) local += mm[q] ? (1 << 16) | __popc(mm[q]) : 0;
+  for (int width = 16; width >= 1; width >>= 1) {
+    const uint32_t low = m & ((1u << width) - 1u);
+    const int c = __popc(low);
+    if (n >= c) {
+      n -= c;
+      m >>= width;
+      pos += width;
     } else {
-      for (int e = e0; e < e1; ++e) {
-        const uint32_t m = R.mask[e];
-        local += m ? (1 << 16) | __popc(m) : 0;
-      }
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    int run = incl - local;
-    for (int e = e0; e < e1; ++e) {
-      const uint32_t m = R.mask[e];
-      if (m) {
-        const int rank = run >> 16, roff = S * B + (run & 0xFFFF);
-        R.rowoff[e] = roff;
-        R.slot_expert[S + rank] = e;
-        R.slot_off[S + rank] = roff;
-        run += (1 << 16) | __popc(m);
-      }
-    }
-    const int n_slots = S + (total >> 16), n_rows = S * B + (total & 0xFFFF);
-    for (int s = lane; s < S; s += 32) {
-      R.slot_expert[s] = E + s;
-      R.slot_off[s] = s * B;
-    }
-    if (lane == 0) {
-      R.slot_off[n_slots] = n_rows;
-      R.n_slots = n_slots;
-      R.n_rows = n_rows;
-    }
-    __syncwarp();
-    FLINT_TRACE(a, tb < 0 ? -1 : 14);
-    for (int p = lane; p < B * k; p += 32) {
-      const int t = p / k, e = R.idx[p];
-      const int row = R.rowoff[e] + __popc(R.mask[e] & ((1u << t) - 1u));
-      R.row_tok[row] = t;
-      R.row_w[row] = R.w[p];
-    }
-    for (int p = lane; p < S * B; p += 32) {
-      R.row_tok[p] = p % B;
-      R.row_w[p] = 1.0f;
+      m = low;
     }
   }
-  __syncthreads();
-  FLINT_TRACE(a, tb < 0 ? -1 : 15);
+  return pos;
+}
+
+// Number of slots: the shared experts plus the distinct selected experts.
+__device__ __forceinline__ int route_slots(const DecodeArgs& a, const RouteSmem& R) {
+  int c = a.S;
+  for (int w = 0; w < (a.E + 31) >> 5; ++w) c += __popc(R.used[w]);
+  return c;
+}
+
+struct SlotInfo {
+  int expert;      // packed expert index (shared experts follow the E routed ones)
+  uint32_t tmask;  // tokens whose output takes this expert
+};
+
+__device__ __forceinline__ SlotInfo slot_info(const DecodeArgs& a, const RouteSmem& R, int slot) {
+  SlotInfo si;
+  if (slot < a.S) {
+    si.expert = a.E + slot;
+    si.tmask = a.B >= 32 ? 0xFFFFFFFFu : (1u << a.B) - 1u;
+    return si;
+  }
+  // The r-th set bit of `used`, four words per 16-byte load (words past E / 32
+  // are zero).
+  int r = slot - a.S, w = -1;
+  uint32_t u = 0u;
+  for (int q = 0; q < USED_WORDS && q < (((a.E + 127) >> 7) << 2); q += 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(&R.used[q]);
+    const int c0 = __popc(v.x), c1 = c0 + __popc(v.y), c2 = c1 + __popc(v.z), c3 = c2 + __popc(v.w);
+    if (r < c3) {
+      if (r < c0) {
+        w = q;
+        u = v.x;
+      } else if (r < c1) {
+        w = q + 1;
+        u = v.y;
+        r -= c0;
+      } else if (r < c2) {
+        w = q + 2;
+        u = v.z;
+        r -= c1;
+      } else {
+        w = q + 3;
+        u = v.w;
+        r -= c2;
+      }
+      break;
+    }
+    r -= c3;
+  }
+  si.expert = w >= 0 ? 32 * w + nth_set_bit(u, r) : 0;  // w < 0 only for slot >= route_slots
+  si.tmask = R.mask[si.expert];
+  return si;
 }
 
 // ===========================================================================
 // K1: router GEMV (logits in the workspace); also clears the per-row |h|
-// maxima that k_gateup accumulates.
-// NCH: 16-byte chunks of a router row per lane per pass (H / 256 capped at 8).
+// maxima that k_gateup accumulates. Block b computes experts 4b .. 4b+3, one
+// per warp; their router rows are contiguous, so one bulk copy brings them
+// into shared memory before the dependency wait (they do not depend on x).
+// NCH: 16-byte chunks of a router row per lane (H / 256).
 // ===========================================================================
+// NT tokens' dot products with one router row: lane l takes 16-byte chunks
+// l, l + 32, ...; all NT sums are independent, so their latencies overlap.
+template <int NCH, int NT>
+__device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* xsm, int H, int lane, float* lg,
+                                            int E, int e, bool dry) {
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const uint4 w = lds128(wrow + (lane + 32 * c) * 16);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = dot8_bf16(w, lds128(xsm + (size_t)t * H * 2 + (lane + 32 * c) * 16), acc[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const float v = warp_sum(acc[t]);
+    if (lane == 0 && !dry) lg[t * E + e] = v;
+  }
+}
+
 template <int NCH>
 __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t dsm[];  // x chunk: up to 8 tokens x H bf16
-  __shared__ __align__(8) uint64_t bar;
+  extern __shared__ __align__(128) uint8_t dsm[];  // router rows [4][H], then x chunk [<= 8][H] (bf16)
+  __shared__ __align__(8) uint64_t bars[2];        // 0: router rows, 1: x
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 4 + warp;
-  const int passes = a.H / (256 * NCH);
+  const int e0 = blockIdx.x * 4, e = e0 + warp;
+  const int nrows = min(4, a.E - e0);
+  uint8_t* wsm = dsm;
+  uint8_t* xsm = dsm + (size_t)4 * a.H * 2;
   FLINT_TRACE(a, 0);
-  uint4 w[NCH];
-  auto load_pass = [&](int p) {
-    const uint8_t* row = reinterpret_cast<const uint8_t*>(a.router + (size_t)e * a.H) + (size_t)p * NCH * 512;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) w[c] = ld_weights_v4(row + (size_t)(lane + 32 * c) * 16);
-  };
-  if (e < a.E) load_pass(0);  // routing-independent: before waiting for x
   if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
     fence_mbar_init();
+    const uint32_t bytes = (uint32_t)nrows * a.H * 2;
+    mbar_arrive_expect_tx(&bars[0], bytes);
+    bulk_g2s(wsm, a.router + (size_t)e0 * a.H, bytes, &bars[0]);
   }
-  pdl_wait();  // x is the previous kernel's output
-  pdl_trigger();
-  FLINT_TRACE(a, 1);
-  __syncthreads();
+  // Two passes at one call site: a dry one on zeroed activations before the
+  // dependency wait (no stores), which brings the dot-product code into this
+  // SM's instruction caches, then the real one on x.
   int* status = ws_hdr(a) + HDR_STATUS;
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < a.W.max_rows; i += blockDim.x) ws_hmax(a)[i] = 0u;
   float* lg = ws_logits(a);
-  uint32_t phase = 0;
-  for (int t0 = 0; t0 < a.B; t0 += 8) {
-    const int nt = min(8, a.B - t0);
-    if (threadIdx.x == 0) {
-      const uint32_t bytes = (uint32_t)nt * a.H * 2;
-      mbar_arrive_expect_tx(&bar, bytes);
-      bulk_g2s(dsm, a.x + (size_t)t0 * a.H, bytes, &bar);
-    }
-    const bool ok = __syncthreads_and(mbar_wait(&bar, phase, status));  // block-uniform
-    phase ^= 1;
-    if (!ok) break;
-    FLINT_TRACE(a, 2);
-    if (e < a.E) {
-      // All tokens of the chunk at once: independent sums give the FMA and
-      // shuffle latencies something to overlap with.
-      float acc[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) acc[t] = 0.f;
-      for (int p = 0; p < passes; ++p) {
-        if (p > 0 || (t0 > 0 && passes > 1)) load_pass(p);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (t < nt) {
-            const uint8_t* xr = dsm + (size_t)t * a.H * 2 + (size_t)p * NCH * 512;
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) acc[t] = dot8_bf16(w[c], lds128(xr + (lane + 32 * c) * 16), acc[t]);
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        if (t < nt) {
-          const float v = warp_sum(acc[t]);
-          if (lane == 0) lg[(t0 + t) * a.E + e] = v;
-        }
-      }
-    }
-    __syncthreads();  // the x chunk buffer is reused by the next copy
+  const uint8_t* wrow = wsm + (size_t)warp * a.H * 2;
+  {
+    const int n = (a.B < 8 ? a.B : 8) * a.H / 8;  // 16-byte words of the first x chunk
+    for (int i = threadIdx.x; i < n; i += blockDim.x) reinterpret_cast<uint4*>(xsm)[i] = make_uint4(0, 0, 0, 0);
   }
+  __syncthreads();  // the barriers are initialised (thread 0) before any thread waits on them
+  const bool okw = mbar_wait(&bars[0], 0, status);
+  uint32_t phase = 0;
+  bool ok = okw;
+#pragma unroll 1
+  for (int pass = 0; pass < 2 && ok; ++pass) {
+    const bool dry = pass == 0;
+    if (!dry) {
+      pdl_wait();  // x is the previous kernel's output
+      pdl_trigger();
+      FLINT_TRACE(a, 1);
+      if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < a.W.max_slots * a.B; i += blockDim.x) ws_hmax(a)[i] = 0u;
+    }
+    for (int t0 = 0; t0 < a.B; t0 += 8) {
+      const int nt = min(8, a.B - t0);
+      if (!dry) {
+        if (threadIdx.x == 0) {
+          const uint32_t bytes = (uint32_t)nt * a.H * 2;
+          mbar_arrive_expect_tx(&bars[1], bytes);
+          bulk_g2s(xsm, a.x + (size_t)t0 * a.H, bytes, &bars[1]);
+        }
+        ok = __syncthreads_and(mbar_wait(&bars[1], phase, status));  // block-uniform
+        phase ^= 1;
+        if (!ok) break;
+        FLINT_TRACE(a, 2);
+      }
+      if (e < a.E) {
+        float* lgc = lg + (size_t)t0 * a.E;
+        switch (nt) {  // one code path per token count: no predicated-off work
+          case 1: router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+          case 2: router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+          case 3: router_dots<NCH, 3>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+          case 4: router_dots<NCH, 4>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+          case 5: router_dots<NCH, 5>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+          case 6: router_dots<NCH, 6>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+          case 7: router_dots<NCH, 7>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+          default: router_dots<NCH, 8>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+        }
+        if (!dry) FLINT_TRACE(a, 7);
+      }
+      fence_proxy_async();  // the zeroing stores and these reads come before the copy into the buffer
+      __syncthreads();      // the x chunk buffer is reused by the next copy
+      if (dry) break;       // one chunk warms the code
+    }
+  }
+  if (!okw) mbar_drain(&bars[0], 0);
   FLINT_TRACE(a, 3);
 }
 
@@ -606,7 +663,7 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
       const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + (int64_t)tile * a.L.gu_tile +
                            (int64_t)gw * kslice;
       mbar_arrive_expect_tx(wbar(b), (uint32_t)kslice);
-      bulk_g2s(wbuf(b), src, (uint32_t)kslice, wbar(b));
+      bulk_g2s_stream(wbuf(b), src, (uint32_t)kslice, wbar(b));
     }
   };
   // The shared experts' units come first and need no routing: fetch them now.
@@ -620,6 +677,7 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
     mbar_arrive_expect_tx(xbar, (uint32_t)(a.B * a.H * 2));
     bulk_g2s(xstage, a.x, (uint32_t)(a.B * a.H * 2), xbar);
   }
+  route_clear(R, a.E);
   const bool okx = __syncthreads_and(mbar_wait(xbar, 0, status));
   if (okx) {  // warp w prescales and reorders tokens w, w + nwarps, ...
     for (int t = warp; t < a.B; t += blockDim.x >> 5) {
@@ -656,12 +714,12 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
   pdl_wait();
   pdl_trigger();
   FLINT_TRACE(a, 9);
-  compute_routing(a, R, blockIdx.x == 0, 21);  // its barriers also publish xs and s_inv
+  route_select(a, R, false, false, 21, ws_logits(a));  // its barrier also publishes xs and s_inv
   FLINT_TRACE(a, 10);
-  const int n_units = R.n_slots * TILES;
+  const int n_units = route_slots(a, R) * TILES;
   for (int jj = pre; jj < NB; ++jj) {
     const int u = unit_of(jj);
-    if (u < n_units) issue_w(jj, R.slot_expert[u / TILES], u % TILES);
+    if (u < n_units) issue_w(jj, slot_info(a, R, u / TILES).expert, u % TILES);
   }
   const float* glob = a.globals;
   for (int jj = 0;; ++jj) {
@@ -670,8 +728,9 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
     const int b = jj % NB;
     const uint32_t par = (uint32_t)((jj / NB) & 1);
     const int slot = u / TILES, tile = u % TILES;
-    const int expert = R.slot_expert[slot], off = R.slot_off[slot], T = R.slot_off[slot + 1] - off;
-    const int nt_used = (T + 7) >> 3;
+    const SlotInfo si = slot_info(a, R, slot);
+    const int expert = si.expert;
+    const int nt_used = (32 - __clz(si.tmask) + 7) >> 3;  // token tiles up to the last selecting token
     float acc[2][NTMAX][4];
 #pragma unroll
     for (int c = 0; c < 2; ++c)
@@ -682,9 +741,9 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
     const bool ok = mbar_wait(wbar(b), par, status) && okx;
     if (jj == 0) FLINT_TRACE(a, 11);
     if (ok) {
-      int tok[NTMAX];
+      int tok[NTMAX];  // column g of token tile nt is token 8 nt + g (past B: a repeat of token B - 1)
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt) tok[nt] = R.row_tok[off + min(nt * 8 + g, T - 1)];
+      for (int nt = 0; nt < NTMAX; ++nt) tok[nt] = min(nt * 8 + g, a.B - 1);
       const uint8_t* wb = wbuf(b);
 #pragma unroll 4
       for (int kl = 0; kl < KGW; ++kl) {
@@ -721,7 +780,7 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
     // This warp's weight slice is free again: fetch its slice of unit jj + NB.
     {
       const int u2 = unit_of(jj + NB);
-      if (u2 < n_units) issue_w(b, R.slot_expert[u2 / TILES], u2 % TILES);
+      if (u2 < n_units) issue_w(b, slot_info(a, R, u2 / TILES).expert, u2 % TILES);
     }
     if (gw != 0) continue;
     float sum[NTMAX][4];
@@ -744,21 +803,24 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
       if (nt >= nt_used) break;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int n = nt * 8 + 2 * t4 + hh;
+        const int n = nt * 8 + 2 * t4 + hh;  // token
+        const size_t row = (size_t)slot * a.B + n;
+        const bool sel = n < a.B && ((si.tmask >> n) & 1u);
         float hv = 0.f;
-        if (n < T) {
-          const float inv = s_inv[R.row_tok[off + n]];
+        if (sel) {
+          const float inv = s_inv[n];
           const float gv = (sum[nt][hh] * inv) * Gg;
           const float uv = (sum[nt][2 + hh] * inv) * Gu;
-          const float sv = gv / (1.0f + expf(-gv));
+          const float ey = 1.0f + expf(-gv);
+          const float sv = ey < RCP_NR_MAX ? gv * rcp_nr(ey) : gv / ey;  // SiLU
           const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
-          h[(size_t)(off + n) * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hb);
+          h[row * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hb);
           hv = fabsf(__bfloat162float(hb));
         }
         hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 4));
         hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 8));
         hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 16));
-        if (g == 0 && n < T && hv > 0.f) atomicMax(hmax + off + n, __float_as_uint(hv));
+        if (g == 0 && sel && hv > 0.f) atomicMax(hmax + row, __float_as_uint(hv));
       }
     }
   }
@@ -776,17 +838,17 @@ struct DownSmemPlan {
   size_t acc_off, items_off, hmax_off, inv_off, bar_off, total;
 };
 
-__host__ __device__ inline DownSmemPlan down_plan(int H, int I, int B, int max_slots, int max_rows, int fmt, int nbuf,
-                                                  int nw) {
+__host__ __device__ inline DownSmemPlan down_plan(int H, int I, int B, int max_slots, int fmt, int nbuf, int nw) {
   DownSmemPlan p;
   const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  const int nt = (B + 7) / 8;
   p.hrows = B < 8 ? B : 8;
   p.hstride = I * 2 + 16;
   p.buf_bytes = (I / KG_COLS) * kgb + p.hrows * p.hstride;
   size_t o = (size_t)nw * nbuf * p.buf_bytes;
   p.acc_off = o;    o += sizeof(float) * nw * B * 16;
-  p.items_off = o;  o += sizeof(int) * (max_slots + max_rows / 8 + 8);
-  p.hmax_off = o;   o += sizeof(float) * max_rows;
+  p.items_off = o;  o += sizeof(int) * 2 * max_slots * nt;
+  p.hmax_off = o;   o += sizeof(float) * max_slots * B;
   o = (o + 15) & ~(size_t)15;
   p.inv_off = o;    o += sizeof(float) * nw * nbuf * 8;
   o = (o + 15) & ~(size_t)15;
@@ -804,10 +866,11 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int nw = blockDim.x >> 5;
   const int tile = blockIdx.x;
-  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, a.W.max_rows, FMT, NBUF, nw);
+  const int NT = (a.B + 7) / 8;  // token tiles
+  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, FMT, NBUF, nw);
   const int dn_bytes = (int)a.L.dn_tile;
   float* acc_s = reinterpret_cast<float*>(smem + P.acc_off);
-  int* s_items = reinterpret_cast<int*>(smem + P.items_off);
+  int* s_items = reinterpret_cast<int*>(smem + P.items_off);  // per item: slot << 16 | tile << 8 | tokens, expert
   float* s_hmax = reinterpret_cast<float*>(smem + P.hmax_off);
   float* s_inv = reinterpret_cast<float*>(smem + P.inv_off) + warp * NBUF * 8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off) + warp * NBUF;
@@ -818,30 +881,34 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
   if (lane < NBUF) mbar_init(&bars[lane], 2);  // one arrival for the weights, one for the h rows
   fence_mbar_init();
   for (int i = threadIdx.x; i < nw * a.B * 16; i += blockDim.x) acc_s[i] = 0.f;
+  route_clear(R, a.E);
   __syncthreads();
 
   auto issue_weights = [&](int j, int expert) {
     if (lane == 0) {
       const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + a.L.gu_bytes + (int64_t)tile * dn_bytes;
       mbar_arrive_expect_tx(&bars[j % NBUF], (uint32_t)dn_bytes);
-      bulk_g2s(buf(j % NBUF), src, (uint32_t)dn_bytes, &bars[j % NBUF]);
+      bulk_g2s_stream(buf(j % NBUF), src, (uint32_t)dn_bytes, &bars[j % NBUF]);
     }
   };
-  // The shared experts' items come first and are known before routing (T = B).
-  const int cps = (a.B + 7) / 8;
+  // Items are (slot, token tile) pairs, slot-major. The shared experts' items
+  // come first and cover every token tile, so they are known before routing.
   int w_issued = 0;
-  for (int i = warp; i < a.S * cps && w_issued < NBUF; i += nw, ++w_issued) issue_weights(w_issued, a.E + i / cps);
+  for (int i = warp; i < a.S * NT && w_issued < NBUF; i += nw, ++w_issued) issue_weights(w_issued, a.E + i / NT);
 
   // k_gateup lets this kernel launch only after its own wait, so the router has
   // finished: route now and fetch the routed down tiles while k_gateup runs.
-  compute_routing(a, R, false, -1);
+  route_select(a, R, true, blockIdx.x == 0, -1, ws_logits(a));
   FLINT_TRACE(a, 17);
+  const int n_slots = route_slots(a, R);
   {
-    const int n_slots = R.n_slots;
     const int spt = (n_slots + blockDim.x - 1) / blockDim.x;
     const int s0 = threadIdx.x * spt;
     int local = 0;
-    for (int s = s0; s < s0 + spt && s < n_slots; ++s) local += (R.slot_off[s + 1] - R.slot_off[s] + 7) >> 3;
+    for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
+      const uint32_t tm = slot_info(a, R, s).tmask;
+      for (int nt = 0; nt < NT; ++nt) local += ((tm >> (8 * nt)) & 0xFFu) != 0u;
+    }
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -853,48 +920,61 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
     int run = incl - local;
     for (int w2 = 0; w2 < warp; ++w2) run += s_wsum[w2];
     for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
-      const int nc = (R.slot_off[s + 1] - R.slot_off[s] + 7) >> 3;
-      for (int c = 0; c < nc; ++c) s_items[run + c] = (s << 8) | c;
-      run += nc;
+      const SlotInfo si = slot_info(a, R, s);
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t bits = (si.tmask >> (8 * nt)) & 0xFFu;
+        if (bits) {
+          s_items[2 * run] = (s << 16) | (nt << 8) | (int)bits;
+          s_items[2 * run + 1] = si.expert;
+          ++run;
+        }
+      }
     }
   }
   __syncthreads();
   int n_items = 0;
   for (int w2 = 0; w2 < nw; ++w2) n_items += s_wsum[w2];
-  auto item_of = [&](int j, int& s, int& r0, int& Tc) {
-    const int it = s_items[warp + nw * j];
-    s = it >> 8;
-    r0 = R.slot_off[s] + 8 * (it & 0xFF);
-    Tc = min(8, R.slot_off[s + 1] - r0);
+  auto item_of = [&](int j, int& s, int& nt, uint32_t& bits, int& expert) {
+    const int it = s_items[2 * (warp + nw * j)];
+    s = it >> 16;
+    nt = (it >> 8) & 0xFF;
+    bits = (uint32_t)it & 0xFFu;
+    expert = s_items[2 * (warp + nw * j) + 1];
   };
   for (int j = w_issued; j < NBUF && warp + nw * j < n_items; ++j) {
-    int s, r0, Tc;
-    item_of(j, s, r0, Tc);
-    issue_weights(j, R.slot_expert[s]);
+    int s, nt, e;
+    uint32_t bits;
+    item_of(j, s, nt, bits, e);
+    issue_weights(j, e);
   }
 
-  pdl_wait();  // h comes from k_gateup
-  pdl_trigger();
-  FLINT_TRACE(a, 18);
-
+  // Token tile nt of slot s is h rows s * B + 8 nt + n, n < 8; only the rows
+  // of tokens that selected the expert are copied (column n of the product is
+  // token n, and the other columns are never combined).
   auto issue_h = [&](int j) {
-    int s, r0, Tc;
-    item_of(j, s, r0, Tc);
+    int s, nt, e;
+    uint32_t bits;
+    item_of(j, s, nt, bits, e);
+    const int r0 = s * a.B + 8 * nt;
     const int b = j % NBUF;
-    if (lane == 0) mbar_arrive_expect_tx(&bars[b], (uint32_t)(Tc * a.I * 2));
+    if (lane == 0) mbar_arrive_expect_tx(&bars[b], (uint32_t)(__popc(bits) * a.I * 2));
     __syncwarp();
-    if (lane < Tc)
+    if (lane < 8 && ((bits >> lane) & 1u))
       bulk_g2s(buf(b) + dn_bytes + lane * P.hstride, ws_h(a) + (size_t)(r0 + lane) * a.I, (uint32_t)(a.I * 2),
                &bars[b]);
   };
-  for (int j = 0; j < NBUF && warp + nw * j < n_items; ++j) issue_h(j);
-  for (int i = threadIdx.x; i < R.n_rows; i += blockDim.x) s_hmax[i] = __uint_as_float(__ldcg(ws_hmax(a) + i));
-  __syncthreads();
-
   const int KG = a.I / KG_COLS;
+  pdl_wait();  // h comes from k_gateup
+  pdl_trigger();
+  FLINT_TRACE(a, 18);
+  for (int j = 0; j < NBUF && warp + nw * j < n_items; ++j) issue_h(j);
+  for (int i = threadIdx.x; i < n_slots * a.B; i += blockDim.x) s_hmax[i] = __uint_as_float(__ldcg(ws_hmax(a) + i));
+  __syncthreads();
   for (int j = 0; warp + nw * j < n_items; ++j) {
-    int s, r0, Tc;
-    item_of(j, s, r0, Tc);
+    int s, nt, expert;
+    uint32_t bits;
+    item_of(j, s, nt, bits, expert);
+    const int r0 = s * a.B + 8 * nt, Tc = min(8, a.B - 8 * nt);
     const int b = j % NBUF;
     const uint32_t parity = (uint32_t)((j / NBUF) & 1);
     if (!mbar_wait(&bars[b], parity, status)) {
@@ -907,6 +987,7 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
     uint8_t* hb = wb + dn_bytes;
     if (FMT == FLINT_MOE_NVFP4) {
       for (int n = 0; n < Tc; ++n) {
+        if (!((bits >> n) & 1u)) continue;
         const int kh = prescale_exp(s_hmax[r0 + n]);
         const float sc = exp2i(kh);
         uint32_t* rowp = reinterpret_cast<uint32_t*>(hb + n * P.hstride);
@@ -938,14 +1019,16 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
       else
         tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
     }
-    const float Gd = a.globals[R.slot_expert[s] * 4 + 2];
+    const float Gd = a.globals[expert * 4 + 2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int n = 2 * t4 + hh;
-      if (n < Tc) {
-        const int row = r0 + n;
-        const int tok = R.row_tok[row];
-        const float wt = R.row_w[row];
+      if (n < Tc && ((bits >> n) & 1u)) {
+        const int tok = 8 * nt + n;
+        float wt = 1.0f;  // the shared experts are unweighted
+        if (s >= a.S)
+          for (int r = 0; r < a.k; ++r)
+            if (R.idx[tok * a.k + r] == expert) wt = R.w[tok * a.k + r];
         const float inv = s_inv[b * 8 + n];
         float* dst = acc_s + (warp * a.B + tok) * 16;
         dst[g] += wt * (((acc[0][0][hh] + acc[1][0][hh]) * inv) * Gd);
@@ -954,9 +1037,10 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
     }
     __syncwarp();
     if (warp + nw * (j + NBUF) < n_items) {
-      int s2, r2, T2;
-      item_of(j + NBUF, s2, r2, T2);
-      issue_weights(j + NBUF, R.slot_expert[s2]);
+      int s2, nt2, e2;
+      uint32_t bits2;
+      item_of(j + NBUF, s2, nt2, bits2, e2);
+      issue_weights(j + NBUF, e2);
       issue_h(j + NBUF);
     }
   }
@@ -987,6 +1071,9 @@ constexpr size_t SMEM_LIMIT = 227 * 1024;
 
 // 8 warps keep more down tiles in flight for small batches; larger batches and
 // BF16 tiles (16 KB each) need the shared memory for fewer, deeper buffers.
+// Router rows of one block (4 experts) plus one x chunk of up to 8 tokens.
+size_t router_smem(int H, int B) { return (size_t)(4 + (B < 8 ? B : 8)) * H * 2; }
+
 int down_warps(int B, int fmt) { return (B <= 4 && fmt == FLINT_MOE_NVFP4) ? 8 : 4; }
 
 int sm_count() {
@@ -1070,24 +1157,26 @@ cudaError_t launch_gateup(const DecodeArgs& a, cudaStream_t stream, int ng) {
 template <int FMT>
 cudaError_t launch_down(const DecodeArgs& a, cudaStream_t stream) {
   const int nw = down_warps(a.B, FMT);
-  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, a.W.max_rows, FMT, DOWN_NBUF, nw);
+  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, FMT, DOWN_NBUF, nw);
   return launch_pdl(k_down<FMT, DOWN_NBUF>, dim3(a.H / 16), dim3(32 * nw), P.total, stream, a);
 }
 
 cudaError_t launch_router(const DecodeArgs& a, cudaStream_t stream) {
   const dim3 grid((a.E + 3) / 4);
-  const size_t smem = (size_t)(a.B < 8 ? a.B : 8) * a.H * 2;
-  switch (a.H) {
-    case 256: return launch_pdl(k_router<1>, grid, dim3(128), smem, stream, a);
-    case 512: return launch_pdl(k_router<2>, grid, dim3(128), smem, stream, a);
-    case 768: return launch_pdl(k_router<3>, grid, dim3(128), smem, stream, a);
-    case 1024: return launch_pdl(k_router<4>, grid, dim3(128), smem, stream, a);
-    case 1280: return launch_pdl(k_router<5>, grid, dim3(128), smem, stream, a);
-    case 1536: return launch_pdl(k_router<6>, grid, dim3(128), smem, stream, a);
-    case 1792: return launch_pdl(k_router<7>, grid, dim3(128), smem, stream, a);
-    default:
-      if (a.H % 2048) return cudaErrorInvalidValue;
-      return launch_pdl(k_router<8>, grid, dim3(128), smem, stream, a);
+  const size_t smem = router_smem(a.H, a.B);
+  switch (a.H / 256) {
+    case 1: return launch_pdl(k_router<1>, grid, dim3(128), smem, stream, a);
+    case 2: return launch_pdl(k_router<2>, grid, dim3(128), smem, stream, a);
+    case 3: return launch_pdl(k_router<3>, grid, dim3(128), smem, stream, a);
+    case 4: return launch_pdl(k_router<4>, grid, dim3(128), smem, stream, a);
+    case 5: return launch_pdl(k_router<5>, grid, dim3(128), smem, stream, a);
+    case 6: return launch_pdl(k_router<6>, grid, dim3(128), smem, stream, a);
+    case 7: return launch_pdl(k_router<7>, grid, dim3(128), smem, stream, a);
+    case 8: return launch_pdl(k_router<8>, grid, dim3(128), smem, stream, a);
+    case 16: return launch_pdl(k_router<16>, grid, dim3(128), smem, stream, a);
+    case 24: return launch_pdl(k_router<24>, grid, dim3(128), smem, stream, a);
+    case 32: return launch_pdl(k_router<32>, grid, dim3(128), smem, stream, a);
+    default: return cudaErrorInvalidValue;
   }
 }
 
@@ -1165,9 +1254,9 @@ extern "C" flint_moe_status flint_moe_decode(const flint_moe_layer* layer, const
     gateup_shape(a.H, B, a.fmt, (units + sms - 1) / sms, gu_ng, a.gu_nb);
   }
   if (gu_ng == 0 ||
-      down_plan(a.H, a.I, B, a.W.max_slots, a.W.max_rows, a.fmt, DOWN_NBUF, down_warps(B, a.fmt)).total + route_smem >
+      down_plan(a.H, a.I, B, a.W.max_slots, a.fmt, DOWN_NBUF, down_warps(B, a.fmt)).total + route_smem >
           SMEM_LIMIT ||
-      (size_t)(B < 8 ? B : 8) * a.H * 2 > SMEM_LIMIT - 16 * 1024)
+      router_smem(a.H, B) > SMEM_LIMIT)
     return FLINT_MOE_EUNSUPPORTED;
   cudaError_t e = launch_router(a, stream);
   if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_gateup<FLINT_MOE_NVFP4>(a, stream, gu_ng)
@@ -1218,6 +1307,36 @@ extern "C" flint_moe_status flint_moe_debug_routing(const flint_moe_config* c, c
   if (cudaMemcpyAsync(w, base + W.topk_w, n * sizeof(float), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
     return FLINT_MOE_ECUDA;
   return FLINT_MOE_OK;
+}
+
+namespace {
+__global__ void k_rcp_check(uint32_t lo, uint32_t hi, unsigned long long* bad) {
+  unsigned long long nb = 0;
+  for (uint64_t i = lo + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < hi; i += (uint64_t)gridDim.x * blockDim.x) {
+    const float y = __uint_as_float((uint32_t)i);
+    if (__float_as_uint(rcp_nr(y)) != __float_as_uint(1.0f / y)) ++nb;
+  }
+  if (nb) atomicAdd(bad, nb);
+}
+}  // namespace
+
+extern "C" flint_moe_status flint_moe_debug_rcp_check(uint32_t lo_bits, uint32_t hi_bits,
+                                                      uint64_t* host_mismatches, cudaStream_t stream) {
+  const uint32_t one = 0x3F800000u, top = (127u + 125u) << 23;  // 1.0f, 2^125
+  if (!host_mismatches || lo_bits < one || hi_bits > top || lo_bits > hi_bits) return FLINT_MOE_EINVAL;
+  unsigned long long* d = nullptr;
+  if (cudaMallocAsync(&d, sizeof(*d), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
+  cudaError_t e = cudaMemsetAsync(d, 0, sizeof(*d), stream);
+  if (e == cudaSuccess && hi_bits > lo_bits) {
+    k_rcp_check<<<sm_count() * 8, 256, 0, stream>>>(lo_bits, hi_bits, d);
+    e = cudaGetLastError();
+  }
+  unsigned long long h = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof(h), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  cudaFreeAsync(d, stream);
+  *host_mismatches = h;
+  return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
 }
 
 extern "C" flint_moe_status flint_moe_read_status(const void* ws, int32_t* host_status, cudaStream_t stream) {
