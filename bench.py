@@ -43,7 +43,8 @@ def parse_args():
     p.add_argument("--batch", type=int, default=1)
     p.add_argument("--layers", type=int, default=47)
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--quick", action="store_true", help="skip the batch-8, isolated, e2e and CPU legs")
+    p.add_argument("--quick", action="store_true", help="skip the batch-8, isolated, e2e, stack and CPU legs")
+    p.add_argument("--stack-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--oracle-leg", type=int, default=0, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -192,6 +193,23 @@ def recorded_traffic(batch: int):
     except (OSError, ValueError, KeyError):
         pass
     return None
+
+
+STACK_BIAS_FILE = os.path.join(ROOT, "tests", "golden", "flint_stack_bias.txt")
+
+
+def stack_bias() -> tuple[float, int]:
+    """(beta, number of biased experts) of the stack workload, as recorded by
+    tests/golden/make_stack_bias.py."""
+    import struct
+    kv = {}
+    with open(STACK_BIAS_FILE) as f:
+        for line in f:
+            if not line.startswith("#") and line.strip():
+                k, v = line.split(None, 1)
+                kv[k] = v.strip()
+    beta = struct.unpack(">f", bytes.fromhex(kv["beta_f32_hex"]))[0]
+    return beta, int(kv["biased_experts"])
 
 
 def gpu_arm(args) -> None:
@@ -349,6 +367,72 @@ def gpu_arm(args) -> None:
         barrier()
         return max_over_ranks(e0.elapsed_time(e1)) * 1000.0 / steps
 
+    def stack_leg(batches=(1, 2, 4, 8, 16, 32), passes=20):
+        """The 47-layer stack: distinct layers (generator seed 1000 + L), the
+        output of layer L is the input of layer L + 1, routing skewed by a
+        selection bias on experts 0..25; per batch, the median over `passes`
+        replays of the whole stack (one CUDA graph, PDL between all kernels)."""
+        beta, nb = stack_bias()
+        bias = torch.zeros(cfg.num_experts, dtype=torch.float32, device=dev)
+        bias[:nb] = beta
+        stack = [layers.synth_layer(cfg, 1000 + L, L, dev, bias=bias) for L in range(P)]
+        ws_s = layers.workspace(cfg, max(batches), dev)
+        res = {}
+        for Bs in batches:
+            bufs = [layers.synth_x(Bs, cfg.hidden, 1000, 0, dev)] + \
+                   [torch.empty(Bs, cfg.hidden, dtype=torch.int16, device=dev) for _ in range(P)]
+            idx = torch.empty(Bs, cfg.top_k, dtype=torch.int32, device=dev)
+            w = torch.empty(Bs, cfg.top_k, dtype=torch.float32, device=dev)
+            dl, picks, biased = [], 0, 0
+            for L in range(P):  # one eager pass: distinct experts and skew per layer
+                fb.flint_moe_decode(stack[L].handle, bufs[L], Bs, bufs[L + 1], ws_s)
+                fb.flint_moe_debug_routing(cfg, ws_s, Bs, idx, w)
+                ii = idx.cpu().numpy().ravel()
+                dl.append(len(set(ii.tolist())))
+                picks += ii.size
+                biased += int((ii < nb).sum())
+            st, bits = fb.flint_moe_read_status(ws_s)
+            if st != fb.OK or bits:
+                raise RuntimeError(f"device status {bits} in the stack")
+            stream = torch.cuda.Stream(device=dev)
+            stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(stream):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for L in range(P):
+                        fb.flint_moe_decode(stack[L].handle, bufs[L], Bs, bufs[L + 1], ws_s, stream)
+                for _ in range(3):
+                    g.replay()
+                stream.synchronize()
+                times = []
+                for _ in range(passes):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    stream.synchronize()
+                    times.append(e0.elapsed_time(e1))
+            us_layer = statistics.median(times) * 1000.0 / P
+            ub = statistics.mean(unique_bytes(D, Bs) for D in dl)
+            res[str(Bs)] = {"us_per_layer": us_layer, "gbs": ub / (us_layer * 1e-6) / 1e9,
+                            "frac": ub / (us_layer * 1e-6) / 1e9 / measured_peak_gbs()[0],
+                            "mean_distinct_experts": statistics.mean(dl), "unique_bytes_per_layer": ub,
+                            "biased_pick_fraction": biased / picks, "passes": passes}
+            del bufs
+        del stack, ws_s
+        torch.cuda.empty_cache()
+        return {"workload": f"{P} chained Flint-shape NVFP4 layers (generator seeds 1000 + L), output of layer L is "
+                            f"the input of layer L + 1, selection bias {beta:.6g} on experts 0..{nb - 1}",
+                "timing": f"median of {passes} replays of the whole stack (one CUDA graph), us per layer = "
+                          f"stack time / {P}",
+                "beta": beta, "per_batch": res}
+
+    if args.stack_only:
+        if rank == 0:
+            print(json.dumps({"stack": stack_leg()}))
+        return
+
     K, W, B = args.steps, max(args.warmup, 3), args.batch
     pool, xs, outs, ws = build_pool(B)
     ds = distinct_per_layer(pool, xs, outs, ws, B)
@@ -377,6 +461,8 @@ def gpu_arm(args) -> None:
                            "isolated_l2_flushed_us": isolated(pool8, xs8, outs8, ws8, 8)}
         del pool8, xs8, outs8, ws8
         torch.cuda.empty_cache()
+    if not args.quick and B == 1 and world == 1:
+        extra["stack"] = stack_leg()
 
     if rank != 0:
         if world > 1:

@@ -222,6 +222,57 @@ def test_routing_reciprocal_is_the_ieee_quotient():
     assert fb.flint_moe_debug_rcp_check(0x3F800000, (127 + 125) << 23) == 0
 
 
+def _stack_bias_vector(E=256):
+    import os
+    import sys
+    sys.path.insert(0, os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden"))
+    import make_stack_bias as msb
+    b = np.zeros(E, np.float32)
+    b[:msb.N_BIASED] = np.float32(msb.read_beta())
+    return b
+
+
+def test_decode_flint_stack_layers_with_selection_bias():
+    """Layers of the skewed 47-layer stack workload (generator seed 1000 + L,
+    selection bias on experts 0..25) at batch 8 and 32, sampled tokens."""
+    bias = _stack_bias_vector()
+    _, _, routing = run_parity(FLINT, 8, seed=1003, layer=3, bias=bias, tokens=[0, 5])
+    assert (routing.idx < 26).any()
+    run_parity(FLINT, 32, seed=1046, layer=46, bias=bias, tokens=[31])
+
+
+def test_flint_stack_chain_graph_equals_serial():
+    """Three chained Flint-shape layers with the stack's selection bias, batch
+    4: a CUDA-graph replay (PDL between all kernels) is bit-identical to the
+    same decodes run one at a time with a full synchronisation between them."""
+    cfg = cfg_of(FLINT)
+    bias = torch.from_numpy(_stack_bias_vector()).to(DEV)
+    B = 4
+    dls = [layers.synth_layer(cfg, 1000 + L, L, DEV, bias=bias) for L in range(3)]
+    ws = layers.workspace(cfg, 32, DEV)
+    x0 = layers.synth_x(B, cfg.hidden, 1000, 0, DEV)
+    serial = [x0] + [torch.empty_like(x0) for _ in range(3)]
+    for L in range(3):
+        fb.flint_moe_decode(dls[L].handle, serial[L], B, serial[L + 1], ws)
+        torch.cuda.synchronize()
+    bufs = [x0] + [torch.zeros_like(x0) for _ in range(3)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for L in range(3):
+                fb.flint_moe_decode(dls[L].handle, bufs[L], B, bufs[L + 1], ws, s)
+    s.synchronize()
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(serial[1:], bufs[1:]):
+            assert torch.equal(a, b)
+    st, bits = fb.flint_moe_read_status(ws)
+    assert st == fb.OK and bits == 0
+
+
 def test_decode_batch0_is_a_noop():
     cfg = cfg_of(TINY)
     dl = layers.synth_layer(cfg, 0, 0, DEV)

@@ -594,7 +594,7 @@ __device__ __forceinline__ void tile_kgroup(const uint8_t* kp, const uint4 (&bx)
 constexpr int GU_MAX_GROUPS = 3;
 
 struct GateupPlan {
-  size_t wbuf_off, xstage_off, xs_off, red_off, inv_off, bar_off, total;
+  size_t wbuf_off, xs_off, red_off, inv_off, bar_off, total;
 };
 
 __host__ __device__ inline GateupPlan gateup_plan(int H, int B, int fmt, int ntmax, int ng, int nb) {
@@ -603,12 +603,11 @@ __host__ __device__ inline GateupPlan gateup_plan(int H, int B, int fmt, int ntm
   GateupPlan p;
   size_t o = 0;
   p.wbuf_off = o;   o += (size_t)ng * nb * 4 * kslice;
-  p.xstage_off = o; o += (size_t)B * H * 2;
   p.xs_off = o;     o += (size_t)B * (H * 2 + 16);
   p.red_off = o;    o += sizeof(float) * ng * 2 * 3 * ntmax * 128;
   p.inv_off = o;    o += sizeof(float) * MAX_BATCH;
   o = (o + 15) & ~(size_t)15;
-  p.bar_off = o;    o += sizeof(uint64_t) * (ng * nb * 4 + 1);
+  p.bar_off = o;    o += sizeof(uint64_t) * ng * nb * 4;
   p.total = o;
   return p;
 }
@@ -640,14 +639,12 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
   const int kslice = KGW * KGB;
   const int xstride = a.H * 2 + 16;
   const GateupPlan P = gateup_plan(a.H, a.B, FMT, NTMAX, NG, NB);
-  uint8_t* xstage = smem + P.xstage_off;
   uint8_t* xs = smem + P.xs_off;
   // Cross-warp partial sums of a group, double-buffered by unit parity: warp 0
   // of the group reads one buffer while warps 1..3 fill the other.
   float* red = reinterpret_cast<float*>(smem + P.red_off) + gi * 2 * 3 * NTMAX * 128;
   float* s_inv = reinterpret_cast<float*>(smem + P.inv_off);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);  // [NG][NB][4] weights, then x
-  uint64_t* xbar = bars + NG * NB * 4;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);  // [NG][NB][4] weight slices
   auto wbar = [&](int b) { return &bars[(gi * NB + b) * 4 + gw]; };
   auto wbuf = [&](int b) { return smem + P.wbuf_off + ((size_t)(gi * NB + b) * 4 + gw) * kslice; };
   int* status = ws_hdr(a) + HDR_STATUS;
@@ -655,7 +652,7 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
   auto unit_of = [&](int jj) { return (int)blockIdx.x + (gi + NG * jj) * G; };
 
   FLINT_TRACE(a, 8);
-  if (threadIdx.x < NG * NB * 4 + 1) mbar_init(&bars[threadIdx.x], 1);
+  if (threadIdx.x < NG * NB * 4) mbar_init(&bars[threadIdx.x], 1);
   fence_mbar_init();
   __syncthreads();
   auto issue_w = [&](int b, int expert, int tile) {
@@ -673,44 +670,62 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
     issue_w(pre, a.E + u / TILES, u % TILES);
     ++pre;
   }
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(xbar, (uint32_t)(a.B * a.H * 2));
-    bulk_g2s(xstage, a.x, (uint32_t)(a.B * a.H * 2), xbar);
-  }
   route_clear(R, a.E);
-  const bool okx = __syncthreads_and(mbar_wait(xbar, 0, status));
-  if (okx) {  // warp w prescales and reorders tokens w, w + nwarps, ...
-    for (int t = warp; t < a.B; t += blockDim.x >> 5) {
-      const uint8_t* src = xstage + (size_t)t * a.H * 2;
-      float mx = 0.f;
+  // Activations: warp w prescales tokens w, w + nwarps, ... and stores them in
+  // fragment order. Read straight from global memory (L2): a row of up to 2048
+  // columns stays in registers between the max and the conversion; wider rows
+  // are read twice.
+  for (int t = warp; t < a.B; t += blockDim.x >> 5) {
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x + (size_t)t * a.H);
+    const int nch = a.H / 256;  // 16-byte chunks per lane
+    uint8_t* dst = xs + (size_t)t * xstride;
+    auto absmax = [&](const uint4& u, float m) {
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16lo(w4[q])), fabsf(bf16hi(w4[q]))));
+      return m;
+    };
+    auto store = [&](const uint4& u, int c, float sc) {
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+      const int col = 8 * (lane + 32 * c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t bits = w4[q];
+        if (FMT == FLINT_MOE_NVFP4) {
+          const __half2 hv = __floats2half2_rn(bf16lo(w4[q]) * sc, bf16hi(w4[q]) * sc);
+          bits = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        *reinterpret_cast<uint32_t*>(dst + 2 * frag_offset_elems(col + 2 * q)) = bits;
+      }
+    };
+    float mx = 0.f;
+    int kx = 0;
+    if (nch <= 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (c < nch) v[c] = ld_cg_v4(src + (lane + 32 * c) * 16);
       if (FMT == FLINT_MOE_NVFP4) {
-        for (int c = lane; c < a.H / 8; c += 32) {
-          const uint4 v = lds128(src + c * 16);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(w4[q])), fabsf(bf16hi(w4[q]))));
-        }
-        mx = warp_max(mx);
+        for (int c = 0; c < 8; ++c)
+          if (c < nch) mx = absmax(v[c], mx);
+        kx = prescale_exp(warp_max(mx));
       }
-      const int kx = FMT == FLINT_MOE_NVFP4 ? prescale_exp(mx) : 0;
       const float sc = exp2i(kx);
-      uint8_t* dst = xs + (size_t)t * xstride;
-      for (int c = lane; c < a.H / 8; c += 32) {
-        const uint4 v = lds128(src + c * 16);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t bits = w4[q];
-          if (FMT == FLINT_MOE_NVFP4) {
-            const __half2 hv = __floats2half2_rn(bf16lo(w4[q]) * sc, bf16hi(w4[q]) * sc);
-            bits = *reinterpret_cast<const uint32_t*>(&hv);
-          }
-          *reinterpret_cast<uint32_t*>(dst + 2 * frag_offset_elems(8 * c + 2 * q)) = bits;
-        }
+      for (int c = 0; c < 8; ++c)
+        if (c < nch) store(v[c], c, sc);
+    } else {
+      if (FMT == FLINT_MOE_NVFP4) {
+        for (int c = 0; c < nch; ++c) mx = absmax(ld_cg_v4(src + (lane + 32 * c) * 16), mx);
+        kx = prescale_exp(warp_max(mx));
       }
-      if (lane == 0) s_inv[t] = exp2i(-kx);
+      const float sc = exp2i(kx);
+      for (int c = 0; c < nch; ++c) store(ld_cg_v4(src + (lane + 32 * c) * 16), c, sc);
     }
+    if (lane == 0) s_inv[t] = exp2i(-kx);
   }
+  __syncthreads();  // route_clear before the selection's atomics
   pdl_wait();
   pdl_trigger();
   FLINT_TRACE(a, 9);
@@ -738,7 +753,7 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
       for (int nt = 0; nt < NTMAX; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
-    const bool ok = mbar_wait(wbar(b), par, status) && okx;
+    const bool ok = mbar_wait(wbar(b), par, status);
     if (jj == 0) FLINT_TRACE(a, 11);
     if (ok) {
       int tok[NTMAX];  // column g of token tile nt is token 8 nt + g (past B: a repeat of token B - 1)
