@@ -19,8 +19,9 @@ routing and combine fused into the GEMVs). For one token x (bf16 values):
 
 Readings where the pages are silent: renormalisation, the selection bias, the
 intermediate size and the rounding points come from the workload definition; the shared expert is unweighted and has the routed
-experts' intermediate size; there is no residual add inside the layer; tokens
-are routed independently. For BF16 expert weights c is the bf16 weight and G = 1.
+experts' intermediate size; there is no residual add inside the layer (the
+pre-norm block below adds it around the layer); tokens are routed
+independently. For BF16 expert weights c is the bf16 weight and G = 1.
 """
 from __future__ import annotations
 
@@ -185,6 +186,35 @@ def moe_layer(x: np.ndarray, router: np.ndarray, get_expert, cfg: Config,
             acc += expert(x[t:t + 1], weights(cfg.num_experts + s))[0]
         out[row] = bf16_round(f32(acc))
     return out, routing
+
+
+# ------------------------------------------------------------ pre-norm block
+
+def rmsnorm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm of every row of x (bf16 values) with weight gamma (bf16 values),
+    rounded to bf16: y = bf16(x * gamma / sqrt(mean(x^2) + eps)), float64 inside.
+
+    The pages describe Flint as a pre-norm MoE ("Day-0 Support for Flint on
+    vLLM", section "Model architecture") whose norm kernels follow the reference
+    rounding (section "Optimisation") without printing the norm; the plain RMS
+    normalisation with a learned per-channel weight is the reading, its output
+    rounded to bf16 because it is the layer's bf16 activation."""
+    x = np.asarray(x, dtype=np.float64)
+    g = np.asarray(gamma, dtype=np.float64)
+    ms = np.mean(x * x, axis=1, keepdims=True)
+    return bf16_round(x / np.sqrt(ms + np.float64(eps)) * g[None, :])
+
+
+def moe_block(r: np.ndarray, router: np.ndarray, get_expert, cfg: Config, gamma: np.ndarray, eps: float,
+              bias: np.ndarray | None = None, tokens=None):
+    """One pre-norm MoE sublayer on the residual stream r (bf16 values):
+    r' = bf16(r + moe_layer(rmsnorm(r))), the layer output being bf16 already.
+
+    Returns (r' float64 bf16 values [len(tokens), H], Routing)."""
+    r = np.asarray(r, dtype=np.float64)
+    tokens = list(range(r.shape[0])) if tokens is None else list(tokens)
+    out, routing = moe_layer(rmsnorm(r, gamma, eps), router, get_expert, cfg, bias, tokens)
+    return bf16_round(r[tokens] + out), routing
 
 
 def distinct_experts(routing: Routing) -> int:

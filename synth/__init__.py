@@ -50,6 +50,7 @@ UP = 3
 DOWN = 4
 X = 5
 BIAS = 6
+NORM = 7
 
 
 def _mix_scalar(z: int) -> int:
@@ -145,3 +146,9 @@ def expert_f32(seed: int, layer: int, expert: int, hidden: int, inter: int, sigm
 def bias_f32(seed: int, layer: int, num_experts: int, sigma: float) -> np.ndarray:
     key = stream_key(seed, layer, BIAS, 0)
     return normal_scaled_f32(key, 0, num_experts, sigma)
+
+
+def norm_bf16(seed: int, layer: int, hidden: int, sigma: float = 0.1) -> np.ndarray:
+    """RMSNorm weight of a layer: bf16 bits of float32(1 + sigma * N(0, 1))."""
+    key = stream_key(seed, layer, NORM, 0)
+    return f32_to_bf16_bits(np.float32(1.0) + normal_scaled_f32(key, 0, hidden, sigma))

@@ -379,3 +379,56 @@ def test_tiny_layer_regression_record():
     assert r.idx[0].tolist() == [int(v) for v in rec["idx"]]
     assert r.w[0].tolist() == [float(v) for v in rec["w"]]
     assert moe.f64_to_bf16_bits(out[0]).tolist() == [int(v, 16) for v in rec["out_bf16_hex"]]
+
+
+# ------------------------------------------------------------------ pre-norm block
+
+def test_rmsnorm_matches_torch_rms_norm():
+    """The normalisation against torch's rms_norm in float64 (a library
+    routine), both rounded by the same bf16 rounding."""
+    H = 256
+    x = moe.bf16_bits_to_f64(synth.x_bf16(3, 0, 5, H))
+    g = moe.bf16_bits_to_f64(synth.norm_bf16(3, 0, H))
+    for eps in (1e-6, 0.5):
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (H,), weight=torch.from_numpy(g), eps=eps).numpy()
+        assert np.array_equal(moe.rmsnorm(x, g, eps), moe.bf16_round(ref))
+
+
+def test_rmsnorm_closed_forms():
+    H = 256
+    g = np.ones(H)
+    # a constant row normalises to its sign (eps = 0)
+    assert np.array_equal(moe.rmsnorm(np.full((1, H), -3.0), g, 0.0), np.full((1, H), -1.0))
+    # one nonzero element v: mean square v^2 / H, so it becomes sign(v) * sqrt(H) = 16
+    x = np.zeros((1, H))
+    x[0, 7] = 0.375
+    y = moe.rmsnorm(x, g, 0.0)
+    assert y[0, 7] == 16.0 and np.count_nonzero(y) == 1
+    # the weight multiplies channel by channel
+    gw = moe.bf16_bits_to_f64(synth.norm_bf16(1, 0, H))
+    assert np.array_equal(moe.rmsnorm(np.full((1, H), 2.0), gw, 0.0)[0], moe.bf16_round(gw))
+
+
+def test_rmsnorm_is_scale_invariant():
+    """Scaling a row by a power of two changes nothing when eps = 0 (exact)."""
+    H = 512
+    x = moe.bf16_bits_to_f64(synth.x_bf16(4, 0, 3, H))
+    g = moe.bf16_bits_to_f64(synth.norm_bf16(4, 0, H))
+    for k in (-6, 5):
+        assert np.array_equal(moe.rmsnorm(x * 2.0 ** k, g, 0.0), moe.rmsnorm(x, g, 0.0))
+
+
+def test_moe_block_with_zero_experts_is_the_identity():
+    """With every expert weight zero the layer adds exactly zero, so the block
+    returns the residual stream unchanged; the routing still happens on the
+    normalised input (the same selection as routing rmsnorm(r) directly)."""
+    cfg = moe.Config(hidden=256, num_experts=16, top_k=2, inter=64, n_shared=1)
+    zero = nvfp4.quantize(np.zeros((64, 256), np.float32))
+    zero_d = nvfp4.quantize(np.zeros((256, 64), np.float32))
+    get = lambda e: (moe.NVFP4Matrix(*zero), moe.NVFP4Matrix(*zero), moe.NVFP4Matrix(*zero_d))  # noqa: E731
+    r = moe.bf16_bits_to_f64(synth.x_bf16(5, 0, 3, 256)) * 8.0  # still bf16 values
+    router = moe.bf16_bits_to_f64(synth.router_bf16(5, 0, 16, 256))
+    g = moe.bf16_bits_to_f64(synth.norm_bf16(5, 0, 256))
+    out, routing = moe.moe_block(r, router, get, cfg, g, 1e-6)
+    assert np.array_equal(out, r)
+    assert np.array_equal(routing.idx, moe.route(moe.rmsnorm(r, g, 1e-6), router, cfg).idx)
