@@ -368,14 +368,15 @@ def gpu_arm(args) -> None:
         return max_over_ranks(e0.elapsed_time(e1)) * 1000.0 / steps
 
     def stack_leg(batches=(1, 2, 4, 8, 16, 32), passes=20):
-        """The 47-layer stack: distinct layers (generator seed 1000 + L), the
-        output of layer L is the input of layer L + 1, routing skewed by a
-        selection bias on experts 0..25; per batch, the median over `passes`
-        replays of the whole stack (one CUDA graph, PDL between all kernels)."""
+        """The 47-layer stack: distinct layers (generator seed 1000 + L) as
+        pre-norm sublayers of one residual stream, r_{L+1} = r_L +
+        layer_L(rmsnorm_L(r_L)), routing skewed by a selection bias on experts
+        0..25; per batch, the median over `passes` replays of the whole stack
+        (one CUDA graph, PDL between all kernels)."""
         beta, nb = stack_bias()
         bias = torch.zeros(cfg.num_experts, dtype=torch.float32, device=dev)
         bias[:nb] = beta
-        stack = [layers.synth_layer(cfg, 1000 + L, L, dev, bias=bias) for L in range(P)]
+        stack = [layers.synth_layer(cfg, 1000 + L, L, dev, bias=bias, norm_eps=layers.NORM_EPS) for L in range(P)]
         ws_s = layers.workspace(cfg, max(batches), dev)
         res = {}
         for Bs in batches:
@@ -385,7 +386,7 @@ def gpu_arm(args) -> None:
             w = torch.empty(Bs, cfg.top_k, dtype=torch.float32, device=dev)
             dl, picks, biased = [], 0, 0
             for L in range(P):  # one eager pass: distinct experts and skew per layer
-                fb.flint_moe_decode(stack[L].handle, bufs[L], Bs, bufs[L + 1], ws_s)
+                fb.flint_moe_decode_prenorm(stack[L].handle, bufs[L], Bs, bufs[L + 1], ws_s)
                 fb.flint_moe_debug_routing(cfg, ws_s, Bs, idx, w)
                 ii = idx.cpu().numpy().ravel()
                 dl.append(len(set(ii.tolist())))
@@ -400,7 +401,7 @@ def gpu_arm(args) -> None:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
                     for L in range(P):
-                        fb.flint_moe_decode(stack[L].handle, bufs[L], Bs, bufs[L + 1], ws_s, stream)
+                        fb.flint_moe_decode_prenorm(stack[L].handle, bufs[L], Bs, bufs[L + 1], ws_s, stream)
                 for _ in range(3):
                     g.replay()
                 stream.synchronize()
@@ -422,8 +423,10 @@ def gpu_arm(args) -> None:
             del bufs
         del stack, ws_s
         torch.cuda.empty_cache()
-        return {"workload": f"{P} chained Flint-shape NVFP4 layers (generator seeds 1000 + L), output of layer L is "
-                            f"the input of layer L + 1, selection bias {beta:.6g} on experts 0..{nb - 1}",
+        return {"workload": f"{P} Flint-shape NVFP4 layers (generator seeds 1000 + L) chained as pre-norm sublayers "
+                            f"of one residual stream (RMSNorm eps {layers.NORM_EPS:g} in the router and gate/up "
+                            f"kernels, residual add in the down kernel), selection bias {beta:.6g} on experts "
+                            f"0..{nb - 1}",
                 "timing": f"median of {passes} replays of the whole stack (one CUDA graph), us per layer = "
                           f"stack time / {P}",
                 "beta": beta, "per_batch": res}

@@ -115,6 +115,8 @@ typedef struct flint_moe_layer {
   const void* packed;        /* flint_moe_pack output, 16-byte aligned */
   const uint16_t* router;    /* bf16 [E][H], row-major, 16-byte aligned */
   const float* sel_bias;     /* float32 [E] added to the keys for selection only; may be NULL */
+  const uint16_t* norm_weight; /* bf16 [H] pre-norm RMSNorm weight (flint_moe_layer_set_norm), or NULL */
+  float norm_eps;              /* RMSNorm epsilon */
 } flint_moe_layer;
 
 /* Checks a configuration; FLINT_MOE_OK if this build supports it. */
@@ -159,6 +161,12 @@ flint_moe_status flint_moe_layer_init(const flint_moe_config* cfg, const void* p
                                       const uint16_t* router_bf16, const float* sel_bias,
                                       flint_moe_layer* out_layer);
 
+/* Gives a layer its pre-norm RMSNorm (needed by flint_moe_decode_prenorm):
+ * norm_weight bf16 [H] (device, 16-byte aligned, not owned), eps >= 0 and
+ * finite, else FLINT_MOE_EINVAL / FLINT_MOE_EALIGN. */
+flint_moe_status flint_moe_layer_set_norm(flint_moe_layer* layer, const uint16_t* norm_weight_bf16,
+                                          float eps);
+
 /* One decode step of the MoE layer for B tokens (0 <= B <= 32; B = 0 is a
  * no-op). x: bf16 [B][H]; out: bf16 [B][H]; workspace: flint_moe_workspace_bytes
  * (cfg, >= B) bytes, initialised once with flint_moe_workspace_init, not shared
@@ -174,6 +182,21 @@ flint_moe_status flint_moe_layer_init(const flint_moe_config* cfg, const void* p
 flint_moe_status flint_moe_decode(const flint_moe_layer* layer, const uint16_t* x_bf16,
                                   int32_t B, uint16_t* out_bf16, void* workspace,
                                   cudaStream_t stream);
+
+/* The layer as a pre-norm sublayer of the residual stream ("Day-0 Support for
+ * Flint on vLLM", section "Model architecture": a pre-norm MoE; section
+ * "Optimisation": norm kernels with the reference rounding). For every token
+ * row r (bf16 [B][H]):
+ *   x  = bf16(r * w / sqrt(mean(r^2) + eps))   (RMSNorm, w = norm_weight)
+ *   r' = bf16(r + flint_moe_decode(x))          (the layer output is bf16)
+ * The norm runs inside the router and gate/up kernels, the residual add inside
+ * the down kernel: still three kernels, no extra pass over memory.
+ * residual_out may be residual_in (in-place update) but must not overlap it
+ * otherwise. FLINT_MOE_EINVAL if the layer has no norm weight. Otherwise as
+ * flint_moe_decode. */
+flint_moe_status flint_moe_decode_prenorm(const flint_moe_layer* layer, const uint16_t* residual_in_bf16,
+                                          int32_t B, uint16_t* residual_out_bf16, void* workspace,
+                                          cudaStream_t stream);
 
 /* Copies the routing of the last decode from the workspace: idx int32 [B][k]
  * and w float32 [B][k] (device pointers), in selection order. */

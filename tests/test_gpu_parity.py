@@ -273,6 +273,46 @@ def test_flint_stack_chain_graph_equals_serial():
     assert st == fb.OK and bits == 0
 
 
+def run_parity_prenorm(d, B, seed=0, layer=0, tokens=None, bias=None, inplace=False, scale=8.0):
+    """The pre-norm block r' = r + layer(rmsnorm(r)) against the oracle; the
+    residual stream is the seeded x times a power of two (still bf16)."""
+    cfg = cfg_of(d)
+    bias_t = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).to(DEV)
+    dl = layers.synth_layer(cfg, seed, layer, DEV, bias=bias_t, norm_eps=1e-6)
+    r = (layers.synth_x(B, cfg.hidden, seed, layer, DEV).view(torch.bfloat16) * scale).view(torch.int16)
+    r_in = r.clone()
+    out = r if inplace else torch.full_like(r, 0x7FC0)
+    ws = layers.workspace(cfg, B, DEV)
+    fb.flint_moe_decode_prenorm(dl.handle, r, B, out, ws)
+    idx = torch.empty(B, cfg.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(B, cfg.top_k, dtype=torch.float32, device=DEV)
+    fb.flint_moe_debug_routing(cfg, ws, B, idx, w)
+    st, bits = fb.flint_moe_read_status(ws)
+    assert st == fb.OK and bits == 0
+    xo, router = oracle_inputs(d, seed, layer, B)
+    ro = xo * scale
+    assert np.array_equal(bits_to_f64(r_in), ro)  # both generators drew the same residual stream
+    gamma = moe.bf16_bits_to_f64(synth.norm_bf16(seed, layer, d["hidden"]))
+    assert np.array_equal(bits_to_f64(dl.norm), gamma)
+    tokens = list(range(B)) if tokens is None else tokens
+    ref, routing = moe.moe_block(ro, router, oracle_experts(d, seed, layer), oracle_config(d), gamma, 1e-6, bias,
+                                 tokens)
+    excluded = check_routing(routing, idx.cpu().numpy(), w.cpu().numpy(), tokens)
+    keep = [i for i, t in enumerate(tokens) if t not in excluded]
+    check_out(ref[keep], bits_to_f64(out)[tokens][keep], f"prenorm B={B} seed={seed}")
+    return routing
+
+
+@pytest.mark.parametrize("B,seed,inplace", [(1, 20, False), (3, 21, True), (32, 22, False)])
+def test_decode_prenorm_tiny(B, seed, inplace):
+    run_parity_prenorm(TINY, B, seed, inplace=inplace)
+
+
+def test_decode_prenorm_flint():
+    run_parity_prenorm(FLINT, 1, seed=23)
+    run_parity_prenorm(FLINT, 8, seed=1004, layer=4, tokens=[2, 6], bias=_stack_bias_vector(), inplace=True)
+
+
 def test_decode_batch0_is_a_noop():
     cfg = cfg_of(TINY)
     dl = layers.synth_layer(cfg, 0, 0, DEV)

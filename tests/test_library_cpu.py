@@ -115,6 +115,21 @@ def test_rcp_check_rejects_ranges_outside_its_domain(lib):
     assert L.flint_moe_debug_rcp_check(0x3F800000, 0x3F800010, None, None) == fb.EINVAL
 
 
+def test_prenorm_needs_a_norm_weight(lib):
+    c = flint_cfg()
+    L = fb.lib()
+    layer = fb.flint_moe_layer()
+    assert L.flint_moe_layer_init(ctypes.byref(c), 0x10000, 0x20000, None, ctypes.byref(layer)) == fb.OK
+    assert layer.norm_weight is None
+    assert L.flint_moe_decode_prenorm(ctypes.byref(layer), 0x30000, 1, 0x30000, 0x50000, None) == fb.EINVAL
+    assert L.flint_moe_layer_set_norm(ctypes.byref(layer), 0x60008, ctypes.c_float(1e-6)) == fb.EALIGN
+    assert L.flint_moe_layer_set_norm(ctypes.byref(layer), 0x60000, ctypes.c_float(float("nan"))) == fb.EINVAL
+    assert L.flint_moe_layer_set_norm(ctypes.byref(layer), 0x60000, ctypes.c_float(-1.0)) == fb.EINVAL
+    assert L.flint_moe_layer_set_norm(ctypes.byref(layer), 0x60000, ctypes.c_float(1e-6)) == fb.OK
+    assert layer.norm_weight == 0x60000 and abs(layer.norm_eps - 1e-6) < 1e-12
+    assert L.flint_moe_decode_prenorm(ctypes.byref(layer), 0x30000, 0, 0x30000, 0x50000, None) == fb.OK  # B = 0
+
+
 def test_layer_init_and_pack_validate(lib):
     c = flint_cfg()
     layer = fb.flint_moe_layer()

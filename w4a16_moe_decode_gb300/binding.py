@@ -24,7 +24,7 @@ NVFP4, BF16 = 0, 1
 DEV_ERR_TIMEOUT, DEV_ERR_NAN_SCALE, DEV_ERR_SLOTS = 1, 2, 4
 
 # synth tensor tags (same numbering as the CPU generator)
-ROUTER, GATE, UP, DOWN, X, BIAS = 1, 2, 3, 4, 5, 6
+ROUTER, GATE, UP, DOWN, X, BIAS, NORM = 1, 2, 3, 4, 5, 6, 7
 
 
 class FlintMoeError(RuntimeError):
@@ -49,7 +49,8 @@ class flint_moe_src(ctypes.Structure):
 
 
 class flint_moe_layer(ctypes.Structure):
-    _fields_ = [("cfg", flint_moe_config), ("packed", c_void_p), ("router", c_void_p), ("sel_bias", c_void_p)]
+    _fields_ = [("cfg", flint_moe_config), ("packed", c_void_p), ("router", c_void_p), ("sel_bias", c_void_p),
+                ("norm_weight", c_void_p), ("norm_eps", ctypes.c_float)]
 
 
 _lib = None
@@ -72,6 +73,9 @@ def lib() -> ctypes.CDLL:
             "flint_moe_unpack_debug": (c_int32, [P(flint_moe_config), c_void_p, P(flint_moe_src), c_void_p]),
             "flint_moe_layer_init": (c_int32, [P(flint_moe_config), c_void_p, c_void_p, c_void_p, P(flint_moe_layer)]),
             "flint_moe_decode": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
+            "flint_moe_layer_set_norm": (c_int32, [P(flint_moe_layer), c_void_p, ctypes.c_float]),
+            "flint_moe_decode_prenorm": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p,
+                                                   c_void_p]),
             "flint_moe_decode_noalloc": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p]),
             "flint_moe_debug_routing": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
             "flint_moe_debug_dequant": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
@@ -174,6 +178,18 @@ def flint_moe_layer_init(cfg, packed, router, sel_bias=None) -> flint_moe_layer:
 def flint_moe_decode(layer: flint_moe_layer, x, B: int, out, workspace, stream=None) -> None:
     _check("flint_moe_decode", lib().flint_moe_decode(ctypes.byref(layer), _ptr(x), B, _ptr(out), _ptr(workspace),
                                                       _stream(stream)))
+
+
+def flint_moe_layer_set_norm(layer: flint_moe_layer, norm_weight, eps: float) -> None:
+    _check("flint_moe_layer_set_norm", lib().flint_moe_layer_set_norm(ctypes.byref(layer), _ptr(norm_weight),
+                                                                      float(eps)))
+
+
+def flint_moe_decode_prenorm(layer: flint_moe_layer, residual_in, B: int, residual_out, workspace,
+                             stream=None) -> None:
+    _check("flint_moe_decode_prenorm", lib().flint_moe_decode_prenorm(ctypes.byref(layer), _ptr(residual_in), B,
+                                                                      _ptr(residual_out), _ptr(workspace),
+                                                                      _stream(stream)))
 
 
 def flint_moe_decode_noalloc(layer: flint_moe_layer, x, B: int, out, stream=None) -> None:

@@ -47,6 +47,11 @@ struct DecodeArgs {
   WsLayout W;
   int gu_nb;      // gate/up weight buffers in flight per warp group (1..3)
   int trace_seq;  // decode call number, used only by trace builds
+  // Pre-norm sublayer: x is the residual stream, normalised (RMSNorm with
+  // weight gamma) on the way in, added to the layer output on the way out.
+  int prenorm;
+  const uint16_t* gamma;
+  float eps;
 };
 
 __device__ __forceinline__ int* ws_hdr(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws); }
@@ -88,6 +93,38 @@ __device__ __forceinline__ float dot8_bf16(const uint4 w, const uint4 x, float a
   acc = fmaf(bf16lo(w.w), bf16lo(x.w), acc);
   acc = fmaf(bf16hi(w.w), bf16hi(x.w), acc);
   return acc;
+}
+
+// RMSNorm pieces shared by the router and the gate/up kernel, so both derive
+// bit-identical normalised activations: lane l owns the 16-byte chunks
+// l, l + 32, ... of a row; its sum of squares runs over them in that order,
+// the warp total is a butterfly (the same value in every lane), then
+// 1 / sqrt(mean + eps) with IEEE square root and division, and each value
+// becomes bf16((x * inv) * w).
+__device__ __forceinline__ float sumsq8(const uint4 u, float acc) {
+  acc = fmaf(bf16lo(u.x), bf16lo(u.x), acc);
+  acc = fmaf(bf16hi(u.x), bf16hi(u.x), acc);
+  acc = fmaf(bf16lo(u.y), bf16lo(u.y), acc);
+  acc = fmaf(bf16hi(u.y), bf16hi(u.y), acc);
+  acc = fmaf(bf16lo(u.z), bf16lo(u.z), acc);
+  acc = fmaf(bf16hi(u.z), bf16hi(u.z), acc);
+  acc = fmaf(bf16lo(u.w), bf16lo(u.w), acc);
+  acc = fmaf(bf16hi(u.w), bf16hi(u.w), acc);
+  return acc;
+}
+
+__device__ __forceinline__ float rms_inv(float part, int H, float eps) {
+  const float ss = warp_sum(part);
+  return 1.0f / sqrtf(ss / (float)H + eps);
+}
+
+__device__ __forceinline__ uint32_t norm2(uint32_t x, uint32_t w, float inv) {
+  const __nv_bfloat162 r = __floats2bfloat162_rn((bf16lo(x) * inv) * bf16lo(w), (bf16hi(x) * inv) * bf16hi(w));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint4 norm8(const uint4 x, const uint4 w, float inv) {
+  return make_uint4(norm2(x.x, w.x, inv), norm2(x.y, w.y, inv), norm2(x.z, w.z, inv), norm2(x.w, w.w, inv));
 }
 
 // ===========================================================================
@@ -462,21 +499,23 @@ __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* 
 
 template <int NCH>
 __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t dsm[];  // router rows [4][H], then x chunk [<= 8][H] (bf16)
+  extern __shared__ __align__(128) uint8_t dsm[];  // router rows [4][H], norm weight [H], x chunk [<= 8][H]
   __shared__ __align__(8) uint64_t bars[2];        // 0: router rows, 1: x
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e0 = blockIdx.x * 4, e = e0 + warp;
   const int nrows = min(4, a.E - e0);
   uint8_t* wsm = dsm;
-  uint8_t* xsm = dsm + (size_t)4 * a.H * 2;
+  uint8_t* gsm = dsm + (size_t)4 * a.H * 2;
+  uint8_t* xsm = gsm + (size_t)a.H * 2;
   FLINT_TRACE(a, 0);
   if (threadIdx.x == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     fence_mbar_init();
     const uint32_t bytes = (uint32_t)nrows * a.H * 2;
-    mbar_arrive_expect_tx(&bars[0], bytes);
+    mbar_arrive_expect_tx(&bars[0], bytes + (a.prenorm ? (uint32_t)a.H * 2 : 0u));
     bulk_g2s(wsm, a.router + (size_t)e0 * a.H, bytes, &bars[0]);
+    if (a.prenorm) bulk_g2s(gsm, a.gamma, (uint32_t)a.H * 2, &bars[0]);
   }
   // Two passes at one call site: a dry one on zeroed activations before the
   // dependency wait (no stores), which brings the dot-product code into this
@@ -514,6 +553,21 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
         phase ^= 1;
         if (!ok) break;
         FLINT_TRACE(a, 2);
+        if (a.prenorm) {  // RMSNorm of the chunk's rows, in place
+          for (int t = warp; t < nt; t += 4) {
+            uint8_t* row = xsm + (size_t)t * a.H * 2;
+            float part = 0.f;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) part = sumsq8(lds128(row + (lane + 32 * c) * 16), part);
+            const float inv = rms_inv(part, a.H, a.eps);
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+              const int off = (lane + 32 * c) * 16;
+              *reinterpret_cast<uint4*>(row + off) = norm8(lds128(row + off), lds128(gsm + off), inv);
+            }
+          }
+          __syncthreads();
+        }
       }
       if (e < a.E) {
         float* lgc = lg + (size_t)t0 * a.E;
@@ -698,6 +752,7 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
         *reinterpret_cast<uint32_t*>(dst + 2 * frag_offset_elems(col + 2 * q)) = bits;
       }
     };
+    const uint8_t* gw8 = reinterpret_cast<const uint8_t*>(a.gamma);
     float mx = 0.f;
     int kx = 0;
     if (nch <= 8) {
@@ -705,6 +760,17 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         if (c < nch) v[c] = ld_cg_v4(src + (lane + 32 * c) * 16);
+      if (a.prenorm) {  // RMSNorm, as the router computes it
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < nch) part = sumsq8(v[c], part);
+        const float inv = rms_inv(part, a.H, a.eps);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < nch)
+            v[c] = norm8(v[c], __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), inv);
+      }
       if (FMT == FLINT_MOE_NVFP4) {
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -716,12 +782,22 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
       for (int c = 0; c < 8; ++c)
         if (c < nch) store(v[c], c, sc);
     } else {
+      float inv = 1.f;
+      if (a.prenorm) {
+        float part = 0.f;
+        for (int c = 0; c < nch; ++c) part = sumsq8(ld_cg_v4(src + (lane + 32 * c) * 16), part);
+        inv = rms_inv(part, a.H, a.eps);
+      }
+      auto chunk = [&](int c) {
+        const uint4 u = ld_cg_v4(src + (lane + 32 * c) * 16);
+        return a.prenorm ? norm8(u, __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), inv) : u;
+      };
       if (FMT == FLINT_MOE_NVFP4) {
-        for (int c = 0; c < nch; ++c) mx = absmax(ld_cg_v4(src + (lane + 32 * c) * 16), mx);
+        for (int c = 0; c < nch; ++c) mx = absmax(chunk(c), mx);
         kx = prescale_exp(warp_max(mx));
       }
       const float sc = exp2i(kx);
-      for (int c = 0; c < nch; ++c) store(ld_cg_v4(src + (lane + 32 * c) * 16), c, sc);
+      for (int c = 0; c < nch; ++c) store(chunk(c), c, sc);
     }
     if (lane == 0) s_inv[t] = exp2i(-kx);
   }
@@ -1064,8 +1140,13 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
     const int t = p >> 4, r = p & 15;
     float v = 0.f;
     for (int w2 = 0; w2 < nw; ++w2) v += acc_s[(w2 * a.B + t) * 16 + r];
-    const __nv_bfloat16 o = __float2bfloat16_rn(v);
-    a.out[(size_t)t * a.H + tile * 16 + r] = *reinterpret_cast<const uint16_t*>(&o);
+    __nv_bfloat16 o = __float2bfloat16_rn(v);
+    const size_t at = (size_t)t * a.H + tile * 16 + r;
+    if (a.prenorm) {  // residual stream: r + bf16(layer output), rounded to bf16
+      const uint32_t rb = (uint32_t)__ldcg(a.x + at) << 16;
+      o = __float2bfloat16_rn(__uint_as_float(rb) + __bfloat162float(o));
+    }
+    a.out[at] = *reinterpret_cast<const uint16_t*>(&o);
   }
   FLINT_TRACE(a, 20);
 }
@@ -1086,8 +1167,9 @@ constexpr size_t SMEM_LIMIT = 227 * 1024;
 
 // 8 warps keep more down tiles in flight for small batches; larger batches and
 // BF16 tiles (16 KB each) need the shared memory for fewer, deeper buffers.
-// Router rows of one block (4 experts) plus one x chunk of up to 8 tokens.
-size_t router_smem(int H, int B) { return (size_t)(4 + (B < 8 ? B : 8)) * H * 2; }
+// Router rows of one block (4 experts), the norm weight and one x chunk of up
+// to 8 tokens.
+size_t router_smem(int H, int B) { return (size_t)(5 + (B < 8 ? B : 8)) * H * 2; }
 
 int down_warps(int B, int fmt) { return (B <= 4 && fmt == FLINT_MOE_NVFP4) ? 8 : 4; }
 
@@ -1221,11 +1303,38 @@ extern "C" flint_moe_status flint_moe_layer_init(const flint_moe_config* c, cons
   out->packed = packed;
   out->router = router;
   out->sel_bias = sel_bias;
+  out->norm_weight = nullptr;
+  out->norm_eps = 0.f;
   return FLINT_MOE_OK;
 }
 
+extern "C" flint_moe_status flint_moe_layer_set_norm(flint_moe_layer* layer, const uint16_t* w, float eps) {
+  if (!layer || !w || !(eps >= 0.f) || !(eps <= 3.0e38f)) return FLINT_MOE_EINVAL;
+  if (!aligned16(w)) return FLINT_MOE_EALIGN;
+  layer->norm_weight = w;
+  layer->norm_eps = eps;
+  return FLINT_MOE_OK;
+}
+
+namespace {
+flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, int32_t B, uint16_t* out, void* ws,
+                             cudaStream_t stream, bool prenorm);
+}  // namespace
+
 extern "C" flint_moe_status flint_moe_decode(const flint_moe_layer* layer, const uint16_t* x, int32_t B,
                                              uint16_t* out, void* ws, cudaStream_t stream) {
+  return decode_impl(layer, x, B, out, ws, stream, false);
+}
+
+extern "C" flint_moe_status flint_moe_decode_prenorm(const flint_moe_layer* layer, const uint16_t* r_in, int32_t B,
+                                                     uint16_t* r_out, void* ws, cudaStream_t stream) {
+  if (!layer || !layer->norm_weight) return FLINT_MOE_EINVAL;
+  return decode_impl(layer, r_in, B, r_out, ws, stream, true);
+}
+
+namespace {
+flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, int32_t B, uint16_t* out, void* ws,
+                             cudaStream_t stream, bool prenorm) {
   if (!layer) return FLINT_MOE_EINVAL;
   const flint_moe_config* c = &layer->cfg;
   const flint_moe_status st = flint_moe_check_config(c);
@@ -1256,6 +1365,10 @@ extern "C" flint_moe_status flint_moe_decode(const flint_moe_layer* layer, const
   // The workspace is laid out for the batch of this call; callers size it for
   // their largest batch, which is at least as large.
   a.W = make_ws_layout(a.H, a.E, a.k, a.I, a.S, B);
+  a.prenorm = prenorm ? 1 : 0;
+  a.gamma = prenorm ? layer->norm_weight : nullptr;
+  a.eps = prenorm ? layer->norm_eps : 0.f;
+  if (prenorm && !aligned16(a.gamma)) return FLINT_MOE_EALIGN;
 #ifdef FLINT_MOE_TRACE
   static std::atomic<int> trace_calls{0};
   a.trace_seq = trace_calls.fetch_add(1);
@@ -1280,6 +1393,7 @@ extern "C" flint_moe_status flint_moe_decode(const flint_moe_layer* layer, const
                                                        : launch_down<FLINT_MOE_BF16>(a, stream);
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
 }
+}  // namespace
 
 extern "C" flint_moe_status flint_moe_trace(int32_t op, uint64_t* host_events, cudaStream_t stream) {
 #ifdef FLINT_MOE_TRACE

@@ -15,6 +15,8 @@ from . import binding as fb
 
 WEIGHT_SIGMA = 0.02
 ROUTER_SIGMA = 0.02
+NORM_SIGMA = 0.1
+NORM_EPS = 1e-6
 
 
 @dataclass
@@ -25,6 +27,7 @@ class DeviceLayer:
     bias: torch.Tensor | None
     handle: fb.flint_moe_layer
     canonical: dict = field(default_factory=dict)
+    norm: torch.Tensor | None = None
 
 
 def _fill_normal(out: torch.Tensor, seed: int, layer: int, tensor: int, expert: int, sigma: float, bf16: bool,
@@ -45,6 +48,13 @@ def synth_x(B: int, hidden: int, seed: int, layer: int, device) -> torch.Tensor:
     for t in range(B):
         _fill_normal(x[t], seed, layer, fb.X, t, 1.0, True)
     return x
+
+
+def synth_norm(hidden: int, seed: int, layer: int, device) -> torch.Tensor:
+    """RMSNorm weight: bf16 bits of float32(1 + 0.1 * N(0, 1))."""
+    n = torch.empty(hidden, dtype=torch.float32, device=device)
+    _fill_normal(n, seed, layer, fb.NORM, 0, NORM_SIGMA, False)
+    return (1.0 + n).to(torch.bfloat16).view(torch.int16)
 
 
 def synth_canonical(cfg, seed: int, layer: int, device) -> dict:
@@ -74,7 +84,8 @@ def synth_canonical(cfg, seed: int, layer: int, device) -> dict:
 
 
 def synth_layer(cfg, seed: int, layer: int = 0, device="cuda", bias: torch.Tensor | None = None,
-                keep_canonical: bool = False) -> DeviceLayer:
+                keep_canonical: bool = False, norm_eps: float | None = None) -> DeviceLayer:
+    """A packed layer; with norm_eps it also gets a pre-norm RMSNorm weight."""
     canon = synth_canonical(cfg, seed, layer, device)
     packed = torch.empty(fb.flint_moe_packed_bytes(cfg), dtype=torch.uint8, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -83,8 +94,12 @@ def synth_layer(cfg, seed: int, layer: int = 0, device="cuda", bias: torch.Tenso
         raise RuntimeError(f"flint_moe_pack reported device status {int(status.item())}")
     router = synth_router(cfg, seed, layer, device)
     handle = fb.flint_moe_layer_init(cfg, packed, router, bias)
+    norm = None
+    if norm_eps is not None:
+        norm = synth_norm(cfg.hidden, seed, layer, device)
+        fb.flint_moe_layer_set_norm(handle, norm, norm_eps)
     return DeviceLayer(cfg=cfg, packed=packed, router=router, bias=bias, handle=handle,
-                       canonical=canon if keep_canonical else {})
+                       canonical=canon if keep_canonical else {}, norm=norm)
 
 
 def workspace(cfg, max_batch: int, device="cuda") -> torch.Tensor:
