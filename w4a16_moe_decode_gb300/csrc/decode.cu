@@ -52,6 +52,9 @@ struct DecodeArgs {
   int prenorm;
   const uint16_t* gamma;
   float eps;
+  int router_epb;  // experts per router block (4, 2 or 1): the block's 4 warps split its tokens
+  int dn_nbuf;     // down tiles in flight per warp
+  int dn_hcap;     // h rows the down kernel stages at a time
 };
 
 __device__ __forceinline__ int* ws_hdr(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws); }
@@ -471,16 +474,20 @@ __device__ __forceinline__ SlotInfo slot_info(const DecodeArgs& a, const RouteSm
 
 // ===========================================================================
 // K1: router GEMV (logits in the workspace); also clears the per-row |h|
-// maxima that k_gateup accumulates. Block b computes experts 4b .. 4b+3, one
-// per warp; their router rows are contiguous, so one bulk copy brings them
-// into shared memory before the dependency wait (they do not depend on x).
+// maxima that k_gateup accumulates. Block b computes experts epb*b ..
+// epb*b + epb - 1 (epb = 4, 2 or 1 as the batch grows); warp w takes expert
+// w % epb for tokens w / epb, w / epb + 4 / epb, ..., so every warp has about
+// as many dot products at any batch size. The block's router rows are
+// contiguous: one bulk copy brings them into shared memory before the
+// dependency wait (they do not depend on x).
 // NCH: 16-byte chunks of a router row per lane (H / 256).
 // ===========================================================================
 // NT tokens' dot products with one router row: lane l takes 16-byte chunks
 // l, l + 32, ...; all NT sums are independent, so their latencies overlap.
+// Tokens t0, t0 + ts, ... (NT of them) of the x chunk.
 template <int NCH, int NT>
 __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* xsm, int H, int lane, float* lg,
-                                            int E, int e, bool dry) {
+                                            int E, int e, int t0, int ts, bool dry) {
   float acc[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t] = 0.f;
@@ -488,12 +495,13 @@ __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* 
   for (int c = 0; c < NCH; ++c) {
     const uint4 w = lds128(wrow + (lane + 32 * c) * 16);
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = dot8_bf16(w, lds128(xsm + (size_t)t * H * 2 + (lane + 32 * c) * 16), acc[t]);
+    for (int t = 0; t < NT; ++t)
+      acc[t] = dot8_bf16(w, lds128(xsm + (size_t)(t0 + t * ts) * H * 2 + (lane + 32 * c) * 16), acc[t]);
   }
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const float v = warp_sum(acc[t]);
-    if (lane == 0 && !dry) lg[t * E + e] = v;
+    if (lane == 0 && !dry) lg[(t0 + t * ts) * E + e] = v;
   }
 }
 
@@ -502,10 +510,11 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t dsm[];  // router rows [4][H], norm weight [H], x chunk [<= 8][H]
   __shared__ __align__(8) uint64_t bars[2];        // 0: router rows, 1: x
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e0 = blockIdx.x * 4, e = e0 + warp;
-  const int nrows = min(4, a.E - e0);
+  const int epb = a.router_epb, G = 4 / epb;  // experts per block, token groups
+  const int e0 = blockIdx.x * epb, e = e0 + warp % epb, tg = warp / epb;
+  const int nrows = min(epb, a.E - e0);
   uint8_t* wsm = dsm;
-  uint8_t* gsm = dsm + (size_t)4 * a.H * 2;
+  uint8_t* gsm = dsm + (size_t)epb * a.H * 2;
   uint8_t* xsm = gsm + (size_t)a.H * 2;
   FLINT_TRACE(a, 0);
   if (threadIdx.x == 0) {
@@ -522,7 +531,7 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
   // SM's instruction caches, then the real one on x.
   int* status = ws_hdr(a) + HDR_STATUS;
   float* lg = ws_logits(a);
-  const uint8_t* wrow = wsm + (size_t)warp * a.H * 2;
+  const uint8_t* wrow = wsm + (size_t)(warp % epb) * a.H * 2;
   {
     const int n = (a.B < 8 ? a.B : 8) * a.H / 8;  // 16-byte words of the first x chunk
     for (int i = threadIdx.x; i < n; i += blockDim.x) reinterpret_cast<uint4*>(xsm)[i] = make_uint4(0, 0, 0, 0);
@@ -569,17 +578,18 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
           __syncthreads();
         }
       }
-      if (e < a.E) {
+      const int ntw = tg < nt ? (nt - tg + G - 1) / G : 0;  // this warp's tokens in the chunk
+      if (e < a.E && ntw > 0) {
         float* lgc = lg + (size_t)t0 * a.E;
-        switch (nt) {  // one code path per token count: no predicated-off work
-          case 1: router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
-          case 2: router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
-          case 3: router_dots<NCH, 3>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
-          case 4: router_dots<NCH, 4>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
-          case 5: router_dots<NCH, 5>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
-          case 6: router_dots<NCH, 6>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
-          case 7: router_dots<NCH, 7>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
-          default: router_dots<NCH, 8>(wrow, xsm, a.H, lane, lgc, a.E, e, dry); break;
+        switch (ntw) {  // one code path per token count: no predicated-off work
+          case 1: router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
+          case 2: router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
+          case 3: router_dots<NCH, 3>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
+          case 4: router_dots<NCH, 4>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
+          case 5: router_dots<NCH, 5>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
+          case 6: router_dots<NCH, 6>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
+          case 7: router_dots<NCH, 7>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
+          default: router_dots<NCH, 8>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
         }
         if (!dry) FLINT_TRACE(a, 7);
       }
@@ -919,18 +929,19 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
 }
 
 // ===========================================================================
-// K3: down GEMV + routing-weighted combine for one tile of 16 output rows.
-// Work items are (slot, chunk of up to 8 of its rows); warp w of nw takes
-// items w, w+nw, ... in order, NBUF of them in flight; per-warp partial sums
-// are added in warp order at the end, so the result does not depend on timing.
+// K3 for small batches (at most 4 tokens, NVFP4): each warp keeps nbuf items
+// in flight, each buffer holding the item's down tile and its h rows, so a
+// warp copies, converts and consumes its own items with no block barrier
+// before the final sum. Measured faster than the staged kernel below at
+// batch 1 (fewer instructions on the cold path after the wait).
 // ===========================================================================
-struct DownSmemPlan {
+struct DownItemsPlan {
   int buf_bytes, hrows, hstride;
   size_t acc_off, items_off, hmax_off, inv_off, bar_off, total;
 };
 
-__host__ __device__ inline DownSmemPlan down_plan(int H, int I, int B, int max_slots, int fmt, int nbuf, int nw) {
-  DownSmemPlan p;
+__host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, int max_slots, int fmt, int nbuf, int nw) {
+  DownItemsPlan p;
   const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
   const int nt = (B + 7) / 8;
   p.hrows = B < 8 ? B : 8;
@@ -949,7 +960,7 @@ __host__ __device__ inline DownSmemPlan down_plan(int H, int I, int B, int max_s
 }
 
 template <int FMT, int NBUF>
-__global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
+__global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   __shared__ int s_wsum[MAX_WARPS];
@@ -958,7 +969,7 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
   const int nw = blockDim.x >> 5;
   const int tile = blockIdx.x;
   const int NT = (a.B + 7) / 8;  // token tiles
-  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, FMT, NBUF, nw);
+  const DownItemsPlan P = down_items_plan(a.H, a.I, a.B, a.W.max_slots, FMT, NBUF, nw);
   const int dn_bytes = (int)a.L.dn_tile;
   float* acc_s = reinterpret_cast<float*>(smem + P.acc_off);
   int* s_items = reinterpret_cast<int*>(smem + P.items_off);  // per item: slot << 16 | tile << 8 | tokens, expert
@@ -1151,6 +1162,292 @@ __global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
   FLINT_TRACE(a, 20);
 }
 
+// ===========================================================================
+// K3: down GEMV + routing-weighted combine for one tile of 16 output rows.
+// Work items are (slot, token tile) pairs with at least one selecting token,
+// slot-major; warp w of nw takes items w, w + nw, ... in order with nbuf down
+// tiles in flight (routing-independent: fetched while k_gateup still runs).
+// The h rows the items read (one per selecting token) are staged once per
+// block, converted to prescaled f16 once, and shared by all warps: in rounds
+// of consecutive items when they do not all fit. Per-warp partial sums are
+// added in warp order at the end, so the result does not depend on timing.
+// ===========================================================================
+struct DownPlan {
+  int nw, nbuf, hcap, hstride;
+  size_t wbuf_off, h_off, acc_off, items_off, hsc_off, hinv_off, bar_off, total;
+};
+
+__host__ __device__ inline DownPlan down_plan(int I, int B, int max_slots, int fmt, int nw, int nbuf, int hcap) {
+  DownPlan p;
+  const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  const int dn = (I / KG_COLS) * kgb;
+  const int nt = (B + 7) / 8;
+  p.nw = nw;
+  p.nbuf = nbuf;
+  p.hcap = hcap;
+  p.hstride = I * 2 + 16;
+  size_t o = 0;
+  p.wbuf_off = o;   o += (size_t)nw * nbuf * dn;
+  p.h_off = o;      o += (size_t)hcap * p.hstride;
+  p.acc_off = o;    o += sizeof(float) * nw * B * 16;
+  p.items_off = o;  o += sizeof(int) * 3 * max_slots * nt;
+  p.hsc_off = o;    o += sizeof(float) * hcap;
+  p.hinv_off = o;   o += sizeof(float) * hcap;
+  o = (o + 15) & ~(size_t)15;
+  p.bar_off = o;    o += sizeof(uint64_t) * nw * (nbuf + 1);
+  p.total = o;
+  return p;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ RouteSmem R;
+  __shared__ int s_wsum[MAX_WARPS];
+  constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int nw = blockDim.x >> 5;
+  const int tile = blockIdx.x;
+  const int NT = (a.B + 7) / 8;  // token tiles
+  const DownPlan P = down_plan(a.I, a.B, a.W.max_slots, FMT, nw, a.dn_nbuf, a.dn_hcap);
+  const int NBUF = P.nbuf;
+  const int dn_bytes = (int)a.L.dn_tile;
+  float* acc_s = reinterpret_cast<float*>(smem + P.acc_off);
+  int* s_items = reinterpret_cast<int*>(smem + P.items_off);  // per item: slot << 16 | tile << 8 | tokens, expert, first row
+  float* s_hsc = reinterpret_cast<float*>(smem + P.hsc_off);  // staged row's max |h|
+  float* s_hinv = reinterpret_cast<float*>(smem + P.hinv_off);  // staged row's inverse prescale
+  uint8_t* hsm = smem + P.h_off;
+  uint64_t* wbars = reinterpret_cast<uint64_t*>(smem + P.bar_off) + warp * NBUF;
+  uint64_t* hbar = reinterpret_cast<uint64_t*>(smem + P.bar_off) + nw * NBUF + warp;  // this warp's h rows
+  auto wbuf = [&](int b) { return smem + P.wbuf_off + (size_t)(warp * NBUF + b) * dn_bytes; };
+  int* status = ws_hdr(a) + HDR_STATUS;
+
+  FLINT_TRACE(a, 16);
+  if (lane < NBUF) mbar_init(&wbars[lane], 1);
+  if (lane == 0) mbar_init(hbar, 1);
+  fence_mbar_init();
+  for (int i = threadIdx.x; i < nw * a.B * 16; i += blockDim.x) acc_s[i] = 0.f;
+  route_clear(R, a.E);
+  __syncthreads();
+
+  auto issue_weights = [&](int j, int expert) {
+    if (lane == 0) {
+      const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + a.L.gu_bytes + (int64_t)tile * dn_bytes;
+      mbar_arrive_expect_tx(&wbars[j % NBUF], (uint32_t)dn_bytes);
+      bulk_g2s_stream(wbuf(j % NBUF), src, (uint32_t)dn_bytes, &wbars[j % NBUF]);
+    }
+  };
+  // The shared experts' items come first and cover every token tile, so they
+  // are known before routing.
+  int w_issued = 0;
+  for (int i = warp; i < a.S * NT && w_issued < NBUF; i += nw, ++w_issued) issue_weights(w_issued, a.E + i / NT);
+
+  // k_gateup lets this kernel launch only after its own wait, so the router has
+  // finished: route now and fetch the routed down tiles while k_gateup runs.
+  route_select(a, R, true, blockIdx.x == 0, -1, ws_logits(a));
+  FLINT_TRACE(a, 17);
+  const int n_slots = route_slots(a, R);
+  {  // item list; items and staged rows counted in one packed prefix sum
+    const int spt = (n_slots + blockDim.x - 1) / blockDim.x;
+    const int s0 = threadIdx.x * spt;
+    int local = 0;
+    for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
+      const uint32_t tm = slot_info(a, R, s).tmask;
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t bits = (tm >> (8 * nt)) & 0xFFu;
+        if (bits) local += (1 << 16) | __popc(bits);
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w2 = 0; w2 < warp; ++w2) run += s_wsum[w2];
+    for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
+      const SlotInfo si = slot_info(a, R, s);
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t bits = (si.tmask >> (8 * nt)) & 0xFFu;
+        if (bits) {
+          const int it = run >> 16;
+          s_items[3 * it] = (s << 16) | (nt << 8) | (int)bits;
+          s_items[3 * it + 1] = si.expert;
+          s_items[3 * it + 2] = run & 0xFFFF;
+          run += (1 << 16) | __popc(bits);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  int tot = 0;
+  for (int w2 = 0; w2 < nw; ++w2) tot += s_wsum[w2];
+  const int n_items = tot >> 16, n_rows = tot & 0xFFFF;
+  auto rowbase = [&](int i) { return i < n_items ? s_items[3 * i + 2] : n_rows; };
+  for (int j = w_issued; j < NBUF && warp + nw * j < n_items; ++j) issue_weights(j, s_items[3 * (warp + nw * j) + 1]);
+
+  const int KG = a.I / KG_COLS;
+  // Round r stages the h rows of items i0 .. i1 - 1, as many as fit.
+  auto round_end = [&](int i0) {
+    const int rb0 = rowbase(i0);
+    int lo = i0 + 1, hi = n_items;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (rowbase(mid) - rb0 <= P.hcap) lo = mid;
+      else hi = mid - 1;
+    }
+    return lo;
+  };
+  int i1 = n_items > 0 ? round_end(0) : 0;
+
+  pdl_wait();  // h comes from k_gateup
+  pdl_trigger();
+  FLINT_TRACE(a, 18);
+
+  uint16_t* h = ws_h(a);
+  const unsigned* hmax = ws_hmax(a);
+  int j = 0;           // this warp's next item is warp + nw * j
+  bool dead = false;   // a weight copy of this warp timed out
+  uint32_t hphase = 0;
+  for (int i0 = 0; i0 < n_items; i0 = i1, i1 = i0 < n_items ? round_end(i0) : i0) {
+    const int rb0 = rowbase(i0);
+    // This warp's items of the round are warp + nw * jj, j <= jj < jend; it
+    // stages their rows (disjoint slices of the shared area) on its own
+    // barrier and converts them itself: no block barrier inside a round.
+    const int jend = i1 > warp ? (i1 - warp + nw - 1) / nw : 0;
+    if (j < jend && !dead) {
+      int myrows = 0;
+      for (int jj = j + lane; jj < jend; jj += 32) myrows += __popc((uint32_t)s_items[3 * (warp + nw * jj)] & 0xFFu);
+      myrows = __reduce_add_sync(0xffffffffu, myrows);
+      if (lane == 0) mbar_arrive_expect_tx(hbar, (uint32_t)(myrows * a.I * 2));
+      __syncwarp();
+      for (int jj = j + lane; jj < jend; jj += 32) {
+        const int it = warp + nw * jj;
+        const int code = s_items[3 * it], s = code >> 16, nt = (code >> 8) & 0xFF;
+        const uint32_t bits = (uint32_t)code & 0xFFu;
+        int r = rowbase(it) - rb0;
+        for (int n = 0; n < 8; ++n) {
+          if (!((bits >> n) & 1u)) continue;
+          const int src = s * a.B + 8 * nt + n;
+          bulk_g2s(hsm + (size_t)r * P.hstride, h + (size_t)src * a.I, (uint32_t)(a.I * 2), hbar);
+          s_hsc[r] = __uint_as_float(__ldcg(hmax + src));
+          ++r;
+        }
+      }
+      const bool okh = mbar_wait(hbar, hphase, status);
+      hphase ^= 1;
+      __syncwarp();
+      if (!okh) {
+        mbar_drain(hbar, hphase ^ 1);
+        dead = true;
+      } else {
+        if (i0 == 0 && warp == 0) FLINT_TRACE(a, 19);
+        for (int jj = j; jj < jend; ++jj) {  // prescaled f16 (NVFP4) or kept (BF16)
+          const int it = warp + nw * jj;
+          const int r0 = rowbase(it) - rb0, nrow = __popc((uint32_t)s_items[3 * it] & 0xFFu);
+          for (int r = r0; r < r0 + nrow; ++r) {
+            int kh = 0;
+            if (FMT == FLINT_MOE_NVFP4) {
+              kh = prescale_exp(s_hsc[r]);
+              const float sc = exp2i(kh);
+              uint32_t* rowp = reinterpret_cast<uint32_t*>(hsm + (size_t)r * P.hstride);
+              for (int q = lane; q < a.I / 2; q += 32) {
+                const uint32_t wv = rowp[q];
+                const __half2 hv = __floats2half2_rn(bf16lo(wv) * sc, bf16hi(wv) * sc);
+                rowp[q] = *reinterpret_cast<const uint32_t*>(&hv);
+              }
+            }
+            if (lane == 0) s_hinv[r] = exp2i(-kh);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    for (; !dead && warp + nw * j < i1; ++j) {
+      const int it = warp + nw * j;
+      const int code = s_items[3 * it], s = code >> 16, nt = (code >> 8) & 0xFF;
+      const uint32_t bits = (uint32_t)code & 0xFFu;
+      const int expert = s_items[3 * it + 1], rb = rowbase(it) - rb0;
+      const int b = j % NBUF;
+      if (!mbar_wait(&wbars[b], (uint32_t)((j / NBUF) & 1), status)) {
+        for (int jj = j; jj < j + NBUF && warp + nw * jj < n_items; ++jj)
+          mbar_drain(&wbars[jj % NBUF], (uint32_t)((jj / NBUF) & 1));
+        dead = true;
+        break;
+      }
+      if (j == 0 && warp == 0) FLINT_TRACE(a, 15);
+      const uint8_t* wb = wbuf(b);
+      // Column g is token 8 nt + g: its staged row if it selected the expert,
+      // else any staged row of the item (a column that is never combined).
+      const bool gsel = (bits >> g) & 1u;
+      const int grow = rb + (gsel ? __popc(bits & ((1u << g) - 1u)) : 0);
+      float acc[2][1][4];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[c][0][i] = 0.f;
+#pragma unroll 4
+      for (int kg = 0; kg < KG; ++kg) {
+        const uint8_t* rp = hsm + (size_t)grow * P.hstride + kg * 128 + t4 * 32;
+        uint4 bx[1][2];
+        bx[0][0] = lds128(rp);
+        bx[0][1] = lds128(rp + 16);
+        if (kg & 1)
+          tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[1]);
+        else
+          tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
+      }
+      const float Gd = a.globals[expert * 4 + 2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int n = 2 * t4 + hh;
+        if ((bits >> n) & 1u) {
+          const int tok = 8 * nt + n;
+          float wt = 1.0f;  // the shared experts are unweighted
+          if (s >= a.S)
+            for (int r = 0; r < a.k; ++r)
+              if (R.idx[tok * a.k + r] == expert) wt = R.w[tok * a.k + r];
+          const float inv = s_hinv[rb + __popc(bits & ((1u << n) - 1u))];
+          float* dst = acc_s + (warp * a.B + tok) * 16;
+          dst[g] += wt * (((acc[0][0][hh] + acc[1][0][hh]) * inv) * Gd);
+          dst[g + 8] += wt * (((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * inv) * Gd);
+        }
+      }
+      __syncwarp();
+      if (warp + nw * (j + NBUF) < n_items) issue_weights(j + NBUF, s_items[3 * (warp + nw * (j + NBUF)) + 1]);
+    }
+    if (i1 < n_items) {     // another round reuses the staging area
+      fence_proxy_async();  // reads of it come before the next round's copies into it
+      if (!__syncthreads_and(!dead)) {
+        dead = true;
+        break;
+      }
+    }
+  }
+  dead = __syncthreads_or(dead);
+  if (dead)  // let this warp's weight copies in flight land before the block exits
+    for (int jj = j; jj < j + NBUF && warp + nw * jj < n_items; ++jj)
+      mbar_drain(&wbars[jj % NBUF], (uint32_t)((jj / NBUF) & 1));
+  __syncthreads();
+  if (dead) return;
+  for (int p = threadIdx.x; p < a.B * 16; p += blockDim.x) {
+    const int t = p >> 4, r = p & 15;
+    float v = 0.f;
+    for (int w2 = 0; w2 < nw; ++w2) v += acc_s[(w2 * a.B + t) * 16 + r];
+    __nv_bfloat16 o = __float2bfloat16_rn(v);
+    const size_t at = (size_t)t * a.H + tile * 16 + r;
+    if (a.prenorm) {  // residual stream: r + bf16(layer output), rounded to bf16
+      const uint32_t rb = (uint32_t)__ldcg(a.x + at) << 16;
+      o = __float2bfloat16_rn(__uint_as_float(rb) + __bfloat162float(o));
+    }
+    a.out[at] = *reinterpret_cast<const uint16_t*>(&o);
+  }
+  FLINT_TRACE(a, 20);
+}
+
 }  // namespace flint
 
 using namespace flint;
@@ -1162,16 +1459,31 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-constexpr int DOWN_NBUF = 2;
 constexpr size_t SMEM_LIMIT = 227 * 1024;
 
-// 8 warps keep more down tiles in flight for small batches; larger batches and
-// BF16 tiles (16 KB each) need the shared memory for fewer, deeper buffers.
-// Router rows of one block (4 experts), the norm weight and one x chunk of up
-// to 8 tokens.
-size_t router_smem(int H, int B) { return (size_t)(5 + (B < 8 ? B : 8)) * H * 2; }
+// Experts per router block: the four warps of a block split its tokens.
+int router_epb(int B) { return B <= 1 ? 4 : (B == 2 ? 2 : 1); }
 
-int down_warps(int B, int fmt) { return (B <= 4 && fmt == FLINT_MOE_NVFP4) ? 8 : 4; }
+// Router rows of one block, the norm weight and one x chunk of up to 8 tokens.
+size_t router_smem(int H, int B) { return (size_t)(router_epb(B) + 1 + (B < 8 ? B : 8)) * H * 2; }
+
+// Down kernel shape: 8 warps with 3 or 2 tiles in flight each if they fit,
+// else 4 warps; the rest of the budget stages h rows (all B (k + S) of them if
+// possible). Small batches keep the block small enough to run beside a
+// gate/up block, which lets it prefetch while k_gateup works.
+bool down_shape(int I, int B, int k, int S, int max_slots, int fmt, size_t budget, DownPlan& out) {
+  const int need = B * (k + S);
+  const int cand[][2] = {{8, 3}, {8, 2}, {4, 2}, {4, 1}};
+  for (const auto& c : cand) {
+    const size_t base = down_plan(I, B, max_slots, fmt, c[0], c[1], 0).total;
+    const size_t per_row = (size_t)(I * 2 + 16) + 8;
+    if (base + 8 * per_row > budget) continue;
+    const int fit = (int)((budget - base) / per_row);
+    out = down_plan(I, B, max_slots, fmt, c[0], c[1], fit < need ? fit : need);
+    if (out.total <= budget) return true;
+  }
+  return false;
+}
 
 int sm_count() {
   int dev = 0, n = 0;
@@ -1252,14 +1564,17 @@ cudaError_t launch_gateup(const DecodeArgs& a, cudaStream_t stream, int ng) {
 }
 
 template <int FMT>
-cudaError_t launch_down(const DecodeArgs& a, cudaStream_t stream) {
-  const int nw = down_warps(a.B, FMT);
-  const DownSmemPlan P = down_plan(a.H, a.I, a.B, a.W.max_slots, FMT, DOWN_NBUF, nw);
-  return launch_pdl(k_down<FMT, DOWN_NBUF>, dim3(a.H / 16), dim3(32 * nw), P.total, stream, a);
+cudaError_t launch_down(const DecodeArgs& a, cudaStream_t stream, const DownPlan& P) {
+  return launch_pdl(k_down<FMT>, dim3(a.H / 16), dim3(32 * P.nw), P.total, stream, a);
+}
+
+constexpr int DOWN_ITEMS_NW = 8, DOWN_ITEMS_NBUF = 2;
+size_t down_items_smem(const DecodeArgs& a) {
+  return down_items_plan(a.H, a.I, a.B, a.W.max_slots, a.fmt, DOWN_ITEMS_NBUF, DOWN_ITEMS_NW).total;
 }
 
 cudaError_t launch_router(const DecodeArgs& a, cudaStream_t stream) {
-  const dim3 grid((a.E + 3) / 4);
+  const dim3 grid((a.E + a.router_epb - 1) / a.router_epb);
   const size_t smem = router_smem(a.H, a.B);
   switch (a.H / 256) {
     case 1: return launch_pdl(k_router<1>, grid, dim3(128), smem, stream, a);
@@ -1366,6 +1681,7 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   // their largest batch, which is at least as large.
   a.W = make_ws_layout(a.H, a.E, a.k, a.I, a.S, B);
   a.prenorm = prenorm ? 1 : 0;
+  a.router_epb = router_epb(B);
   a.gamma = prenorm ? layer->norm_weight : nullptr;
   a.eps = prenorm ? layer->norm_eps : 0.f;
   if (prenorm && !aligned16(a.gamma)) return FLINT_MOE_EALIGN;
@@ -1381,16 +1697,25 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
     const int units = a.W.max_slots * (a.I / 8), sms = sm_count();
     gateup_shape(a.H, B, a.fmt, (units + sms - 1) / sms, gu_ng, a.gu_nb);
   }
-  if (gu_ng == 0 ||
-      down_plan(a.H, a.I, B, a.W.max_slots, a.fmt, DOWN_NBUF, down_warps(B, a.fmt)).total + route_smem >
-          SMEM_LIMIT ||
+  DownPlan dp;
+  const size_t down_budget = (B <= 2 ? 110 * 1024 : SMEM_LIMIT) - route_smem;
+  if (gu_ng == 0 || !down_shape(a.I, B, a.k, a.S, a.W.max_slots, a.fmt, down_budget, dp) ||
       router_smem(a.H, B) > SMEM_LIMIT)
     return FLINT_MOE_EUNSUPPORTED;
+  a.dn_nbuf = dp.nbuf;
+  a.dn_hcap = dp.hcap;
+  const bool small_down = B <= 4 && a.fmt == FLINT_MOE_NVFP4 && down_items_smem(a) <= down_budget;
   cudaError_t e = launch_router(a, stream);
   if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_gateup<FLINT_MOE_NVFP4>(a, stream, gu_ng)
                                                        : launch_gateup<FLINT_MOE_BF16>(a, stream, gu_ng);
-  if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_down<FLINT_MOE_NVFP4>(a, stream)
-                                                       : launch_down<FLINT_MOE_BF16>(a, stream);
+  if (e == cudaSuccess) {
+    if (small_down)
+      e = launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF>, dim3(a.H / 16), dim3(32 * DOWN_ITEMS_NW),
+                     down_items_smem(a), stream, a);
+    else
+      e = a.fmt == FLINT_MOE_NVFP4 ? launch_down<FLINT_MOE_NVFP4>(a, stream, dp)
+                                   : launch_down<FLINT_MOE_BF16>(a, stream, dp);
+  }
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
 }
 }  // namespace
