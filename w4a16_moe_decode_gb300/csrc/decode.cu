@@ -655,7 +655,7 @@ __device__ __forceinline__ void tile_kgroup(const uint8_t* kp, const uint4 (&bx)
 // previous layer's output, which had completed before the router (which lets
 // this kernel launch only after its own wait) started.
 // ===========================================================================
-constexpr int GU_MAX_GROUPS = 3;
+constexpr int GU_MAX_GROUPS = 4;
 
 struct GateupPlan {
   size_t wbuf_off, xs_off, red_off, inv_off, bar_off, total;
@@ -668,7 +668,7 @@ __host__ __device__ inline GateupPlan gateup_plan(int H, int B, int fmt, int ntm
   size_t o = 0;
   p.wbuf_off = o;   o += (size_t)ng * nb * 4 * kslice;
   p.xs_off = o;     o += (size_t)B * (H * 2 + 16);
-  p.red_off = o;    o += sizeof(float) * ng * 2 * 3 * ntmax * 128;
+  p.red_off = o;    o += sizeof(float) * ng * 2 * 4 * ntmax * 128;
   p.inv_off = o;    o += sizeof(float) * MAX_BATCH;
   o = (o + 15) & ~(size_t)15;
   p.bar_off = o;    o += sizeof(uint64_t) * ng * nb * 4;
@@ -691,7 +691,7 @@ __device__ __forceinline__ bool group_sync_and(int gi, bool v) {
 }
 
 template <int FMT, int NTMAX>
-__global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 leaves room for k_down
+__global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 groups leave room for k_down
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
@@ -704,9 +704,9 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
   const int xstride = a.H * 2 + 16;
   const GateupPlan P = gateup_plan(a.H, a.B, FMT, NTMAX, NG, NB);
   uint8_t* xs = smem + P.xs_off;
-  // Cross-warp partial sums of a group, double-buffered by unit parity: warp 0
-  // of the group reads one buffer while warps 1..3 fill the other.
-  float* red = reinterpret_cast<float*>(smem + P.red_off) + gi * 2 * 3 * NTMAX * 128;
+  // Partial sums of the group's four warps, double-buffered by unit parity:
+  // the finalising warps read one buffer while the next unit fills the other.
+  float* red = reinterpret_cast<float*>(smem + P.red_off) + gi * 2 * 4 * NTMAX * 128;
   float* s_inv = reinterpret_cast<float*>(smem + P.inv_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);  // [NG][NB][4] weight slices
   auto wbar = [&](int b) { return &bars[(gi * NB + b) * 4 + gw]; };
@@ -866,13 +866,15 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
     } else {
       mbar_drain(wbar(b), par);
     }
-    float* rb = red + (jj & 1) * 3 * NTMAX * 128;
-    if (gw > 0) {
+    // Every warp's partial sums go to the group's reduction buffer
+    // (double-buffered by unit parity); after the barrier the 2 * nt_used
+    // (token tile, column parity) pairs are finalised by warps p % 4, each
+    // adding the four partials in warp order.
+    float* rb = red + (jj & 1) * 4 * NTMAX * 128;
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt)
+    for (int nt = 0; nt < NTMAX; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) rb[((gw - 1) * NTMAX + nt) * 128 + lane * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
-    }
+      for (int i = 0; i < 4; ++i) rb[(gw * NTMAX + nt) * 128 + lane * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
     if (!group_sync_and(gi, ok)) {  // a copy timed out: let the next buffer's copies land, then stop
       if (unit_of(jj + 1) < n_units && NB > 1) mbar_drain(wbar((jj + 1) % NB), (uint32_t)(((jj + 1) / NB) & 1));
       break;
@@ -883,46 +885,37 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 384 threads x 96 le
       const int u2 = unit_of(jj + NB);
       if (u2 < n_units) issue_w(b, slot_info(a, R, u2 / TILES).expert, u2 % TILES);
     }
-    if (gw != 0) continue;
-    float sum[NTMAX][4];
-#pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float v = acc[0][nt][i] + acc[1][nt][i];
-#pragma unroll
-        for (int w2 = 0; w2 < 3; ++w2) v += rb[(w2 * NTMAX + nt) * 128 + lane * 4 + i];
-        sum[nt][i] = v;
-      }
     const float Gg = glob[expert * 4 + 0];
     const float Gu = glob[expert * 4 + 1];
     const int hoff = frag_offset_elems(tile * 8 + g);
     uint16_t* h = ws_h(a);
     unsigned* hmax = ws_hmax(a);
+    for (int pr = gw; pr < 2 * nt_used; pr += 4) {
+      const int nt = pr >> 1, hh = pr & 1;
+      float gs = 0.f, us = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NTMAX; ++nt) {
-      if (nt >= nt_used) break;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int n = nt * 8 + 2 * t4 + hh;  // token
-        const size_t row = (size_t)slot * a.B + n;
-        const bool sel = n < a.B && ((si.tmask >> n) & 1u);
-        float hv = 0.f;
-        if (sel) {
-          const float inv = s_inv[n];
-          const float gv = (sum[nt][hh] * inv) * Gg;
-          const float uv = (sum[nt][2 + hh] * inv) * Gu;
-          const float ey = 1.0f + expf(-gv);
-          const float sv = ey < RCP_NR_MAX ? gv * rcp_nr(ey) : gv / ey;  // SiLU
-          const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
-          h[row * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hb);
-          hv = fabsf(__bfloat162float(hb));
-        }
-        hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 4));
-        hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 8));
-        hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 16));
-        if (g == 0 && sel && hv > 0.f) atomicMax(hmax + row, __float_as_uint(hv));
+      for (int w2 = 0; w2 < 4; ++w2) {
+        gs += rb[(w2 * NTMAX + nt) * 128 + lane * 4 + hh];
+        us += rb[(w2 * NTMAX + nt) * 128 + lane * 4 + 2 + hh];
       }
+      const int n = nt * 8 + 2 * t4 + hh;  // token
+      const size_t row = (size_t)slot * a.B + n;
+      const bool sel = n < a.B && ((si.tmask >> n) & 1u);
+      float hv = 0.f;
+      if (sel) {
+        const float inv = s_inv[n];
+        const float gv = (gs * inv) * Gg;
+        const float uv = (us * inv) * Gu;
+        const float ey = 1.0f + expf(-gv);
+        const float sv = ey < RCP_NR_MAX ? gv * rcp_nr(ey) : gv / ey;  // SiLU
+        const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
+        h[row * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hb);
+        hv = fabsf(__bfloat162float(hb));
+      }
+      hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 4));
+      hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 8));
+      hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 16));
+      if (g == 0 && sel && hv > 0.f) atomicMax(hmax + row, __float_as_uint(hv));
     }
   }
   FLINT_TRACE(a, 13);
@@ -1528,16 +1521,21 @@ void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) 
   const size_t route = sizeof(RouteSmem) + 1024;
   const int ntmax = (B + 7) / 8;
   const size_t budget = B <= 2 ? 110 * 1024 : SMEM_LIMIT;
-  const int want_nb = units_per_block <= GU_MAX_GROUPS ? 1 : 2;
-  const int cand[][2] = {{3, want_nb}, {3, 1}, {2, 2}, {2, 1}, {1, 3}, {1, 2}, {1, 1}};
-  for (const auto& c : cand) {
+  const int want_nb = units_per_block <= 3 ? 1 : 2;
+  // Up to 2 tokens a gate/up block stays small (3 groups) so that a down block
+  // runs beside it; larger batches take a fourth group of warps.
+  const int first = B <= 2 ? 2 : 0;
+  const int cand[][2] = {{4, want_nb}, {4, 1}, {3, want_nb}, {3, 1}, {2, 2}, {2, 1}, {1, 3}, {1, 2}, {1, 1}};
+  for (int i = first; i < (int)(sizeof(cand) / sizeof(cand[0])); ++i) {
+    const auto& c = cand[i];
     if (gateup_plan(H, B, fmt, ntmax, c[0], c[1]).total + route <= budget) {
       ng = c[0];
       nb = c[1];
       return;
     }
   }
-  for (const auto& c : cand) {
+  for (int i = first; i < (int)(sizeof(cand) / sizeof(cand[0])); ++i) {
+    const auto& c = cand[i];
     if (gateup_plan(H, B, fmt, ntmax, c[0], c[1]).total + route <= SMEM_LIMIT) {
       ng = c[0];
       nb = c[1];
