@@ -1193,7 +1193,7 @@ __host__ __device__ inline DownPlan down_plan(int I, int B, int max_slots, int f
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(256) k_down(DecodeArgs a) {
+__global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   __shared__ int s_wsum[MAX_WARPS];
@@ -1466,8 +1466,11 @@ size_t router_smem(int H, int B) { return (size_t)(router_epb(B) + 1 + (B < 8 ? 
 // gate/up block, which lets it prefetch while k_gateup works.
 bool down_shape(int I, int B, int k, int S, int max_slots, int fmt, size_t budget, DownPlan& out) {
   const int need = B * (k + S);
-  const int cand[][2] = {{8, 3}, {8, 2}, {4, 2}, {4, 1}};
-  for (const auto& c : cand) {
+  // Up to 2 tokens the block must fit beside a gate/up block (8 warps at
+  // most); from 3 tokens on it runs alone on its SM and takes 16 warps.
+  const int cand[][2] = {{16, 2}, {8, 3}, {8, 2}, {4, 2}, {4, 1}};
+  for (int i = B <= 2 ? 1 : 0; i < 5; ++i) {
+    const auto& c = cand[i];
     const size_t base = down_plan(I, B, max_slots, fmt, c[0], c[1], 0).total;
     const size_t per_row = (size_t)(I * 2 + 16) + 8;
     if (base + 8 * per_row > budget) continue;
