@@ -921,6 +921,29 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 gro
   FLINT_TRACE(a, 13);
 }
 
+// One row of I bf16 values (row stride >= 2 I) to f16 times 2^kh, in place:
+// each lane converts 16-byte words lane, lane + 32, ..., two at a time so
+// that their shared-memory latencies overlap.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc) {
+  const __half2 hv = __floats2half2_rn(bf16lo(w) * sc, bf16hi(w) * sc);
+  return *reinterpret_cast<const uint32_t*>(&hv);
+}
+__device__ __forceinline__ void row_to_f16(uint8_t* row, int I, int kh, int lane) {
+  const float sc = exp2i(kh);
+  for (int q = lane; q < I / 8; q += 64) {
+    const bool two = q + 32 < I / 8;
+    uint4 u0 = lds128(row + q * 16), u1 = two ? lds128(row + (q + 32) * 16) : make_uint4(0, 0, 0, 0);
+    u0 = make_uint4(bf16x2_to_f16x2_scaled(u0.x, sc), bf16x2_to_f16x2_scaled(u0.y, sc),
+                    bf16x2_to_f16x2_scaled(u0.z, sc), bf16x2_to_f16x2_scaled(u0.w, sc));
+    *reinterpret_cast<uint4*>(row + q * 16) = u0;
+    if (two) {
+      u1 = make_uint4(bf16x2_to_f16x2_scaled(u1.x, sc), bf16x2_to_f16x2_scaled(u1.y, sc),
+                      bf16x2_to_f16x2_scaled(u1.z, sc), bf16x2_to_f16x2_scaled(u1.w, sc));
+      *reinterpret_cast<uint4*>(row + (q + 32) * 16) = u1;
+    }
+  }
+}
+
 // ===========================================================================
 // K3 for small batches (at most 4 tokens, NVFP4): each warp keeps nbuf items
 // in flight, each buffer holding the item's down tile and its h rows, so a
@@ -1084,13 +1107,7 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
       for (int n = 0; n < Tc; ++n) {
         if (!((bits >> n) & 1u)) continue;
         const int kh = prescale_exp(s_hmax[r0 + n]);
-        const float sc = exp2i(kh);
-        uint32_t* rowp = reinterpret_cast<uint32_t*>(hb + n * P.hstride);
-        for (int q = lane; q < a.I / 2; q += 32) {
-          const uint32_t wv = rowp[q];
-          const __half2 hv = __floats2half2_rn(bf16lo(wv) * sc, bf16hi(wv) * sc);
-          rowp[q] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
+        row_to_f16(hb + n * P.hstride, a.I, kh, lane);
         if (lane == 0) s_inv[b * 8 + n] = exp2i(-kh);
       }
     } else if (lane < Tc) {
@@ -1321,14 +1338,19 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
         const int it = warp + nw * jj;
         const int code = s_items[3 * it], s = code >> 16, nt = (code >> 8) & 0xFF;
         const uint32_t bits = (uint32_t)code & 0xFFu;
-        int r = rowbase(it) - rb0;
-        for (int n = 0; n < 8; ++n) {
-          if (!((bits >> n) & 1u)) continue;
-          const int src = s * a.B + 8 * nt + n;
-          bulk_g2s(hsm + (size_t)r * P.hstride, h + (size_t)src * a.I, (uint32_t)(a.I * 2), hbar);
-          s_hsc[r] = __uint_as_float(__ldcg(hmax + src));
-          ++r;
+        const int r0 = rowbase(it) - rb0, src0 = s * a.B + 8 * nt;
+        unsigned hv[8];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {  // copies first, then all the maxima in flight together
+          const int r = r0 + __popc(bits & ((1u << n) - 1u));
+          if ((bits >> n) & 1u) {
+            bulk_g2s(hsm + (size_t)r * P.hstride, h + (size_t)(src0 + n) * a.I, (uint32_t)(a.I * 2), hbar);
+            hv[n] = __ldcg(hmax + src0 + n);
+          }
         }
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+          if ((bits >> n) & 1u) s_hsc[r0 + __popc(bits & ((1u << n) - 1u))] = __uint_as_float(hv[n]);
       }
       const bool okh = mbar_wait(hbar, hphase, status);
       hphase ^= 1;
@@ -1345,18 +1367,13 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
             int kh = 0;
             if (FMT == FLINT_MOE_NVFP4) {
               kh = prescale_exp(s_hsc[r]);
-              const float sc = exp2i(kh);
-              uint32_t* rowp = reinterpret_cast<uint32_t*>(hsm + (size_t)r * P.hstride);
-              for (int q = lane; q < a.I / 2; q += 32) {
-                const uint32_t wv = rowp[q];
-                const __half2 hv = __floats2half2_rn(bf16lo(wv) * sc, bf16hi(wv) * sc);
-                rowp[q] = *reinterpret_cast<const uint32_t*>(&hv);
-              }
+              row_to_f16(hsm + (size_t)r * P.hstride, a.I, kh, lane);
             }
             if (lane == 0) s_hinv[r] = exp2i(-kh);
           }
         }
         __syncwarp();
+        if (i0 == 0 && warp == 0) FLINT_TRACE(a, 6);
       }
     }
     for (; !dead && warp + nw * j < i1; ++j) {
