@@ -690,56 +690,15 @@ __device__ __forceinline__ bool group_sync_and(int gi, bool v) {
   return r != 0;
 }
 
-template <int FMT, int NTMAX>
-__global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 groups leave room for k_down
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ RouteSmem R;
-  constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
-  const int NG = blockDim.x >> 7, NB = a.gu_nb;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-  const int gi = warp >> 2, gw = warp & 3;
-  const int TILES = a.I / 8;
-  const int KGW = a.H / (KG_COLS * 4);
-  const int kslice = KGW * KGB;
-  const int xstride = a.H * 2 + 16;
-  const GateupPlan P = gateup_plan(a.H, a.B, FMT, NTMAX, NG, NB);
-  uint8_t* xs = smem + P.xs_off;
-  // Partial sums of the group's four warps, double-buffered by unit parity:
-  // the finalising warps read one buffer while the next unit fills the other.
-  float* red = reinterpret_cast<float*>(smem + P.red_off) + gi * 2 * 4 * NTMAX * 128;
-  float* s_inv = reinterpret_cast<float*>(smem + P.inv_off);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);  // [NG][NB][4] weight slices
-  auto wbar = [&](int b) { return &bars[(gi * NB + b) * 4 + gw]; };
-  auto wbuf = [&](int b) { return smem + P.wbuf_off + ((size_t)(gi * NB + b) * 4 + gw) * kslice; };
-  int* status = ws_hdr(a) + HDR_STATUS;
-  const int G = gridDim.x;
-  auto unit_of = [&](int jj) { return (int)blockIdx.x + (gi + NG * jj) * G; };
-
-  FLINT_TRACE(a, 8);
-  if (threadIdx.x < NG * NB * 4) mbar_init(&bars[threadIdx.x], 1);
-  fence_mbar_init();
-  __syncthreads();
-  auto issue_w = [&](int b, int expert, int tile) {
-    if (lane == 0) {
-      const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + (int64_t)tile * a.L.gu_tile +
-                           (int64_t)gw * kslice;
-      mbar_arrive_expect_tx(wbar(b), (uint32_t)kslice);
-      bulk_g2s_stream(wbuf(b), src, (uint32_t)kslice, wbar(b));
-    }
-  };
-  // The shared experts' units come first and need no routing: fetch them now.
-  int pre = 0;
-  while (pre < NB && unit_of(pre) < a.S * TILES) {
-    const int u = unit_of(pre);
-    issue_w(pre, a.E + u / TILES, u % TILES);
-    ++pre;
-  }
-  route_clear(R, a.E);
-  // Activations: warp w prescales tokens w, w + nwarps, ... and stores them in
-  // fragment order. Read straight from global memory (L2): a row of up to 2048
-  // columns stays in registers between the max and the conversion; wider rows
-  // are read twice.
-  for (int t = warp; t < a.B; t += blockDim.x >> 5) {
+// Activations for the gate/up kernels: warp w takes tokens w, w + nwarps, ...,
+// applies the RMSNorm if asked, a per-token power-of-two prescale (NVFP4
+// layers) and stores the row in mma B-fragment order (f16, or bf16 as is).
+// Read straight from global memory (L2): a row of up to 2048 columns stays in
+// registers between the max and the conversion; wider rows are read twice.
+template <int FMT>
+__device__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xstride, float* s_inv, int warp, int nwarps,
+                        int lane) {
+  for (int t = warp; t < a.B; t += nwarps) {
     const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x + (size_t)t * a.H);
     const int nch = a.H / 256;  // 16-byte chunks per lane
     uint8_t* dst = xs + (size_t)t * xstride;
@@ -811,6 +770,54 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 gro
     }
     if (lane == 0) s_inv[t] = exp2i(-kx);
   }
+}
+
+template <int FMT, int NTMAX>
+__global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 groups leave room for k_down
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ RouteSmem R;
+  constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  const int NG = blockDim.x >> 7, NB = a.gu_nb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int gi = warp >> 2, gw = warp & 3;
+  const int TILES = a.I / 8;
+  const int KGW = a.H / (KG_COLS * 4);
+  const int kslice = KGW * KGB;
+  const int xstride = a.H * 2 + 16;
+  const GateupPlan P = gateup_plan(a.H, a.B, FMT, NTMAX, NG, NB);
+  uint8_t* xs = smem + P.xs_off;
+  // Partial sums of the group's four warps, double-buffered by unit parity:
+  // the finalising warps read one buffer while the next unit fills the other.
+  float* red = reinterpret_cast<float*>(smem + P.red_off) + gi * 2 * 4 * NTMAX * 128;
+  float* s_inv = reinterpret_cast<float*>(smem + P.inv_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off);  // [NG][NB][4] weight slices
+  auto wbar = [&](int b) { return &bars[(gi * NB + b) * 4 + gw]; };
+  auto wbuf = [&](int b) { return smem + P.wbuf_off + ((size_t)(gi * NB + b) * 4 + gw) * kslice; };
+  int* status = ws_hdr(a) + HDR_STATUS;
+  const int G = gridDim.x;
+  auto unit_of = [&](int jj) { return (int)blockIdx.x + (gi + NG * jj) * G; };
+
+  FLINT_TRACE(a, 8);
+  if (threadIdx.x < NG * NB * 4) mbar_init(&bars[threadIdx.x], 1);
+  fence_mbar_init();
+  __syncthreads();
+  auto issue_w = [&](int b, int expert, int tile) {
+    if (lane == 0) {
+      const uint8_t* src = a.packed + (int64_t)expert * a.L.expert_bytes + (int64_t)tile * a.L.gu_tile +
+                           (int64_t)gw * kslice;
+      mbar_arrive_expect_tx(wbar(b), (uint32_t)kslice);
+      bulk_g2s_stream(wbuf(b), src, (uint32_t)kslice, wbar(b));
+    }
+  };
+  // The shared experts' units come first and need no routing: fetch them now.
+  int pre = 0;
+  while (pre < NB && unit_of(pre) < a.S * TILES) {
+    const int u = unit_of(pre);
+    issue_w(pre, a.E + u / TILES, u % TILES);
+    ++pre;
+  }
+  route_clear(R, a.E);
+  stage_x<FMT>(a, xs, xstride, s_inv, warp, blockDim.x >> 5, lane);
   __syncthreads();  // route_clear before the selection's atomics
   pdl_wait();
   pdl_trigger();
