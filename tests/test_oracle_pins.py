@@ -432,3 +432,46 @@ def test_moe_block_with_zero_experts_is_the_identity():
     out, routing = moe.moe_block(r, router, get, cfg, g, 1e-6)
     assert np.array_equal(out, r)
     assert np.array_equal(routing.idx, moe.route(moe.rmsnorm(r, g, 1e-6), router, cfg).idx)
+
+
+# ------------------------------------------------------------------ dense GEMV
+
+def _dense_matrix(seed, N, K):
+    w = synth.matrix_f32(seed, 0, synth.DOWN, 0, N, K, 0.02)
+    return moe.NVFP4Matrix(*nvfp4.quantize(w))
+
+
+def test_gemv_matches_torch_matmul_of_the_dequantised_matrix():
+    from oracle import dense
+    W = _dense_matrix(11, 48, 256)
+    x = moe.bf16_bits_to_f64(synth.x_bf16(11, 0, 3, 256))
+    ref = torch.from_numpy(x) @ torch.from_numpy(nvfp4.dequantize(W.codes, W.scales, W.G)).T
+    assert np.array_equal(dense.gemv(x, W), moe.bf16_round(ref.numpy()))
+
+
+def test_gemv_one_hot_input_selects_a_column():
+    """x = e_j gives y = bf16(G * c[:, j]) exactly."""
+    from oracle import dense
+    W = _dense_matrix(12, 32, 128)
+    for j in (0, 17, 127):
+        x = np.zeros((1, 128))
+        x[0, j] = 1.0
+        assert np.array_equal(dense.gemv(x, W)[0], moe.bf16_round(np.float64(W.G) * W.c()[:, j]))
+
+
+def test_gemv_commutes_with_power_of_two_scaling():
+    from oracle import dense
+    W = _dense_matrix(13, 64, 256)
+    x = moe.bf16_bits_to_f64(synth.x_bf16(13, 0, 2, 256))
+    for k in (-5, 4):
+        assert np.array_equal(dense.gemv(x * 2.0 ** k, W), dense.gemv(x, W) * 2.0 ** k)
+
+
+def test_gemv_with_norm_weight_is_gemv_of_the_normalised_rows():
+    from oracle import dense
+    W = _dense_matrix(14, 32, 256)
+    x = moe.bf16_bits_to_f64(synth.x_bf16(14, 0, 2, 256)) * 4.0
+    g = moe.bf16_bits_to_f64(synth.norm_bf16(14, 0, 256))
+    assert np.array_equal(dense.gemv(x, W, g, 1e-6), dense.gemv(moe.rmsnorm(x, g, 1e-6), W))
+    # and normalisation makes the result independent of the row scale (eps = 0)
+    assert np.array_equal(dense.gemv(x, W, g, 0.0), dense.gemv(x * 0.125, W, g, 0.0))
