@@ -30,7 +30,7 @@ def _declared():
 
 def test_every_declared_symbol_is_exported(lib):
     names = _declared()
-    assert {"flint_moe_decode", "flint_moe_pack", "flint_synth_normal"} <= names
+    assert {"flint_moe_decode", "flint_moe_pack", "flint_synth_normal", "flint_gemv", "flint_gemv_pack"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
 
@@ -128,6 +128,23 @@ def test_prenorm_needs_a_norm_weight(lib):
     assert L.flint_moe_layer_set_norm(ctypes.byref(layer), 0x60000, ctypes.c_float(1e-6)) == fb.OK
     assert layer.norm_weight == 0x60000 and abs(layer.norm_eps - 1e-6) < 1e-12
     assert L.flint_moe_decode_prenorm(ctypes.byref(layer), 0x30000, 0, 0x30000, 0x50000, None) == fb.OK  # B = 0
+
+
+def test_gemv_host_validation(lib):
+    L = fb.lib()
+    assert fb.flint_gemv_packed_bytes(2048, 2048, fb.NVFP4) == 128 * 32 * 576 + 256
+    assert fb.flint_gemv_packed_bytes(2048, 2048, fb.BF16) == 128 * 32 * 2048 + 256
+    for N, K in ((2040, 2048), (2048, 200), (2048, 3072), (2048, 16384), (0, 256)):
+        assert fb.flint_gemv_packed_bytes(N, K, fb.NVFP4) == 0
+    args = lambda N, K, B, x=0x30000, y=0x40000, w=None, eps=0.0: (0x10000, N, K, fb.NVFP4, x, B, y, w,  # noqa: E731
+                                                                  ctypes.c_float(eps), None, None)
+    assert L.flint_gemv(*args(2048, 2048, 0)) == fb.OK                    # B = 0: nothing to do
+    assert L.flint_gemv(*args(2040, 2048, 1)) == fb.EUNSUPPORTED
+    assert L.flint_gemv(*args(2048, 2048, 33)) == fb.EINVAL
+    assert L.flint_gemv(*args(2048, 2048, 1, x=0x30008)) == fb.EALIGN
+    assert L.flint_gemv(*args(2048, 2048, 1, w=0x50004)) == fb.EALIGN
+    assert L.flint_gemv(*args(2048, 2048, 1, eps=float("nan"))) == fb.EINVAL
+    assert L.flint_gemv(*args(64, 8192, 32)) == fb.EUNSUPPORTED          # activations exceed shared memory
 
 
 def test_layer_init_and_pack_validate(lib):

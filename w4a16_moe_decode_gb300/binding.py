@@ -48,6 +48,10 @@ class flint_moe_src(ctypes.Structure):
                 ("gate_bf16", c_void_p), ("up_bf16", c_void_p), ("down_bf16", c_void_p)]
 
 
+class flint_gemv_src(ctypes.Structure):
+    _fields_ = [("codes", c_void_p), ("scales", c_void_p), ("global_", c_void_p), ("bf16", c_void_p)]
+
+
 class flint_moe_layer(ctypes.Structure):
     _fields_ = [("cfg", flint_moe_config), ("packed", c_void_p), ("router", c_void_p), ("sel_bias", c_void_p),
                 ("norm_weight", c_void_p), ("norm_eps", ctypes.c_float)]
@@ -84,6 +88,12 @@ def lib() -> ctypes.CDLL:
             "flint_moe_debug_rcp_check": (c_int32, [ctypes.c_uint32, ctypes.c_uint32, P(ctypes.c_uint64), c_void_p]),
             "flint_moe_quantize_nvfp4": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                                    c_void_p]),
+            "flint_gemv_packed_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
+            "flint_gemv_pack": (c_int32, [P(flint_gemv_src), c_int32, c_int32, c_int32, c_void_p, c_size_t, c_void_p,
+                                          c_void_p]),
+            "flint_gemv_unpack_debug": (c_int32, [c_void_p, c_int32, c_int32, c_int32, P(flint_gemv_src), c_void_p]),
+            "flint_gemv": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
+                                     ctypes.c_float, c_void_p, c_void_p]),
             "flint_synth_stream_key": (ctypes.c_uint64, [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
                                                          ctypes.c_uint32]),
             "flint_synth_normal": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint64, c_size_t, ctypes.c_float, c_int32,
@@ -241,6 +251,34 @@ def flint_moe_debug_rcp_check(lo_bits: int, hi_bits: int, stream=None) -> int:
 def flint_moe_quantize_nvfp4(w, n_mat, rows, cols, codes, scales, global_, stream=None) -> None:
     _check("flint_moe_quantize_nvfp4", lib().flint_moe_quantize_nvfp4(_ptr(w), n_mat, rows, cols, _ptr(codes),
                                                                       _ptr(scales), _ptr(global_), _stream(stream)))
+
+
+def _gemv_src(d: dict) -> flint_gemv_src:
+    return flint_gemv_src(_ptr(d.get("codes")), _ptr(d.get("scales")), _ptr(d.get("global")), _ptr(d.get("bf16")))
+
+
+def flint_gemv_packed_bytes(N: int, K: int, fmt: int = NVFP4) -> int:
+    return lib().flint_gemv_packed_bytes(N, K, fmt)
+
+
+def flint_gemv_pack(src: dict, N: int, K: int, fmt, dst, dev_status=None, stream=None) -> None:
+    """src: {codes, scales, global} (NVFP4) or {bf16} tensors of W [N][K]."""
+    s = _gemv_src(src)
+    _check("flint_gemv_pack", lib().flint_gemv_pack(ctypes.byref(s), N, K, fmt, _ptr(dst),
+                                                    dst.numel() * dst.element_size(), _ptr(dev_status),
+                                                    _stream(stream)))
+
+
+def flint_gemv_unpack_debug(packed, N: int, K: int, fmt, dst: dict, stream=None) -> None:
+    s = _gemv_src(dst)
+    _check("flint_gemv_unpack_debug", lib().flint_gemv_unpack_debug(_ptr(packed), N, K, fmt, ctypes.byref(s),
+                                                                    _stream(stream)))
+
+
+def flint_gemv(packed, N: int, K: int, fmt, x, B: int, y, norm_weight=None, eps: float = 0.0, dev_status=None,
+               stream=None) -> None:
+    _check("flint_gemv", lib().flint_gemv(_ptr(packed), N, K, fmt, _ptr(x), B, _ptr(y), _ptr(norm_weight),
+                                          float(eps), _ptr(dev_status), _stream(stream)))
 
 
 def flint_synth_stream_key(seed, layer, tensor, expert) -> int:

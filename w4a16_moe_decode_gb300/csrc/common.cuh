@@ -63,6 +63,21 @@ __host__ __device__ inline Layout make_layout(int H, int I, int E, int S, int fm
   return L;
 }
 
+// A dense matrix W [N][K] for the small-batch GEMV: laid out like one
+// expert's down matrix (N / 16 tiles of 16 rows x K / 64 k-groups), then its
+// tensor scale (float32 words [G, G, G, 0]).
+__host__ __device__ inline Layout make_dense_layout(int N, int K, int fmt) {
+  Layout L;
+  L.kg_bytes = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  L.gu_tile = 0;
+  L.gu_bytes = 0;
+  L.dn_tile = (int64_t)(K / KG_COLS) * L.kg_bytes;
+  L.expert_bytes = (int64_t)(N / 16) * L.dn_tile;
+  L.globals_off = L.expert_bytes;
+  L.total = L.globals_off + 256;
+  return L;
+}
+
 // ---------------------------------------------------------------------------
 // Workspace layout. Header words, then 256-byte aligned regions.
 // ---------------------------------------------------------------------------

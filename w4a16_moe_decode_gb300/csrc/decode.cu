@@ -30,6 +30,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "flint_gemv.h"
 
 namespace flint {
 
@@ -696,11 +697,11 @@ __device__ __forceinline__ bool group_sync_and(int gi, bool v) {
 // Read straight from global memory (L2): a row of up to 2048 columns stays in
 // registers between the max and the conversion; wider rows are read twice.
 template <int FMT>
-__device__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xstride, float* s_inv, int warp, int nwarps,
-                        int lane) {
-  for (int t = warp; t < a.B; t += nwarps) {
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x + (size_t)t * a.H);
-    const int nch = a.H / 256;  // 16-byte chunks per lane
+__device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const uint16_t* gamma, float eps,
+                           uint8_t* xs, int xstride, float* s_inv, int warp, int nwarps, int lane) {
+  for (int t = warp; t < B; t += nwarps) {
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(x + (size_t)t * K);
+    const int nch = K / 256;  // 16-byte chunks per lane
     uint8_t* dst = xs + (size_t)t * xstride;
     auto absmax = [&](const uint4& u, float m) {
       const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
@@ -721,7 +722,7 @@ __device__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xstride, float* s_
         *reinterpret_cast<uint32_t*>(dst + 2 * frag_offset_elems(col + 2 * q)) = bits;
       }
     };
-    const uint8_t* gw8 = reinterpret_cast<const uint8_t*>(a.gamma);
+    const uint8_t* gw8 = reinterpret_cast<const uint8_t*>(gamma);
     float mx = 0.f;
     int kx = 0;
     if (nch <= 8) {
@@ -729,12 +730,12 @@ __device__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xstride, float* s_
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         if (c < nch) v[c] = ld_cg_v4(src + (lane + 32 * c) * 16);
-      if (a.prenorm) {  // RMSNorm, as the router computes it
+      if (prenorm) {  // RMSNorm, as the router computes it
         float part = 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           if (c < nch) part = sumsq8(v[c], part);
-        const float inv = rms_inv(part, a.H, a.eps);
+        const float inv = rms_inv(part, K, eps);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           if (c < nch)
@@ -752,14 +753,14 @@ __device__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xstride, float* s_
         if (c < nch) store(v[c], c, sc);
     } else {
       float inv = 1.f;
-      if (a.prenorm) {
+      if (prenorm) {
         float part = 0.f;
         for (int c = 0; c < nch; ++c) part = sumsq8(ld_cg_v4(src + (lane + 32 * c) * 16), part);
-        inv = rms_inv(part, a.H, a.eps);
+        inv = rms_inv(part, K, eps);
       }
       auto chunk = [&](int c) {
         const uint4 u = ld_cg_v4(src + (lane + 32 * c) * 16);
-        return a.prenorm ? norm8(u, __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), inv) : u;
+        return prenorm ? norm8(u, __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), inv) : u;
       };
       if (FMT == FLINT_MOE_NVFP4) {
         for (int c = 0; c < nch; ++c) mx = absmax(chunk(c), mx);
@@ -770,6 +771,12 @@ __device__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xstride, float* s_
     }
     if (lane == 0) s_inv[t] = exp2i(-kx);
   }
+}
+
+template <int FMT>
+__device__ __forceinline__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xstride, float* s_inv, int warp,
+                                        int nwarps, int lane) {
+  stage_rows<FMT>(a.x, a.B, a.H, a.prenorm, a.gamma, a.eps, xs, xstride, s_inv, warp, nwarps, lane);
 }
 
 template <int FMT, int NTMAX>
@@ -1465,6 +1472,116 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
   FLINT_TRACE(a, 20);
 }
 
+// ===========================================================================
+// Small-batch dense GEMV: y [B][N] = x [B][K] W^T for a packed NVFP4 or BF16
+// matrix (16-row tiles of 64-column k-groups). One block per 16 output rows;
+// its nw warps split K into contiguous k-group ranges, each fetching its slice
+// of the tile with one bulk copy before the dependency wait (the weights do
+// not depend on the previous kernel), and the warps' partial sums are added
+// in warp order.
+// ===========================================================================
+struct GemvArgs {
+  int N, K, B, fmt, prenorm;
+  const uint16_t* x;
+  uint16_t* y;
+  const uint8_t* packed;
+  const float* G;  // the tensor scale word after the tiles
+  Layout L;
+  const uint16_t* gamma;
+  float eps;
+  int* status;
+};
+
+__host__ __device__ inline size_t gemv_smem(int K, int B, int fmt, int nw, int ntmax, size_t* xs_off,
+                                            size_t* inv_off, size_t* wbuf_off, size_t* red_off, size_t* bar_off) {
+  const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  size_t o = 0;
+  *wbuf_off = o;  o += (size_t)(K / KG_COLS) * kgb;
+  *xs_off = o;    o += (size_t)B * (K * 2 + 16);
+  *inv_off = o;   o += sizeof(float) * MAX_BATCH;
+  *red_off = o;   o += sizeof(float) * nw * ntmax * 128;
+  o = (o + 15) & ~(size_t)15;
+  *bar_off = o;   o += sizeof(uint64_t) * nw;
+  return o;
+}
+
+template <int FMT, int NTMAX>
+__global__ void __launch_bounds__(256) k_gemv(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int nw = blockDim.x >> 5;
+  const int KGW = (a.K / KG_COLS) / nw;  // k-groups per warp
+  size_t xs_off, inv_off, wbuf_off, red_off, bar_off;
+  gemv_smem(a.K, a.B, FMT, nw, NTMAX, &xs_off, &inv_off, &wbuf_off, &red_off, &bar_off);
+  uint8_t* wb = smem + wbuf_off + (size_t)warp * KGW * KGB;
+  uint8_t* xs = smem + xs_off;
+  float* s_inv = reinterpret_cast<float*>(smem + inv_off);
+  float* red = reinterpret_cast<float*>(smem + red_off);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + bar_off) + warp;
+  const int xstride = a.K * 2 + 16;
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = (uint32_t)KGW * KGB;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s_stream(wb, a.packed + (int64_t)blockIdx.x * a.L.dn_tile + (int64_t)warp * bytes, bytes, bar);
+  }
+  pdl_wait();  // x may be the previous kernel's output
+  pdl_trigger();
+  stage_rows<FMT>(a.x, a.B, a.K, a.prenorm, a.gamma, a.eps, xs, xstride, s_inv, warp, nw, lane);
+  __syncthreads();
+  const int nt_used = (a.B + 7) >> 3;
+  float acc[2][NTMAX][4];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int nt = 0; nt < NTMAX; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
+  const bool ok = mbar_wait(bar, 0, a.status);
+  if (ok) {
+    int tok[NTMAX];  // column g of token tile nt is token 8 nt + g (past B: a repeat of token B - 1)
+#pragma unroll
+    for (int nt = 0; nt < NTMAX; ++nt) tok[nt] = min(nt * 8 + g, a.B - 1);
+#pragma unroll 4
+    for (int kl = 0; kl < KGW; ++kl) {
+      const int kg = warp * KGW + kl;
+      uint4 bx[NTMAX][2];
+#pragma unroll
+      for (int nt = 0; nt < NTMAX; ++nt) {
+        if (nt < nt_used) {
+          const uint8_t* rp = xs + (size_t)tok[nt] * xstride + kg * 128 + t4 * 32;
+          bx[nt][0] = lds128(rp);
+          bx[nt][1] = lds128(rp + 16);
+        }
+      }
+      if (kl & 1)
+        tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[1]);
+      else
+        tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[0]);
+    }
+  } else {
+    mbar_drain(bar, 0);
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTMAX; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[((warp * NTMAX + nt) * 32 + lane) * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
+  if (!__syncthreads_and(ok)) return;
+  // Output (row r of the tile, token t): token tile t / 8, fragment lane
+  // 4 (r % 8) + (t % 8) / 2, element 2 (r / 8) + t % 2.
+  const float G = FMT == FLINT_MOE_NVFP4 ? a.G[0] : 1.0f;
+  for (int p = threadIdx.x; p < 16 * a.B; p += blockDim.x) {
+    const int r = p & 15, t = p >> 4, nt = t >> 3, c = t & 7;
+    const int ln = 4 * (r & 7) + (c >> 1), i = 2 * (r >> 3) + (c & 1);
+    float v = 0.f;
+    for (int w2 = 0; w2 < nw; ++w2) v += red[((w2 * NTMAX + nt) * 32 + ln) * 4 + i];
+    const __nv_bfloat16 o = __float2bfloat16_rn((v * s_inv[t]) * G);
+    a.y[(size_t)t * a.N + blockIdx.x * 16 + r] = *reinterpret_cast<const uint16_t*>(&o);
+  }
+}
+
 }  // namespace flint
 
 using namespace flint;
@@ -1513,8 +1630,16 @@ int sm_count() {
   return n;
 }
 
+template <typename K, typename Args>
+cudaError_t launch_any(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Args& a);
+
 template <typename K>
 cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const DecodeArgs& a) {
+  return launch_any(kernel, grid, block, smem, stream, a);
+}
+
+template <typename K, typename Args>
+cudaError_t launch_any(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Args& a) {
   if (smem > 48 * 1024 - sizeof(RouteSmem)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1815,6 +1940,53 @@ extern "C" flint_moe_status flint_moe_debug_rcp_check(uint32_t lo_bits, uint32_t
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   cudaFreeAsync(d, stream);
   *host_mismatches = h;
+  return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
+}
+
+extern "C" flint_moe_status flint_gemv(const void* packed, int32_t N, int32_t K, int32_t fmt, const uint16_t* x,
+                                       int32_t B, uint16_t* y, const uint16_t* norm_weight, float eps,
+                                       int32_t* dev_status, cudaStream_t stream) {
+  if (flint_gemv_packed_bytes(N, K, fmt) == 0) return FLINT_MOE_EUNSUPPORTED;
+  if (B < 0 || B > MAX_BATCH || !(eps >= 0.f) || !(eps <= 3.0e38f)) return FLINT_MOE_EINVAL;
+  if (B == 0) return FLINT_MOE_OK;
+  if (!packed || !x || !y) return FLINT_MOE_EINVAL;
+  if (!aligned16(packed) || !aligned16(x) || !aligned16(y) || (norm_weight && !aligned16(norm_weight)))
+    return FLINT_MOE_EALIGN;
+  GemvArgs a;
+  a.N = N;
+  a.K = K;
+  a.B = B;
+  a.fmt = fmt;
+  a.prenorm = norm_weight != nullptr;
+  a.x = x;
+  a.y = y;
+  a.packed = static_cast<const uint8_t*>(packed);
+  a.L = make_dense_layout(N, K, fmt);
+  a.G = reinterpret_cast<const float*>(a.packed + a.L.globals_off + 8);  // [G, G, G, 0]: the third word
+  a.gamma = norm_weight;
+  a.eps = eps;
+  a.status = dev_status;
+  const int kg = K / KG_COLS, nw = kg % 8 == 0 ? 8 : 4, ntmax = (B + 7) / 8;
+  size_t o1, o2, o3, o4, o5;
+  const size_t smem = gemv_smem(K, B, fmt, nw, ntmax, &o1, &o2, &o3, &o4, &o5);
+  if ((size_t)B * (K * 2 + 16) > 160 * 1024 || smem > SMEM_LIMIT) return FLINT_MOE_EUNSUPPORTED;
+  const dim3 grid(N / 16), block(32 * nw);
+  cudaError_t e;
+  if (fmt == FLINT_MOE_NVFP4) {
+    switch (ntmax) {
+      case 1: e = launch_any(k_gemv<FLINT_MOE_NVFP4, 1>, grid, block, smem, stream, a); break;
+      case 2: e = launch_any(k_gemv<FLINT_MOE_NVFP4, 2>, grid, block, smem, stream, a); break;
+      case 3: e = launch_any(k_gemv<FLINT_MOE_NVFP4, 3>, grid, block, smem, stream, a); break;
+      default: e = launch_any(k_gemv<FLINT_MOE_NVFP4, 4>, grid, block, smem, stream, a); break;
+    }
+  } else {
+    switch (ntmax) {
+      case 1: e = launch_any(k_gemv<FLINT_MOE_BF16, 1>, grid, block, smem, stream, a); break;
+      case 2: e = launch_any(k_gemv<FLINT_MOE_BF16, 2>, grid, block, smem, stream, a); break;
+      case 3: e = launch_any(k_gemv<FLINT_MOE_BF16, 3>, grid, block, smem, stream, a); break;
+      default: e = launch_any(k_gemv<FLINT_MOE_BF16, 4>, grid, block, smem, stream, a); break;
+    }
+  }
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
 }
 

@@ -9,6 +9,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "flint_gemv.h"
 
 namespace flint {
 
@@ -483,5 +484,83 @@ extern "C" flint_moe_status flint_moe_quantize_nvfp4(const float* w, int32_t n_m
   k_amax<<<ag, 256, 0, stream>>>(w, per_mat, n_mat, amax_bits);
   k_quant<<<grid_for(per_mat / 16 * n_mat, 256), 256, 0, stream>>>(w, per_mat, cols, n_mat, amax_bits, codes, scales);
   k_quant_globals<<<(n_mat + 127) / 128, 128, 0, stream>>>(amax_bits, global, n_mat);
+  return cudaGetLastError() == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Dense matrices for the small-batch GEMV: the MoE repack with a layout of one
+// down matrix (H = N rows, I = K columns) and no gate/up tiles.
+// ---------------------------------------------------------------------------
+static bool gemv_shape_ok(int32_t N, int32_t K, int32_t fmt) {
+  if (N < 16 || N % 16 || N > (1 << 20)) return false;
+  if (K < 256 || K > 8192 || K % 256 || (K > 2048 && K % 2048)) return false;
+  return fmt == FLINT_MOE_NVFP4 || fmt == FLINT_MOE_BF16;
+}
+
+extern "C" size_t flint_gemv_packed_bytes(int32_t N, int32_t K, int32_t fmt) {
+  return gemv_shape_ok(N, K, fmt) ? (size_t)make_dense_layout(N, K, fmt).total : 0;
+}
+
+extern "C" flint_moe_status flint_gemv_pack(const flint_gemv_src* src, int32_t N, int32_t K, int32_t fmt, void* dst,
+                                            size_t dst_bytes, int32_t* dev_status, cudaStream_t stream) {
+  if (!gemv_shape_ok(N, K, fmt)) return FLINT_MOE_EUNSUPPORTED;
+  if (!src || !dst) return FLINT_MOE_EINVAL;
+  const Layout L = make_dense_layout(N, K, fmt);
+  if (dst_bytes < (size_t)L.total) return FLINT_MOE_EINVAL;
+  if (!aligned16(dst)) return FLINT_MOE_EALIGN;
+  if (fmt == FLINT_MOE_NVFP4) {
+    if (!src->codes || !src->scales || !src->global_) return FLINT_MOE_EINVAL;
+    if (!aligned16(src->scales)) return FLINT_MOE_EALIGN;
+  } else {
+    if (!src->bf16) return FLINT_MOE_EINVAL;
+    if (!aligned16(src->bf16)) return FLINT_MOE_EALIGN;
+  }
+  PackArgs a = {};
+  a.L = L;
+  a.H = N;
+  a.I = K;
+  a.fmt = fmt;
+  a.n_words = L.globals_off / 4;
+  a.codes[2] = src->codes;
+  a.scales[2] = src->scales;
+  a.bf16[2] = reinterpret_cast<const uint8_t*>(src->bf16);
+  a.dst = static_cast<uint8_t*>(dst);
+  a.status = dev_status;
+  k_pack<<<grid_for(a.n_words, 256), 256, 0, stream>>>(a);
+  GlobalsArgs ga;
+  for (int m = 0; m < 3; ++m) ga.g[m] = src->global_;
+  ga.dst = reinterpret_cast<float*>(static_cast<uint8_t*>(dst) + L.globals_off);
+  ga.n = 1;
+  ga.fmt = fmt;
+  k_pack_globals<<<1, 32, 0, stream>>>(ga);
+  return cudaGetLastError() == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
+}
+
+extern "C" flint_moe_status flint_gemv_unpack_debug(const void* packed, int32_t N, int32_t K, int32_t fmt,
+                                                    const flint_gemv_src* dst, cudaStream_t stream) {
+  if (!gemv_shape_ok(N, K, fmt)) return FLINT_MOE_EUNSUPPORTED;
+  if (!packed || !dst) return FLINT_MOE_EINVAL;
+  const Layout L = make_dense_layout(N, K, fmt);
+  UnpackArgs a = {};
+  a.L = L;
+  a.H = N;
+  a.I = K;
+  a.fmt = fmt;
+  a.n_words = L.globals_off / 4;
+  a.src = static_cast<const uint8_t*>(packed);
+  if (fmt == FLINT_MOE_NVFP4) {
+    if (!dst->codes || !dst->scales || !dst->global_) return FLINT_MOE_EINVAL;
+    a.codes[2] = const_cast<uint8_t*>(dst->codes);
+    a.scales[2] = const_cast<uint8_t*>(dst->scales);
+  } else {
+    if (!dst->bf16) return FLINT_MOE_EINVAL;
+    a.bf16[2] = reinterpret_cast<uint8_t*>(const_cast<uint16_t*>(dst->bf16));
+  }
+  k_unpack<<<grid_for(a.n_words, 256), 256, 0, stream>>>(a);
+  if (fmt == FLINT_MOE_NVFP4) {
+    float* g = const_cast<float*>(dst->global_);
+    k_unpack_globals<<<1, 32, 0, stream>>>(reinterpret_cast<const float*>(a.src + L.globals_off), nullptr, nullptr,
+                                          g, 1);
+  }
   return cudaGetLastError() == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
 }

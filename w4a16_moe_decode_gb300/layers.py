@@ -102,6 +102,28 @@ def synth_layer(cfg, seed: int, layer: int = 0, device="cuda", bias: torch.Tenso
                        canonical=canon if keep_canonical else {}, norm=norm)
 
 
+def synth_dense(N: int, K: int, seed: int, layer: int = 0, fmt: int = fb.NVFP4, device="cuda"):
+    """A packed dense matrix W [N][K] (stream (seed, layer, DOWN, 0), N(0, 0.02)),
+    quantised (NVFP4) or rounded (BF16) on the GPU. Returns (packed, canonical)."""
+    if fmt == fb.NVFP4:
+        w = torch.empty(N, K, dtype=torch.float32, device=device)
+        _fill_normal(w, seed, layer, fb.DOWN, 0, WEIGHT_SIGMA, False)
+        canon = {"codes": torch.empty(N, K // 2, dtype=torch.uint8, device=device),
+                 "scales": torch.empty(N, K // 16, dtype=torch.uint8, device=device),
+                 "global": torch.empty(1, dtype=torch.float32, device=device)}
+        fb.flint_moe_quantize_nvfp4(w, 1, N, K, canon["codes"], canon["scales"], canon["global"])
+        del w
+    else:
+        canon = {"bf16": torch.empty(N, K, dtype=torch.int16, device=device)}
+        _fill_normal(canon["bf16"], seed, layer, fb.DOWN, 0, WEIGHT_SIGMA, True)
+    packed = torch.empty(fb.flint_gemv_packed_bytes(N, K, fmt), dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    fb.flint_gemv_pack(canon, N, K, fmt, packed, status)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"flint_gemv_pack reported device status {int(status.item())}")
+    return packed, canon
+
+
 def workspace(cfg, max_batch: int, device="cuda") -> torch.Tensor:
     ws = torch.empty(fb.flint_moe_workspace_bytes(cfg, max_batch), dtype=torch.uint8, device=device)
     fb.flint_moe_workspace_init(cfg, max_batch, ws)
