@@ -45,6 +45,7 @@ def parse_args():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--quick", action="store_true", help="skip the batch-8, isolated, e2e, stack and CPU legs")
     p.add_argument("--stack-only", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--dense-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--oracle-leg", type=int, default=0, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -431,9 +432,53 @@ def gpu_arm(args) -> None:
                           f"stack time / {P}",
                 "beta": beta, "per_batch": res}
 
+    def dense_leg(shapes=((2048, 2048), (8192, 2048), (2048, 8192)), batches=(1, 8), steps=2000):
+        """Small-batch dense GEMV y = x W^T on packed NVFP4 matrices, rotating
+        through distinct seeded matrices (more bytes than L2 per rotation),
+        launched back to back with programmatic dependent launch from a CUDA
+        graph; GB/s over the matrix bytes."""
+        res = {}
+        peak = measured_peak_gbs()[0]
+        for (N, K) in shapes:
+            nbytes = fb.flint_gemv_packed_bytes(N, K, fb.NVFP4)
+            nm = max(8, -(-384 * 1024 * 1024 // nbytes))  # at least 3x L2 per rotation
+            mats = [layers.synth_dense(N, K, 2000 + i, 0, fb.NVFP4, dev)[0] for i in range(nm)]
+            for Bd in batches:
+                x = layers.synth_x(Bd, K, 2000, 0, dev)
+                y = torch.empty(Bd, N, dtype=torch.int16, device=dev)
+                stream = torch.cuda.Stream(device=dev)
+                stream.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(stream):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for m in mats:
+                            fb.flint_gemv(m, N, K, fb.NVFP4, x, Bd, y, None, 0.0, None, stream)
+                    for _ in range(3):
+                        g.replay()
+                    reps = max(1, steps // nm)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    e1.record(stream)
+                    stream.synchronize()
+                us = e0.elapsed_time(e1) * 1000.0 / (reps * nm)
+                gbs = nbytes / (us * 1e-6) / 1e9
+                res[f"{N}x{K}_b{Bd}"] = {"us": us, "gbs": gbs, "frac": gbs / peak, "matrix_bytes": nbytes,
+                                         "matrices_in_rotation": nm}
+            del mats
+            torch.cuda.empty_cache()
+        return {"workload": "y[B][N] = x[B][K] W^T, W NVFP4 [N][K] packed, bf16 x and y, FP32 accumulation",
+                "per_shape": res}
+
     if args.stack_only:
         if rank == 0:
             print(json.dumps({"stack": stack_leg()}))
+        return
+    if args.dense_only:
+        if rank == 0:
+            print(json.dumps({"dense_gemv": dense_leg()}))
         return
 
     K, W, B = args.steps, max(args.warmup, 3), args.batch
@@ -466,6 +511,7 @@ def gpu_arm(args) -> None:
         torch.cuda.empty_cache()
     if not args.quick and B == 1 and world == 1:
         extra["stack"] = stack_leg()
+        extra["dense_gemv"] = dense_leg()
 
     if rank != 0:
         if world > 1:
