@@ -730,7 +730,11 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const u
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         if (c < nch) v[c] = ld_cg_v4(src + (lane + 32 * c) * 16);
-      if (prenorm) {  // RMSNorm, as the router computes it
+      if (prenorm) {  // RMSNorm, as the router computes it; weights loaded beside x
+        uint4 wv[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < nch) wv[c] = __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16));
         float part = 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -738,8 +742,7 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const u
         const float inv = rms_inv(part, K, eps);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          if (c < nch)
-            v[c] = norm8(v[c], __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), inv);
+          if (c < nch) v[c] = norm8(v[c], wv[c], inv);
       }
       if (FMT == FLINT_MOE_NVFP4) {
 #pragma unroll
@@ -994,6 +997,7 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   __shared__ int s_wsum[MAX_WARPS];
+  __shared__ uint16_t s_res[MAX_BATCH * 16];  // residual values (pre-norm block)
   constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int nw = blockDim.x >> 5;
@@ -1096,6 +1100,11 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
                &bars[b]);
   };
   const int KG = a.I / KG_COLS;
+  // The residual rows of this tile (the layer's input, final before the
+  // router ran) are read now, while the wait is pending.
+  if (a.prenorm)
+    for (int p = threadIdx.x; p < a.B * 16; p += blockDim.x)
+      s_res[p] = __ldcg(a.x + (size_t)(p >> 4) * a.H + tile * 16 + (p & 15));
   pdl_wait();  // h comes from k_gateup
   pdl_trigger();
   FLINT_TRACE(a, 18);
@@ -1176,12 +1185,11 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
     float v = 0.f;
     for (int w2 = 0; w2 < nw; ++w2) v += acc_s[(w2 * a.B + t) * 16 + r];
     __nv_bfloat16 o = __float2bfloat16_rn(v);
-    const size_t at = (size_t)t * a.H + tile * 16 + r;
     if (a.prenorm) {  // residual stream: r + bf16(layer output), rounded to bf16
-      const uint32_t rb = (uint32_t)__ldcg(a.x + at) << 16;
+      const uint32_t rb = (uint32_t)s_res[p] << 16;
       o = __float2bfloat16_rn(__uint_as_float(rb) + __bfloat162float(o));
     }
-    a.out[at] = *reinterpret_cast<const uint16_t*>(&o);
+    a.out[(size_t)t * a.H + tile * 16 + r] = *reinterpret_cast<const uint16_t*>(&o);
   }
   FLINT_TRACE(a, 20);
 }
@@ -1228,6 +1236,7 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   __shared__ int s_wsum[MAX_WARPS];
+  __shared__ uint16_t s_res[MAX_BATCH * 16];  // residual values (pre-norm block)
   constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   const int nw = blockDim.x >> 5;
@@ -1327,6 +1336,11 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
   };
   int i1 = n_items > 0 ? round_end(0) : 0;
 
+  // The residual rows of this tile (the layer's input, final before the
+  // router ran) are read now, while the wait is pending.
+  if (a.prenorm)
+    for (int p = threadIdx.x; p < a.B * 16; p += blockDim.x)
+      s_res[p] = __ldcg(a.x + (size_t)(p >> 4) * a.H + tile * 16 + (p & 15));
   pdl_wait();  // h comes from k_gateup
   pdl_trigger();
   FLINT_TRACE(a, 18);
@@ -1462,12 +1476,11 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
     float v = 0.f;
     for (int w2 = 0; w2 < nw; ++w2) v += acc_s[(w2 * a.B + t) * 16 + r];
     __nv_bfloat16 o = __float2bfloat16_rn(v);
-    const size_t at = (size_t)t * a.H + tile * 16 + r;
     if (a.prenorm) {  // residual stream: r + bf16(layer output), rounded to bf16
-      const uint32_t rb = (uint32_t)__ldcg(a.x + at) << 16;
+      const uint32_t rb = (uint32_t)s_res[p] << 16;
       o = __float2bfloat16_rn(__uint_as_float(rb) + __bfloat162float(o));
     }
-    a.out[at] = *reinterpret_cast<const uint16_t*>(&o);
+    a.out[(size_t)t * a.H + tile * 16 + r] = *reinterpret_cast<const uint16_t*>(&o);
   }
   FLINT_TRACE(a, 20);
 }
@@ -1841,7 +1854,9 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
 #else
   a.trace_seq = 0;
 #endif
-  const size_t route_smem = sizeof(RouteSmem) + 64;
+  // Static shared memory of the down kernels: the routing, the warp sums and
+  // the residual values.
+  const size_t route_smem = sizeof(RouteSmem) + sizeof(int) * MAX_WARPS + sizeof(uint16_t) * MAX_BATCH * 16 + 64;
   int gu_ng = 0;
   {
     const int units = a.W.max_slots * (a.I / 8), sms = sm_count();
