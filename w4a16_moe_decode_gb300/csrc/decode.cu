@@ -848,7 +848,10 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 gro
     const int slot = u / TILES, tile = u % TILES;
     const SlotInfo si = slot_info(a, R, slot);
     const int expert = si.expert;
-    const int nt_used = (32 - __clz(si.tmask) + 7) >> 3;  // token tiles up to the last selecting token
+    // One token tile (B <= 8): column c is token c. More: column c is the
+    // slot's c-th selecting token, so a slot chosen by few tokens needs one tile.
+    const int T = NTMAX == 1 ? a.B : __popc(si.tmask);
+    const int nt_used = (T + 7) >> 3;
     float acc[2][NTMAX][4];
 #pragma unroll
     for (int c = 0; c < 2; ++c)
@@ -859,9 +862,10 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 gro
     const bool ok = mbar_wait(wbar(b), par, status);
     if (jj == 0) FLINT_TRACE(a, 11);
     if (ok) {
-      int tok[NTMAX];  // column g of token tile nt is token 8 nt + g (past B: a repeat of token B - 1)
+      int tok[NTMAX];  // column 8 nt + g (past T: a repeat of the last selecting token)
 #pragma unroll
-      for (int nt = 0; nt < NTMAX; ++nt) tok[nt] = min(nt * 8 + g, a.B - 1);
+      for (int nt = 0; nt < NTMAX; ++nt)
+        tok[nt] = NTMAX == 1 ? min(g, a.B - 1) : nth_set_bit(si.tmask, min(nt * 8 + g, T - 1));
       const uint8_t* wb = wbuf(b);
 #pragma unroll 4
       for (int kl = 0; kl < KGW; ++kl) {
@@ -915,12 +919,13 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 gro
         gs += rb[(w2 * NTMAX + nt) * 128 + lane * 4 + hh];
         us += rb[(w2 * NTMAX + nt) * 128 + lane * 4 + 2 + hh];
       }
-      const int n = nt * 8 + 2 * t4 + hh;  // token
-      const size_t row = (size_t)slot * a.B + n;
-      const bool sel = n < a.B && ((si.tmask >> n) & 1u);
+      const int n = nt * 8 + 2 * t4 + hh;  // column
+      const bool sel = n < T && (NTMAX > 1 || ((si.tmask >> n) & 1u));
+      const int tk = NTMAX == 1 ? n : (sel ? nth_set_bit(si.tmask, n) : 0);  // its token
+      const size_t row = (size_t)slot * a.B + tk;
       float hv = 0.f;
       if (sel) {
-        const float inv = s_inv[n];
+        const float inv = s_inv[tk];
         const float gv = (gs * inv) * Gg;
         const float uv = (us * inv) * Gu;
         const float ey = 1.0f + expf(-gv);
@@ -1222,7 +1227,7 @@ __host__ __device__ inline DownPlan down_plan(int I, int B, int max_slots, int f
   p.wbuf_off = o;   o += (size_t)nw * nbuf * dn;
   p.h_off = o;      o += (size_t)hcap * p.hstride;
   p.acc_off = o;    o += sizeof(float) * nw * B * 16;
-  p.items_off = o;  o += sizeof(int) * 3 * max_slots * nt;
+  p.items_off = o;  o += sizeof(int) * 4 * max_slots * nt;
   p.hsc_off = o;    o += sizeof(float) * hcap;
   p.hinv_off = o;   o += sizeof(float) * hcap;
   o = (o + 15) & ~(size_t)15;
@@ -1246,7 +1251,8 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
   const int NBUF = P.nbuf;
   const int dn_bytes = (int)a.L.dn_tile;
   float* acc_s = reinterpret_cast<float*>(smem + P.acc_off);
-  int* s_items = reinterpret_cast<int*>(smem + P.items_off);  // per item: slot << 16 | tile << 8 | tokens, expert, first row
+  // per item: slot << 16 | chunk << 8 | count, expert, first staged row, token mask
+  int* s_items = reinterpret_cast<int*>(smem + P.items_off);
   float* s_hsc = reinterpret_cast<float*>(smem + P.hsc_off);  // staged row's max |h|
   float* s_hinv = reinterpret_cast<float*>(smem + P.hinv_off);  // staged row's inverse prescale
   uint8_t* hsm = smem + P.h_off;
@@ -1280,16 +1286,14 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
   route_select(a, R, true, blockIdx.x == 0, -1, ws_logits(a));
   FLINT_TRACE(a, 17);
   const int n_slots = route_slots(a, R);
-  {  // item list; items and staged rows counted in one packed prefix sum
+  {  // item list: chunks of up to 8 of a slot's selecting tokens; items and
+     // staged rows counted in one packed prefix sum
     const int spt = (n_slots + blockDim.x - 1) / blockDim.x;
     const int s0 = threadIdx.x * spt;
     int local = 0;
     for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
-      const uint32_t tm = slot_info(a, R, s).tmask;
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t bits = (tm >> (8 * nt)) & 0xFFu;
-        if (bits) local += (1 << 16) | __popc(bits);
-      }
+      const int T = __popc(slot_info(a, R, s).tmask);
+      local += (((T + 7) >> 3) << 16) | T;
     }
     int incl = local;
 #pragma unroll
@@ -1303,15 +1307,14 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
     for (int w2 = 0; w2 < warp; ++w2) run += s_wsum[w2];
     for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
       const SlotInfo si = slot_info(a, R, s);
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t bits = (si.tmask >> (8 * nt)) & 0xFFu;
-        if (bits) {
-          const int it = run >> 16;
-          s_items[3 * it] = (s << 16) | (nt << 8) | (int)bits;
-          s_items[3 * it + 1] = si.expert;
-          s_items[3 * it + 2] = run & 0xFFFF;
-          run += (1 << 16) | __popc(bits);
-        }
+      const int T = __popc(si.tmask);
+      for (int c = 0; 8 * c < T; ++c) {
+        const int it = run >> 16, cnt = min(8, T - 8 * c);
+        s_items[4 * it] = (s << 16) | (c << 8) | cnt;
+        s_items[4 * it + 1] = si.expert;
+        s_items[4 * it + 2] = run & 0xFFFF;
+        s_items[4 * it + 3] = (int)si.tmask;
+        run += (1 << 16) | cnt;
       }
     }
   }
@@ -1319,8 +1322,8 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
   int tot = 0;
   for (int w2 = 0; w2 < nw; ++w2) tot += s_wsum[w2];
   const int n_items = tot >> 16, n_rows = tot & 0xFFFF;
-  auto rowbase = [&](int i) { return i < n_items ? s_items[3 * i + 2] : n_rows; };
-  for (int j = w_issued; j < NBUF && warp + nw * j < n_items; ++j) issue_weights(j, s_items[3 * (warp + nw * j) + 1]);
+  auto rowbase = [&](int i) { return i < n_items ? s_items[4 * i + 2] : n_rows; };
+  for (int j = w_issued; j < NBUF && warp + nw * j < n_items; ++j) issue_weights(j, s_items[4 * (warp + nw * j) + 1]);
 
   const int KG = a.I / KG_COLS;
   // Round r stages the h rows of items i0 .. i1 - 1, as many as fit.
@@ -1358,27 +1361,27 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
     const int jend = i1 > warp ? (i1 - warp + nw - 1) / nw : 0;
     if (j < jend && !dead) {
       int myrows = 0;
-      for (int jj = j + lane; jj < jend; jj += 32) myrows += __popc((uint32_t)s_items[3 * (warp + nw * jj)] & 0xFFu);
+      for (int jj = j + lane; jj < jend; jj += 32) myrows += s_items[4 * (warp + nw * jj)] & 0xFF;
       myrows = __reduce_add_sync(0xffffffffu, myrows);
       if (lane == 0) mbar_arrive_expect_tx(hbar, (uint32_t)(myrows * a.I * 2));
       __syncwarp();
       for (int jj = j + lane; jj < jend; jj += 32) {
         const int it = warp + nw * jj;
-        const int code = s_items[3 * it], s = code >> 16, nt = (code >> 8) & 0xFF;
-        const uint32_t bits = (uint32_t)code & 0xFFu;
-        const int r0 = rowbase(it) - rb0, src0 = s * a.B + 8 * nt;
+        const int code = s_items[4 * it], s = code >> 16, c = (code >> 8) & 0xFF, cnt = code & 0xFF;
+        const uint32_t tm = (uint32_t)s_items[4 * it + 3];
+        const int r0 = rowbase(it) - rb0;
         unsigned hv[8];
 #pragma unroll
         for (int n = 0; n < 8; ++n) {  // copies first, then all the maxima in flight together
-          const int r = r0 + __popc(bits & ((1u << n) - 1u));
-          if ((bits >> n) & 1u) {
-            bulk_g2s(hsm + (size_t)r * P.hstride, h + (size_t)(src0 + n) * a.I, (uint32_t)(a.I * 2), hbar);
-            hv[n] = __ldcg(hmax + src0 + n);
+          if (n < cnt) {
+            const int src = s * a.B + nth_set_bit(tm, 8 * c + n);
+            bulk_g2s(hsm + (size_t)(r0 + n) * P.hstride, h + (size_t)src * a.I, (uint32_t)(a.I * 2), hbar);
+            hv[n] = __ldcg(hmax + src);
           }
         }
 #pragma unroll
         for (int n = 0; n < 8; ++n)
-          if ((bits >> n) & 1u) s_hsc[r0 + __popc(bits & ((1u << n) - 1u))] = __uint_as_float(hv[n]);
+          if (n < cnt) s_hsc[r0 + n] = __uint_as_float(hv[n]);
       }
       const bool okh = mbar_wait(hbar, hphase, status);
       hphase ^= 1;
@@ -1390,7 +1393,7 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
         if (i0 == 0 && warp == 0) FLINT_TRACE(a, 19);
         for (int jj = j; jj < jend; ++jj) {  // prescaled f16 (NVFP4) or kept (BF16)
           const int it = warp + nw * jj;
-          const int r0 = rowbase(it) - rb0, nrow = __popc((uint32_t)s_items[3 * it] & 0xFFu);
+          const int r0 = rowbase(it) - rb0, nrow = s_items[4 * it] & 0xFF;
           for (int r = r0; r < r0 + nrow; ++r) {
             int kh = 0;
             if (FMT == FLINT_MOE_NVFP4) {
@@ -1406,9 +1409,9 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
     }
     for (; !dead && warp + nw * j < i1; ++j) {
       const int it = warp + nw * j;
-      const int code = s_items[3 * it], s = code >> 16, nt = (code >> 8) & 0xFF;
-      const uint32_t bits = (uint32_t)code & 0xFFu;
-      const int expert = s_items[3 * it + 1], rb = rowbase(it) - rb0;
+      const int code = s_items[4 * it], s = code >> 16, c = (code >> 8) & 0xFF, cnt = code & 0xFF;
+      const uint32_t tm = (uint32_t)s_items[4 * it + 3];
+      const int expert = s_items[4 * it + 1], rb = rowbase(it) - rb0;
       const int b = j % NBUF;
       if (!mbar_wait(&wbars[b], (uint32_t)((j / NBUF) & 1), status)) {
         for (int jj = j; jj < j + NBUF && warp + nw * jj < n_items; ++jj)
@@ -1418,10 +1421,9 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
       }
       if (j == 0 && warp == 0) FLINT_TRACE(a, 15);
       const uint8_t* wb = wbuf(b);
-      // Column g is token 8 nt + g: its staged row if it selected the expert,
-      // else any staged row of the item (a column that is never combined).
-      const bool gsel = (bits >> g) & 1u;
-      const int grow = rb + (gsel ? __popc(bits & ((1u << g) - 1u)) : 0);
+      // Column n < cnt is the item's n-th token (staged row rb + n); the
+      // other columns read row rb and are never combined.
+      const int grow = rb + (g < cnt ? g : 0);
       float acc[2][1][4];
 #pragma unroll
       for (int c = 0; c < 2; ++c)
@@ -1442,20 +1444,20 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int n = 2 * t4 + hh;
-        if ((bits >> n) & 1u) {
-          const int tok = 8 * nt + n;
+        if (n < cnt) {
+          const int tok = nth_set_bit(tm, 8 * c + n);
           float wt = 1.0f;  // the shared experts are unweighted
           if (s >= a.S)
             for (int r = 0; r < a.k; ++r)
               if (R.idx[tok * a.k + r] == expert) wt = R.w[tok * a.k + r];
-          const float inv = s_hinv[rb + __popc(bits & ((1u << n) - 1u))];
+          const float inv = s_hinv[rb + n];
           float* dst = acc_s + (warp * a.B + tok) * 16;
           dst[g] += wt * (((acc[0][0][hh] + acc[1][0][hh]) * inv) * Gd);
           dst[g + 8] += wt * (((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * inv) * Gd);
         }
       }
       __syncwarp();
-      if (warp + nw * (j + NBUF) < n_items) issue_weights(j + NBUF, s_items[3 * (warp + nw * (j + NBUF)) + 1]);
+      if (warp + nw * (j + NBUF) < n_items) issue_weights(j + NBUF, s_items[4 * (warp + nw * (j + NBUF)) + 1]);
     }
     if (i1 < n_items) {     // another round reuses the staging area
       fence_proxy_async();  // reads of it come before the next round's copies into it
