@@ -196,6 +196,33 @@ def recorded_traffic(batch: int):
     return None
 
 
+# --------------------------------------------------------------------------- replicas (N GPUs)
+# The layer has no exchange step and runs at TP = 1, so N GPUs run N independent
+# replicas: rank r draws its own layers and tokens, every rank times the same
+# number of steps, and the job's time is the slowest rank's.
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Generator seed of rank `rank`'s layers and tokens."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    """The largest value of v over the ranks of the default process group."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_layer(ms_slowest: float, steps: int, world: int) -> float:
+    """Whole-job time per decoded layer: world * steps layers in the slowest
+    rank's time."""
+    return ms_slowest * 1000.0 / steps / world
+
+
 STACK_BIAS_FILE = os.path.join(ROOT, "tests", "golden", "flint_stack_bias.txt")
 
 
@@ -240,19 +267,15 @@ def gpu_arm(args) -> None:
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def slowest(v: float) -> float:
+        return max_over_ranks(v, world, dev)
 
     cfg = fb.make_config(**FLINT)
     P = args.layers
 
     def build_pool(B):
-        pool = [layers.synth_layer(cfg, args.seed + 1000 * rank, L, dev) for L in range(P)]
-        xs = [layers.synth_x(B, cfg.hidden, args.seed + 1000 * rank, L, dev) for L in range(P)]
+        pool = [layers.synth_layer(cfg, replica_seed(args.seed, rank), L, dev) for L in range(P)]
+        xs = [layers.synth_x(B, cfg.hidden, replica_seed(args.seed, rank), L, dev) for L in range(P)]
         outs = [torch.empty_like(x) for x in xs]
         ws = layers.workspace(cfg, B, dev)
         return pool, xs, outs, ws
@@ -321,7 +344,7 @@ def gpu_arm(args) -> None:
         st, bits = fb.flint_moe_read_status(ws, stream)
         if st != fb.OK or bits:
             raise RuntimeError(f"device status {bits} after the timed region")
-        return max_over_ranks(ms), clocks
+        return slowest(ms), clocks
 
     def isolated(pool, xs, outs, ws, B, reps=40):
         """One layer at a time with L2 flushed before each (256 MB write)."""
@@ -366,7 +389,7 @@ def gpu_arm(args) -> None:
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        return max_over_ranks(e0.elapsed_time(e1)) * 1000.0 / steps
+        return job_us_per_layer(slowest(e0.elapsed_time(e1)), steps, world)
 
     def stack_leg(batches=(1, 2, 4, 8, 16, 32), passes=20):
         """The 47-layer stack: distinct layers (generator seed 1000 + L) as
@@ -486,7 +509,7 @@ def gpu_arm(args) -> None:
     ds = distinct_per_layer(pool, xs, outs, ws, B)
     bytes_per_step = statistics.mean(unique_bytes(D, B) for D in ds)
     ms, clocks = timed_graph(pool, xs, outs, ws, B, K, W, sample_clocks=True)
-    us = ms * 1000.0 / K / world
+    us = job_us_per_layer(ms, K, world)
     us_rank = ms * 1000.0 / K
     gbs = bytes_per_step / (us_rank * 1e-6) / 1e9
     peak, peak_kind = measured_peak_gbs()
