@@ -46,6 +46,7 @@ def parse_args():
     p.add_argument("--quick", action="store_true", help="skip the batch-8, isolated, e2e, stack and CPU legs")
     p.add_argument("--stack-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--dense-only", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--bf16-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--oracle-leg", type=int, default=0, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -495,9 +496,64 @@ def gpu_arm(args) -> None:
         return {"workload": "y[B][N] = x[B][K] W^T, W NVFP4 [N][K] packed, bf16 x and y, FP32 accumulation",
                 "per_shape": res}
 
+    def bf16_leg(batches=(1, 8), n_layers=16, steps=2000):
+        """The same layer with BF16 expert weights (no quantisation): a rotation
+        of distinct seeded BF16 layers (45 MB touched per layer at batch 1, so
+        each rotation is far larger than L2), CUDA graph, PDL."""
+        cfg_b = fb.make_config(**FLINT, weight_fmt=fb.BF16)
+        pool_b = [layers.synth_layer(cfg_b, args.seed, L, dev) for L in range(n_layers)]
+        res = {}
+        peak = measured_peak_gbs()[0]
+        per_matrix = cfg_b.inter * cfg_b.hidden * 2
+        for Bb in batches:
+            xs_b = [layers.synth_x(Bb, cfg_b.hidden, args.seed, L, dev) for L in range(n_layers)]
+            outs_b = [torch.empty_like(x) for x in xs_b]
+            ws_b = layers.workspace(cfg_b, Bb, dev)
+            idx = torch.empty(Bb, cfg_b.top_k, dtype=torch.int32, device=dev)
+            w = torch.empty(Bb, cfg_b.top_k, dtype=torch.float32, device=dev)
+            dl = []
+            for L in range(n_layers):
+                fb.flint_moe_decode(pool_b[L].handle, xs_b[L], Bb, outs_b[L], ws_b)
+                fb.flint_moe_debug_routing(cfg_b, ws_b, Bb, idx, w)
+                dl.append(len(set(idx.cpu().numpy().ravel().tolist())))
+            stream = torch.cuda.Stream(device=dev)
+            stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(stream):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for L in range(n_layers):
+                        fb.flint_moe_decode(pool_b[L].handle, xs_b[L], Bb, outs_b[L], ws_b, stream)
+                for _ in range(3):
+                    g.replay()
+                reps = max(1, steps // n_layers)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+                stream.synchronize()
+            st, bits = fb.flint_moe_read_status(ws_b)
+            if st != fb.OK or bits:
+                raise RuntimeError(f"device status {bits} in the BF16 leg")
+            us = e0.elapsed_time(e1) * 1000.0 / (reps * n_layers)
+            ub = statistics.mean(cfg_b.num_experts * cfg_b.hidden * 2 + (D + cfg_b.n_shared) * 3 * per_matrix +
+                                 2 * Bb * cfg_b.hidden * 2 for D in dl)
+            res[str(Bb)] = {"us_per_layer": us, "gbs": ub / (us * 1e-6) / 1e9, "frac": ub / (us * 1e-6) / 1e9 / peak,
+                            "mean_distinct_experts": statistics.mean(dl), "unique_bytes_per_layer": ub}
+            del xs_b, outs_b, ws_b
+        del pool_b
+        torch.cuda.empty_cache()
+        return {"workload": f"Flint-shape layer with BF16 expert weights, {n_layers} distinct layers rotated",
+                "per_batch": res}
+
     if args.stack_only:
         if rank == 0:
             print(json.dumps({"stack": stack_leg()}))
+        return
+    if args.bf16_only:
+        if rank == 0:
+            print(json.dumps({"bf16_experts": bf16_leg()}))
         return
     if args.dense_only:
         if rank == 0:
@@ -535,6 +591,7 @@ def gpu_arm(args) -> None:
     if not args.quick and B == 1 and world == 1:
         extra["stack"] = stack_leg()
         extra["dense_gemv"] = dense_leg()
+        extra["bf16_experts"] = bf16_leg()
 
     if rank != 0:
         if world > 1:
