@@ -1,26 +1,30 @@
 // Decode step of the Flint-style W4A16 MoE layer on sm_103a: three kernels
-// chained with programmatic dependent launch (PDL).
+// chained with programmatic dependent launch (PDL), plus the dense GEMV.
 //
-//   k_router   logits = x Wr^T (FP32 accumulation); also writes the
-//              activations once in tensor-core fragment order.
-//   k_gateup   one block per (slot, 8 intermediate rows). A slot is one of the
-//              always-on shared experts or one of the distinct experts the
-//              batch selected (ascending id). Every block derives the routing
-//              itself from the 1 KB-per-token logits, bulk-copies its packed
-//              gate/up tile and the slot's activation rows into shared memory,
-//              dequantises into mma fragments and writes h = bf16(silu(g) * u).
-//   k_down     one block per 16 output rows: derives the routing *before*
-//              waiting for k_gateup and prefetches the down tiles it needs,
-//              then, once h exists, multiplies and accumulates w * y in a fixed
-//              slot order; writes out = bf16(sum).
+//   k_router      logits = x Wr^T (FP32 accumulation), optionally on the
+//                 RMS-normalised x; a block's router rows arrive by one bulk
+//                 copy before the wait, its warps split the tokens.
+//   k_gateup      persistent, one block per SM; warp groups take units (slot,
+//                 8 intermediate rows). A slot is one of the always-on shared
+//                 experts or one of the distinct experts the batch selected
+//                 (ascending id). Every block derives the selection itself from
+//                 the 1 KB-per-token logits, streams its units' packed gate/up
+//                 tiles into shared memory, dequantises into mma fragments and
+//                 writes h = bf16(silu(g) * u).
+//   k_down_items  (up to 4 tokens) / k_down (more): one block per 16 output
+//                 rows; routes and prefetches its down tiles *before* waiting
+//                 for k_gateup, then, once h exists, multiplies and accumulates
+//                 w * y per warp, adds the warps in a fixed order and writes
+//                 out = bf16(sum) (plus the residual for the pre-norm block).
+//   k_gemv        dense y = x W^T on the same packed layout.
 //
 // Launch order inside a layer and across layers (same stream):
 //   k_router waits for the previous layer, then lets k_gateup launch;
-//   k_gateup fetches the shared expert before its wait and lets k_down launch
-//   right after its wait (so the router has finished when k_down starts);
-//   k_down routes and fetches its weights while k_gateup runs, and waits only
-//   for h. Each kernel's routing-independent bytes therefore move while the
-//   previous kernel runs.
+//   k_gateup fetches the shared expert before its wait and lets the down kernel
+//   launch right after its wait (so the router has finished when it starts);
+//   the down kernel routes and fetches its weights while k_gateup runs, and
+//   waits only for h. Each kernel's routing-independent bytes therefore move
+//   while the previous kernel runs.
 //
 // "Day-0 Support for Flint on vLLM", section "Optimisation": the small-batch
 // MoE kernels read only the selected experts' weights; routing and the expert
