@@ -164,3 +164,39 @@ def test_synth_stream_key_matches_cpu_generator(lib):
     import synth
     for args in [(0, 0, 1, 0), (12345, 3, 4, 200), (2**63 + 5, 46, 2, 256)]:
         assert fb.flint_synth_stream_key(*args) == synth.stream_key(*args)
+
+
+def test_prefill_workspace_bytes(lib):
+    c = flint_cfg()
+    assert fb.flint_moe_prefill_workspace_bytes(c, 0) == 0
+    assert fb.flint_moe_prefill_workspace_bytes(c, 65537) == 0
+    assert fb.flint_moe_prefill_workspace_bytes(flint_cfg(weight_fmt=fb.BF16), 64) == 0  # NVFP4 only
+    w16, w512, w4096 = (fb.flint_moe_prefill_workspace_bytes(c, t) for t in (16, 512, 4096))
+    assert 0 < w16 < w512 < w4096
+    # the FP32 expert outputs y [T][S + k][H] and h [T (S + k)][I] bf16 dominate
+    assert w4096 >= 4096 * 7 * (2048 * 4 + 512 * 2)
+    assert w4096 < 4096 * 7 * (2048 * 4 + 512 * 2) * 1.1
+
+
+def test_prefill_rejects_bad_arguments_on_the_host(lib):
+    c = flint_cfg()
+    layer = fb.flint_moe_layer()
+    layer.cfg = c
+    layer.packed = 0x10000
+    layer.router = 0x20000
+    x, out, ws = 0x100000, 0x200000, 0x300000
+    need = fb.flint_moe_prefill_workspace_bytes(c, 64)
+    L = fb.lib()
+    P = L.flint_moe_prefill
+    assert P(ctypes.byref(layer), x, 0, out, ws, need, None) == fb.OK  # B = 0: nothing to do
+    assert P(ctypes.byref(layer), x, -1, out, ws, need, None) == fb.EINVAL
+    assert P(ctypes.byref(layer), x, 65537, out, ws, need, None) == fb.EINVAL
+    assert P(ctypes.byref(layer), None, 64, out, ws, need, None) == fb.EINVAL
+    assert P(ctypes.byref(layer), x, 64, out, None, need, None) == fb.EINVAL
+    assert P(ctypes.byref(layer), x + 2, 64, out, ws, need, None) == fb.EALIGN
+    assert P(ctypes.byref(layer), x, 64, out, ws + 16, need, None) == fb.EALIGN
+    assert P(ctypes.byref(layer), x, 64, out, ws, need - 1, None) == fb.EINVAL   # workspace too small
+    assert P(ctypes.byref(layer), x, 64, x + 4096, ws, need, None) == fb.EINVAL  # out overlaps x
+    assert P(None, x, 64, out, ws, need, None) == fb.EINVAL
+    layer.cfg.weight_fmt = fb.BF16
+    assert P(ctypes.byref(layer), x, 64, out, ws, need, None) == fb.EUNSUPPORTED

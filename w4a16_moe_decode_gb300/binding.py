@@ -94,6 +94,12 @@ def lib() -> ctypes.CDLL:
             "flint_gemv_unpack_debug": (c_int32, [c_void_p, c_int32, c_int32, c_int32, P(flint_gemv_src), c_void_p]),
             "flint_gemv": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                                      ctypes.c_float, c_void_p, c_void_p]),
+            "flint_moe_prefill_workspace_bytes": (c_size_t, [P(flint_moe_config), c_int32]),
+            "flint_moe_prefill_workspace_init": (c_int32, [P(flint_moe_config), c_int32, c_void_p, c_void_p]),
+            "flint_moe_prefill": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p, c_size_t,
+                                            c_void_p]),
+            "flint_moe_prefill_debug_routing": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_void_p, c_void_p,
+                                                          c_void_p, c_void_p]),
             "flint_synth_stream_key": (ctypes.c_uint64, [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
                                                          ctypes.c_uint32]),
             "flint_synth_normal": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint64, c_size_t, ctypes.c_float, c_int32,
@@ -207,6 +213,28 @@ def flint_moe_decode_noalloc(layer: flint_moe_layer, x, B: int, out, stream=None
     place of a workspace, for callers that cannot allocate device memory."""
     _check("flint_moe_decode_noalloc", lib().flint_moe_decode_noalloc(ctypes.byref(layer), _ptr(x), B, _ptr(out),
                                                                       _stream(stream)))
+
+
+def flint_moe_prefill_workspace_bytes(cfg: flint_moe_config, max_tokens: int) -> int:
+    return lib().flint_moe_prefill_workspace_bytes(ctypes.byref(cfg), max_tokens)
+
+
+def flint_moe_prefill_workspace_init(cfg, max_tokens, workspace, stream=None) -> None:
+    _check("flint_moe_prefill_workspace_init",
+           lib().flint_moe_prefill_workspace_init(ctypes.byref(cfg), max_tokens, _ptr(workspace), _stream(stream)))
+
+
+def flint_moe_prefill(layer: flint_moe_layer, x, B: int, out, workspace, workspace_bytes=None, stream=None) -> None:
+    """The expert-grouped tensor-core path for B tokens (include/flint_moe_prefill.h)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    _check("flint_moe_prefill", lib().flint_moe_prefill(ctypes.byref(layer), _ptr(x), B, _ptr(out), _ptr(workspace),
+                                                        nbytes, _stream(stream)))
+
+
+def flint_moe_prefill_debug_routing(cfg, workspace, B, idx, w, logits=None, stream=None) -> None:
+    _check("flint_moe_prefill_debug_routing",
+           lib().flint_moe_prefill_debug_routing(ctypes.byref(cfg), _ptr(workspace), B, _ptr(idx), _ptr(w),
+                                                 _ptr(logits), _stream(stream)))
 
 
 def flint_moe_debug_routing(cfg, workspace, B, idx, w, stream=None) -> None:

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.environ.get("FLINT_MOE_LIB") or os.path.join(PKG, "libflint_moe.so")
-SOURCES = ["decode.cu", "pack.cu", "synth.cu"]
+SOURCES = ["decode.cu", "pack.cu", "synth.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

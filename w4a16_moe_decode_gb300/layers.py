@@ -128,3 +128,12 @@ def workspace(cfg, max_batch: int, device="cuda") -> torch.Tensor:
     ws = torch.empty(fb.flint_moe_workspace_bytes(cfg, max_batch), dtype=torch.uint8, device=device)
     fb.flint_moe_workspace_init(cfg, max_batch, ws)
     return ws
+
+
+def prefill_workspace(cfg, max_tokens: int, device="cuda") -> torch.Tensor:
+    nbytes = fb.flint_moe_prefill_workspace_bytes(cfg, max_tokens)
+    if nbytes == 0:
+        raise ValueError("configuration or token count not supported by the prefill path")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    fb.flint_moe_prefill_workspace_init(cfg, max_tokens, ws)
+    return ws
