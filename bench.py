@@ -47,6 +47,7 @@ def parse_args():
     p.add_argument("--stack-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--dense-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--bf16-only", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--prefill-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--oracle-leg", type=int, default=0, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -174,6 +175,16 @@ def measured_peak_gbs() -> tuple[float, str]:
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback"
+
+
+def measured_peak_tflops() -> tuple[float, str]:
+    """Dense bf16 tensor-core peak (cuBLAS burst, measured on this part)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
 
 
 def recorded_traffic(batch: int):
@@ -547,6 +558,78 @@ def gpu_arm(args) -> None:
         return {"workload": f"Flint-shape layer with BF16 expert weights, {n_layers} distinct layers rotated",
                 "per_batch": res}
 
+    def prefill_leg(batches=(16, 32, 64, 128, 256, 512, 1024, 4096), n_layers=8, max_calls=400):
+        """The expert-grouped tensor-core path (flint_moe_prefill) on a rotation of
+        distinct seeded Flint-shape layers (every layer's touched experts are
+        read from HBM: 8 layers hold 3.6 GB), one CUDA graph per batch size;
+        the decode path on the same layers beside it up to 32 tokens."""
+        pool_p = [layers.synth_layer(cfg, args.seed, L, dev) for L in range(n_layers)]
+        peak_tf, peak_tf_kind = measured_peak_tflops()
+        peak = measured_peak_gbs()[0]
+        res = {}
+        for Bp in batches:
+            xs_p = [layers.synth_x(Bp, cfg.hidden, args.seed, L, dev) for L in range(n_layers)]
+            outs_p = [torch.empty_like(x) for x in xs_p]
+            ws_p = layers.prefill_workspace(cfg, Bp, dev)
+            idx = torch.empty(Bp, cfg.top_k, dtype=torch.int32, device=dev)
+            w = torch.empty(Bp, cfg.top_k, dtype=torch.float32, device=dev)
+            dl = []
+            for L in range(n_layers):
+                fb.flint_moe_prefill(pool_p[L].handle, xs_p[L], Bp, outs_p[L], ws_p)
+                fb.flint_moe_prefill_debug_routing(cfg, ws_p, Bp, idx, w)
+                dl.append(len(set(idx.cpu().numpy().ravel().tolist())))
+
+            def time_graph(call):
+                stream = torch.cuda.Stream(device=dev)
+                stream.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(stream):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for L in range(n_layers):
+                            call(L, stream)
+                    for _ in range(3):
+                        g.replay()
+                    reps = max(3, max_calls // n_layers if Bp <= 1024 else 64 // n_layers)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    e1.record(stream)
+                    stream.synchronize()
+                return e0.elapsed_time(e1) * 1000.0 / (reps * n_layers)
+
+            us = time_graph(lambda L, st: fb.flint_moe_prefill(pool_p[L].handle, xs_p[L], Bp, outs_p[L], ws_p,
+                                                               None, st))
+            stt, bits = fb.flint_moe_read_status(ws_p)
+            if stt != fb.OK or bits:
+                raise RuntimeError(f"device status {bits} in the prefill leg")
+            flops = 2.0 * Bp * cfg.num_experts * cfg.hidden + 6.0 * Bp * (cfg.top_k + cfg.n_shared) * cfg.hidden * \
+                cfg.inter
+            ub = statistics.mean(unique_bytes(D, Bp) for D in dl)
+            tf = flops / (us * 1e-6) / 1e12
+            r = {"us_per_layer": us, "tokens_per_s": Bp / (us * 1e-6), "tflops": tf, "tflops_frac": tf / peak_tf,
+                 "gbs": ub / (us * 1e-6) / 1e9, "gbs_frac": ub / (us * 1e-6) / 1e9 / peak,
+                 "mean_distinct_experts": statistics.mean(dl), "unique_bytes_per_layer": ub,
+                 "flops_per_layer": flops}
+            if Bp <= 32:
+                ws_d = layers.workspace(cfg, Bp, dev)
+                r["decode_path_us_per_layer"] = time_graph(
+                    lambda L, st: fb.flint_moe_decode(pool_p[L].handle, xs_p[L], Bp, outs_p[L], ws_d, st))
+                del ws_d
+            res[str(Bp)] = r
+            del xs_p, outs_p, ws_p
+            torch.cuda.empty_cache()
+        del pool_p
+        torch.cuda.empty_cache()
+        return {"workload": f"Flint-shape NVFP4 layer, {n_layers} distinct layers rotated, B tokens per call",
+                "tflops_peak": peak_tf, "tflops_peak_kind": peak_tf_kind,
+                "flops": "2 B E H (router) + 6 B (k + S) H I (gate, up, down)", "per_batch": res}
+
+    if args.prefill_only:
+        if rank == 0:
+            print(json.dumps({"prefill": prefill_leg()}))
+        return
     if args.stack_only:
         if rank == 0:
             print(json.dumps({"stack": stack_leg()}))
@@ -592,6 +675,7 @@ def gpu_arm(args) -> None:
         extra["stack"] = stack_leg()
         extra["dense_gemv"] = dense_leg()
         extra["bf16_experts"] = bf16_leg()
+        extra["prefill"] = prefill_leg()
 
     if rank != 0:
         if world > 1:

@@ -20,6 +20,8 @@
 #include <atomic>
 #include <cmath>
 
+#include <cuda.h>  // CUtensorMap and its enums (types only; the encoder comes through the runtime)
+
 #include "common.cuh"
 #include "flint_moe_prefill.h"
 
@@ -29,9 +31,7 @@ namespace pf {
 constexpr int BM = 128;       // weight rows per tile (MMA M)
 constexpr int BK = 64;        // k per pipeline stage: one 128-byte swizzle row of bf16
 constexpr int NT = 128;       // tokens per tile at most (MMA N)
-constexpr int STAGES = 4;     // shared-memory stages
-constexpr int PREF = 2;       // k-blocks loaded ahead of the one being consumed
-constexpr int THREADS = 256;  // 8 warps: each dequantises one 16-row packed tile per stage
+constexpr int STAGES = 4;     // operand stages in shared memory
 constexpr uint32_t TMEM_COLS = 2 * NT;  // N <= NT columns are used; the margin costs nothing at one CTA per SM
 constexpr int A_STAGE = BM * BK * 2;              // 16 KiB
 constexpr int B_STAGE = NT * BK * 2;              // 16 KiB
@@ -44,7 +44,7 @@ enum : int { PF_STATUS = HDR_STATUS, PF_NSLOTS = 2, PF_NGU = 3, PF_NDN = 4 };
 // Workspace: header words, then 256-byte aligned regions sized for T tokens.
 struct PfLayout {
   size_t counts, logits, idx, w, pos, slot_expert, slot_row0, slot_count, list_tok, list_q, list_w, gu_tiles,
-      dn_tiles, h, y, total;
+      dn_tiles, xg, h, y, total;
   int max_slots, max_rows, max_gu, max_dn;
 };
 
@@ -70,6 +70,7 @@ __host__ __device__ inline PfLayout make_pf_layout(int H, int E, int k, int I, i
   W.list_w = o;      o = ws_align(o + sizeof(float) * (size_t)W.max_rows);
   W.gu_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_gu);
   W.dn_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_dn);
+  W.xg = o;          o = ws_align(o + (size_t)2 * T * k * H);  // routed pairs' activation rows, grouped
   W.h = o;           o = ws_align(o + (size_t)2 * W.max_rows * I);
   W.y = o;           o = ws_align(o + sizeof(float) * (size_t)W.max_rows * H);
   W.total = o;
@@ -177,22 +178,109 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
 
 // ---------------------------------------------------------------------------
 // The grouped GEMM. A tile is (slot, m-tile of 128 weight rows, first grouped
-// row, token count n <= NT); the kernel is persistent over its tile list.
+// row, token count n <= NT); the kernel is persistent over its tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ..., and treats their k-blocks as one
+// stream: k-block g of the CTA is k-block g % KB of its tile g / KB.
+//
+// Warp roles, handing off through mbarriers only (no block-wide barrier in
+// the main loop):
+//   warp 16  streams the packed weight k-blocks (bulk copies) into a ring of
+//            RAW_ST slots, as far ahead as the ring allows, across tiles;
+//   warp 17  loads each k-block's 128 activation rows (and the router's
+//            weight rows) with TMA in the 128-byte swizzle into the stage;
+//   warp 18  issues the four MMAs of a k-block once both operands are in,
+//            commits them to the stage's mbarrier, and after a tile's last
+//            k-block to the accumulator buffer's mbarrier;
+//   warps 0-15 dequantise the packed k-block into the stage's bf16 operand
+//            (warp w: packed tile w % 8, k-steps 2 (w / 8) and 2 (w / 8) + 1)
+//            and run the epilogue of each tile from tensor memory. Two
+//            accumulator buffers (columns 0-127, 128-255) let the MMAs of the
+//            next tile start before the epilogue of this one has finished.
 // ---------------------------------------------------------------------------
-struct GemmSmem {
-  uint64_t raw_full[STAGES];
-  uint64_t mma_done[STAGES];
-  uint32_t tmem_base;
-  const uint16_t* src[NT];  // activation row of each tile column
-  int col_tok[NT];
-  int col_q[NT];
-  float col_w[NT];
+constexpr int CWARPS = 16;
+constexpr int W_RAW = 16, W_B = 17, W_MMA = 18;
+constexpr int GEMM_THREADS = 19 * 32;
+constexpr int RAW_ST = 12;  // packed weight k-blocks in flight
+
+struct PfMaps {  // TMA descriptors, bf16, 64-column x 128-row boxes, 128-byte swizzle
+  CUtensorMap a;   // router rows (router GEMM)
+  CUtensorMap b0;  // activations: x (router GEMM, shared experts' gate/up), h (down)
+  CUtensorMap b1;  // the routed pairs' grouped activation rows (gate/up)
 };
 
-constexpr size_t gemm_dyn_smem() { return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE + RAW_STAGE); }
+struct GemmSmem {
+  uint64_t raw_full[RAW_ST];
+  uint64_t raw_empty[RAW_ST];
+  uint64_t b_full[STAGES];
+  uint64_t a_ready[STAGES];
+  uint64_t mma_done[STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t gemm_dyn_smem() {
+  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + (size_t)RAW_ST * RAW_STAGE;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// 2-D TMA tile load (box from the descriptor) into shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Bounded wait that also gives up as soon as another warp of the CTA has given up.
+__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 63) {
+      if (*abort) return false;
+      if (global_ns() - t0 > WAIT_LIMIT_NS) {
+        atomicOr(status, FLINT_MOE_DEV_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+struct TileInfo {
+  int slot, mt, row0, n, expert;
+};
 
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1) k_pf_gemm(PfArgs a) {
+__device__ __forceinline__ TileInfo tile_info(const PfArgs& a, int tile) {
+  TileInfo t;
+  if (MODE == ROUTER) {
+    const int mtc = (a.E + BM - 1) / BM;
+    t.slot = 0;
+    t.mt = tile % mtc;
+    t.row0 = (tile / mtc) * NT;
+    t.n = min(NT, a.B - t.row0);
+    t.expert = 0;
+  } else {
+    const int4 v = __ldcg(ws_at<const int4>(a, MODE == GATEUP ? a.W.gu_tiles : a.W.dn_tiles) + tile);
+    t.slot = v.x;
+    t.mt = v.y;
+    t.row0 = v.z;
+    t.n = v.w;
+    t.expert = __ldcg(ws_at<const int>(a, a.W.slot_expert) + v.x);
+  }
+  return t;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, const __grid_constant__ PfMaps maps) {
   extern __shared__ uint8_t dsmem[];
   __shared__ GemmSmem G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -200,26 +288,34 @@ __global__ void __launch_bounds__(THREADS, 1) k_pf_gemm(PfArgs a) {
   uint8_t* const base_ptr = dsmem + (base - smem_addr(dsmem));
   const uint32_t a_op = base;                                   // STAGES x 16 KiB
   const uint32_t b_op = base + STAGES * A_STAGE;                // STAGES x 16 KiB
-  uint8_t* const raw = base_ptr + STAGES * (A_STAGE + B_STAGE);  // STAGES x 4608 B
+  uint8_t* const raw = base_ptr + STAGES * (A_STAGE + B_STAGE);  // RAW_ST x 4608 B
   int* status = ws_at<int>(a, 0) + PF_STATUS;
+  volatile int* abort = &G.abort;
 
   const int K = MODE == DOWN ? a.I : a.H;
   const int KB = K / BK;
-  int n_tiles, mt_count = 0, nt_count = 0;
-  if (MODE == ROUTER) {
-    mt_count = (a.E + BM - 1) / BM;
-    nt_count = (a.B + NT - 1) / NT;
-    n_tiles = mt_count * nt_count;
-  } else {
-    n_tiles = __ldcg(ws_at<int>(a, 0) + (MODE == GATEUP ? PF_NGU : PF_NDN));
-  }
+  const int n_tiles = MODE == ROUTER ? ((a.E + BM - 1) / BM) * ((a.B + NT - 1) / NT)
+                                     : __ldcg(ws_at<int>(a, 0) + (MODE == GATEUP ? PF_NGU : PF_NDN));
   if ((int)blockIdx.x >= n_tiles) return;  // uniform: no tensor memory taken
+  const int my_tiles = (n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int total = my_tiles * KB;  // k-blocks of this CTA
+  auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < RAW_ST; ++s) {
       mbar_init(&G.raw_full[s], 1);
+      mbar_init(&G.raw_empty[s], CWARPS);
+    }
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&G.b_full[s], 1);
+      mbar_init(&G.a_ready[s], CWARPS);
       mbar_init(&G.mma_done[s], 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&G.acc_full[b], 1);
+      mbar_init(&G.acc_empty[b], CWARPS);
+    }
+    G.abort = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -233,208 +329,211 @@ __global__ void __launch_bounds__(THREADS, 1) k_pf_gemm(PfArgs a) {
   tc_fence_after();
   const uint32_t tmem = G.tmem_base;
 
-  const int* slot_expert = ws_at<int>(a, a.W.slot_expert);
-  const int4* tiles = ws_at<int4>(a, MODE == GATEUP ? a.W.gu_tiles : a.W.dn_tiles);
-  const int* list_tok = ws_at<int>(a, a.W.list_tok);
-  const int* list_q = ws_at<int>(a, a.W.list_q);
-  const float* list_w = ws_at<float>(a, a.W.list_w);
-  uint16_t* hbuf = ws_at<uint16_t>(a, a.W.h);
-
-  uint32_t gk = 0;  // k-blocks this CTA has started, over all its tiles (stage = gk % STAGES)
-  bool failed = false;
-  for (int tile = blockIdx.x; tile < n_tiles && !failed; tile += gridDim.x) {
-    int slot = 0, mt, row0, n;
-    if (MODE == ROUTER) {
-      mt = tile % mt_count;
-      row0 = (tile / mt_count) * NT;
-      n = min(NT, a.B - row0);
-    } else {
-      const int4 t = __ldcg(tiles + tile);
-      slot = t.x;
-      mt = t.y;
-      row0 = t.z;
-      n = t.w;
-    }
-    const int expert = MODE == ROUTER ? 0 : __ldcg(slot_expert + slot);
-    for (int i = threadIdx.x; i < NT; i += THREADS) {
-      const uint16_t* s = nullptr;
-      if (i < n) {
-        if (MODE == ROUTER) s = a.x + (size_t)(row0 + i) * a.H;
-        if (MODE == GATEUP) s = a.x + (size_t)__ldcg(list_tok + row0 + i) * a.H;
-        if (MODE == DOWN) {
-          s = hbuf + (size_t)(row0 + i) * a.I;
-          G.col_tok[i] = __ldcg(list_tok + row0 + i);
-          G.col_q[i] = __ldcg(list_q + row0 + i);
-          G.col_w[i] = __ldcg(list_w + row0 + i);
+  if (warp == W_RAW) {
+    // ---------------- packed weight k-blocks -> raw ring ----------------
+    if (MODE != ROUTER && lane == 0) {
+      int q = 0;
+      TileInfo nxt = tile_info<MODE>(a, tile_of(0));
+      const uint8_t* wbase = nullptr;
+      int64_t wtile = 0;
+      for (; q < total; ++q) {
+        const int slot = q % RAW_ST, i = q / KB, kb = q % KB;
+        if (q >= RAW_ST && !wait_ab(&G.raw_empty[slot], ((q / RAW_ST) - 1) & 1, abort, status)) break;
+        if (kb == 0) {
+          const TileInfo t = nxt;
+          if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
+          const uint8_t* eb = a.packed + (int64_t)t.expert * a.L.expert_bytes;
+          wtile = MODE == GATEUP ? a.L.gu_tile : a.L.dn_tile;
+          wbase = eb + (MODE == GATEUP ? 0 : a.L.gu_bytes) + (int64_t)(t.mt * 8) * wtile;
         }
-      }
-      G.src[i] = s;
-    }
-    __syncthreads();
-
-    // Packed weight tiles of this m-tile: tile p of the expert's gate/up or down run.
-    const uint8_t* wbase = nullptr;
-    int64_t wtile = 0;
-    if (MODE == GATEUP) {
-      wbase = a.packed + (int64_t)expert * a.L.expert_bytes + (int64_t)(mt * 8) * a.L.gu_tile;
-      wtile = a.L.gu_tile;
-    } else if (MODE == DOWN) {
-      wbase = a.packed + (int64_t)expert * a.L.expert_bytes + a.L.gu_bytes + (int64_t)(mt * 8) * a.L.dn_tile;
-      wtile = a.L.dn_tile;
-    }
-
-    // Loads of k-block kb of this tile into stage s.
-    auto issue = [&](int kb, int s) {
-      if (MODE == ROUTER) {
-        for (int c = threadIdx.x; c < BM * 8; c += THREADS) {
-          const int r = c >> 3, ch = c & 7, e = mt * BM + r;
-          const uint16_t* src = a.router + (size_t)(e < a.E ? e : 0) * a.H + kb * BK + ch * 8;
-          cp_async16(a_op + s * A_STAGE + sw128_off(r, ch * 8), src, e < a.E ? 16u : 0u);
-        }
-      } else if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&G.raw_full[s], (uint32_t)RAW_STAGE);
+        mbar_arrive_expect_tx(&G.raw_full[slot], (uint32_t)RAW_STAGE);
         for (int p = 0; p < BM / 16; ++p)
-          bulk_g2s_stream(raw + s * RAW_STAGE + p * KG_NVFP4, wbase + p * wtile + (int64_t)kb * KG_NVFP4,
-                          (uint32_t)KG_NVFP4, &G.raw_full[s]);
+          bulk_g2s_stream(raw + slot * RAW_STAGE + p * KG_NVFP4, wbase + p * wtile + (int64_t)kb * KG_NVFP4,
+                          (uint32_t)KG_NVFP4, &G.raw_full[slot]);
       }
-      for (int c = threadIdx.x; c < n * 8; c += THREADS) {
-        const int r = c >> 3, ch = c & 7;
-        cp_async16(b_op + s * B_STAGE + sw128_off(r, ch * 8), G.src[r] + kb * BK + ch * 8, 16u);
-      }
-    };
-
-    const uint32_t g0 = gk;
-    bool ok = true;
-    for (int p = 0; p < PREF; ++p) {
-      const uint32_t gq = g0 + p;
-      if (p < KB) {
-        if (gq >= STAGES) ok &= mbar_wait(&G.mma_done[gq % STAGES], ((gq / STAGES) - 1) & 1, status);
-        if (ok) issue(p, gq % STAGES);
-      }
-      cp_async_commit();
+      // The CTA's memory must outlive every copy this warp started.
+      for (int r = (q > RAW_ST ? q - RAW_ST : 0); r < q; ++r) mbar_drain(&G.raw_full[r % RAW_ST], (r / RAW_ST) & 1);
     }
-    const uint32_t idesc = idesc_bf16_f32(BM, (n + 15) & ~15);
-    for (int kb = 0; kb < KB; ++kb) {
-      const uint32_t g = g0 + kb, s = g % STAGES;
-      cp_async_wait<PREF - 1>();
-      if (MODE != ROUTER && ok) {
-        ok = mbar_wait(&G.raw_full[s], (g / STAGES) & 1, status);
-        if (ok) {
-          // Warp w dequantises packed tile w: rows 16 w .. 16 w + 15 of the block.
-          const uint8_t* kp = raw + s * RAW_STAGE + warp * KG_NVFP4;
-          const uint4 codes = lds128(kp + lane * 16);
-          const int gr = lane >> 2, t4 = lane & 3;
-          const uint32_t sg = lds32(kp + KG_CODE_BYTES + gr * 4);
-          const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (gr + 8) * 4);
-          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-          uint8_t* ap = base_ptr + s * A_STAGE;
-          const int r0 = warp * 16 + gr;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            uint32_t af[4];
-            nvfp4_afrag(cw[ks], sg, sg8, ks, af);
-            const int c0 = ks * 16 + 2 * t4;
-            *reinterpret_cast<uint32_t*>(ap + sw128_off(r0, c0)) = f16x2_to_bf16x2(af[0]);
-            *reinterpret_cast<uint32_t*>(ap + sw128_off(r0 + 8, c0)) = f16x2_to_bf16x2(af[1]);
-            *reinterpret_cast<uint32_t*>(ap + sw128_off(r0, c0 + 8)) = f16x2_to_bf16x2(af[2]);
-            *reinterpret_cast<uint32_t*>(ap + sw128_off(r0 + 8, c0 + 8)) = f16x2_to_bf16x2(af[3]);
-          }
+  } else if (warp == W_B) {
+    // ---------------- activation (and router weight) k-blocks -> stages, TMA ----------------
+    if (lane == 0) {
+      int q = 0;
+      TileInfo nxt = tile_info<MODE>(a, tile_of(0)), t = nxt;
+      for (; q < total; ++q) {
+        const int s = q % STAGES, i = q / KB, kb = q % KB;
+        if (q >= STAGES && !wait_ab(&G.mma_done[s], ((q / STAGES) - 1) & 1, abort, status)) break;
+        if (kb == 0) {
+          t = nxt;
+          if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
+        }
+        mbar_arrive_expect_tx(&G.b_full[s], (uint32_t)(MODE == ROUTER ? A_STAGE + B_STAGE : B_STAGE));
+        if (MODE == ROUTER) {
+          tma_load_2d(a_op + s * A_STAGE, &maps.a, kb * BK, t.mt * BM, &G.b_full[s]);
+          tma_load_2d(b_op + s * B_STAGE, &maps.b0, kb * BK, t.row0, &G.b_full[s]);
+        } else if (MODE == GATEUP) {
+          if (t.slot < a.S)  // a shared expert's rows are the tokens in order
+            tma_load_2d(b_op + s * B_STAGE, &maps.b0, kb * BK, t.row0 - t.slot * a.B, &G.b_full[s]);
+          else
+            tma_load_2d(b_op + s * B_STAGE, &maps.b1, kb * BK, t.row0 - a.S * a.B, &G.b_full[s]);
+        } else {
+          tma_load_2d(b_op + s * B_STAGE, &maps.b0, kb * BK, t.row0, &G.b_full[s]);
         }
       }
-      fence_proxy_async();  // this thread's cp.async and st.shared data -> visible to the tensor core
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
-      if (threadIdx.x == 0) {
+      for (int r = (q > STAGES ? q - STAGES : 0); r < q; ++r) mbar_drain(&G.b_full[r % STAGES], (r / STAGES) & 1);
+    }
+  } else if (warp == W_MMA) {
+    // ---------------- tensor-core issue ----------------
+    if (lane == 0) {
+      int g = 0;
+      TileInfo nxt = tile_info<MODE>(a, tile_of(0));
+      uint32_t idesc = 0, acc = tmem;
+      for (; g < total; ++g) {
+        const int s = g % STAGES, i = g / KB, kb = g % KB;
+        if (kb == 0) {
+          const TileInfo t = nxt;
+          if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
+          idesc = idesc_bf16_f32(BM, (t.n + 15) & ~15);
+          acc = tmem + (uint32_t)((i & 1) * NT);
+          if (i >= 2 && !wait_ab(&G.acc_empty[i & 1], ((i / 2) - 1) & 1, abort, status)) break;
+        }
+        if (!wait_ab(&G.b_full[s], (g / STAGES) & 1, abort, status)) break;
+        if (MODE != ROUTER && !wait_ab(&G.a_ready[s], (g / STAGES) & 1, abort, status)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks)
-          tc_mma(tmem, sw128_desc(a_op + s * A_STAGE + ks * 32), sw128_desc(b_op + s * B_STAGE + ks * 32), idesc,
+          tc_mma(acc, sw128_desc(a_op + s * A_STAGE + ks * 32), sw128_desc(b_op + s * B_STAGE + ks * 32), idesc,
                  (kb > 0 || ks > 0) ? 1u : 0u);
         tc_commit(&G.mma_done[s]);
+        if (kb == KB - 1) tc_commit(&G.acc_full[i & 1]);
       }
-      // Prefetch k-block kb + PREF once the MMAs that last read its stage are done.
-      const int kn = kb + PREF;
-      if (kn < KB) {
-        const uint32_t gq = g0 + kn;
-        if (gq >= STAGES) ok &= mbar_wait(&G.mma_done[gq % STAGES], ((gq / STAGES) - 1) & 1, status);
-        if (ok) issue(kn, gq % STAGES);
+      // Let the MMAs in flight finish before the memory goes away.
+      for (int r = (g > STAGES ? g - STAGES : 0); r < g; ++r) mbar_drain(&G.mma_done[r % STAGES], (r / STAGES) & 1);
+    }
+  } else {
+    // ---------------- consumers: dequantise, epilogue ----------------
+    TileInfo nxt = tile_info<MODE>(a, tile_of(0)), t = nxt;
+    const int q4 = warp & 3, cg = warp >> 2;  // epilogue: lanes 32 q4.., columns 32 cg..
+    int ctok = 0, cq = 0;
+    float cw = 0.f;
+    for (int g = 0; g < total; ++g) {
+      const int s = g % STAGES, i = g / KB, kb = g % KB;
+      if (kb == 0) {
+        t = nxt;
+        if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
+        if (MODE == DOWN && cg * 32 + lane < t.n) {  // this lane's epilogue column
+          const int row = t.row0 + cg * 32 + lane;
+          ctok = __ldcg(ws_at<const int>(a, a.W.list_tok) + row);
+          cq = __ldcg(ws_at<const int>(a, a.W.list_q) + row);
+          cw = __ldcg(ws_at<const float>(a, a.W.list_w) + row);
+        }
       }
-      cp_async_commit();
-    }
-    gk = g0 + KB;
-    if (failed) break;
-    // All MMAs of the tile: the commit of its last k-block covers them.
-    ok = mbar_wait(&G.mma_done[(gk - 1) % STAGES], ((gk - 1) / STAGES) & 1, status);
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-
-    // Epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (weight
-    // rows), columns 64 (w / 4) .. + 63 (tokens), 16 at a time.
-    const int q4 = warp & 3, chalf = warp >> 2;
-    const int r = q4 * 32 + lane;  // weight row within the m-tile
-    for (int c0 = chalf * 64; c0 < chalf * 64 + 64 && c0 < n; c0 += 16) {
-      uint32_t v[16];
-      tc_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)c0, v);
-      if (MODE == ROUTER) {
-        const int e = mt * BM + r;
-        float* logits = ws_at<float>(a, a.W.logits);
+      if (MODE != ROUTER) {
+        bool ok = g < STAGES || wait_ab(&G.mma_done[s], ((g / STAGES) - 1) & 1, abort, status);
+        ok = ok && wait_ab(&G.raw_full[g % RAW_ST], (g / RAW_ST) & 1, abort, status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int p = warp & 7, hs = warp >> 3;
+        const uint8_t* kp = raw + (g % RAW_ST) * RAW_STAGE + p * KG_NVFP4;
+        uint2 codes;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(codes.x), "=r"(codes.y)
+                     : "r"(smem_addr(kp + lane * 16 + hs * 8)));
+        const int gr = lane >> 2, t4 = lane & 3;
+        const uint32_t sg = lds32(kp + KG_CODE_BYTES + gr * 4);
+        const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (gr + 8) * 4);
+        uint8_t* ap = base_ptr + s * A_STAGE;
+        const int r0 = p * 16 + gr;
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (e < a.E && c0 + j < n) logits[(size_t)(row0 + c0 + j) * a.E + e] = __uint_as_float(v[j]);
-      } else if (MODE == GATEUP) {
-        // Rows 16 t .. 16 t + 7 of packed tile t are gate rows, the next 8 the
-        // up rows of the same intermediate indices (8 (8 mt + t) + r % 8).
-        const float Gg = a.globals[expert * 4 + 0], Gu = a.globals[expert * 4 + 1];
-        const bool gate = (lane & 8) == 0;
-        const int i = (mt * 8 + q4 * 2 + (lane >> 4)) * 8 + (lane & 7);
+        for (int h = 0; h < 2; ++h) {
+          const int ks = 2 * hs + h;
+          uint32_t af[4];
+          nvfp4_afrag(h ? codes.y : codes.x, sg, sg8, ks, af);
+          const int c0 = ks * 16 + 2 * t4;
+          *reinterpret_cast<uint32_t*>(ap + sw128_off(r0, c0)) = f16x2_to_bf16x2(af[0]);
+          *reinterpret_cast<uint32_t*>(ap + sw128_off(r0 + 8, c0)) = f16x2_to_bf16x2(af[1]);
+          *reinterpret_cast<uint32_t*>(ap + sw128_off(r0, c0 + 8)) = f16x2_to_bf16x2(af[2]);
+          *reinterpret_cast<uint32_t*>(ap + sw128_off(r0 + 8, c0 + 8)) = f16x2_to_bf16x2(af[3]);
+        }
+        fence_proxy_async();  // these st.shared -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&G.raw_empty[g % RAW_ST]);
+          mbar_arrive(&G.a_ready[s]);
+        }
+      }
+      if (kb == KB - 1) {  // the tile's epilogue
+        const int ab = i & 1;
+        const bool ok = wait_ab(&G.acc_full[ab], (i / 2) & 1, abort, status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        const int r = q4 * 32 + lane;  // weight row within the m-tile
+        const uint32_t tacc = tmem + (uint32_t)(ab * NT) + ((uint32_t)(q4 * 32) << 16);
+        for (int c0 = cg * 32; c0 < cg * 32 + 32 && c0 < t.n; c0 += 16) {
+          uint32_t v[16];
+          tc_ld16(tacc + (uint32_t)c0, v);
+          if (MODE == ROUTER) {
+            const int e = t.mt * BM + r;
+            float* logits = ws_at<float>(a, a.W.logits);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[j]), 8);
-          if (gate && c0 + j < n) {
-            const float gv = __uint_as_float(v[j]) * Gg;
-            const float uv = up * Gu;
-            const float sv = gv / (1.0f + expf(-gv));
-            const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
-            hbuf[(size_t)(row0 + c0 + j) * a.I + i] = *reinterpret_cast<const uint16_t*>(&hb);
+            for (int j = 0; j < 16; ++j)
+              if (e < a.E && c0 + j < t.n) logits[(size_t)(t.row0 + c0 + j) * a.E + e] = __uint_as_float(v[j]);
+          } else if (MODE == GATEUP) {
+            // Rows 16 u .. 16 u + 7 of packed tile u are gate rows, the next 8 the
+            // up rows of the same intermediate indices 8 (8 mt + u) + r % 8.
+            const float Gg = a.globals[t.expert * 4 + 0], Gu = a.globals[t.expert * 4 + 1];
+            const bool gate = (lane & 8) == 0;
+            const int ii = (t.mt * 8 + q4 * 2 + (lane >> 4)) * 8 + (lane & 7);
+            uint16_t* hbuf = ws_at<uint16_t>(a, a.W.h);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[j]), 8);
+              if (gate && c0 + j < t.n) {
+                const float gv = __uint_as_float(v[j]) * Gg;
+                const float uv = up * Gu;
+                const float sv = gv / (1.0f + expf(-gv));
+                const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
+                hbuf[(size_t)(t.row0 + c0 + j) * a.I + ii] = *reinterpret_cast<const uint16_t*>(&hb);
+              }
+            }
+          } else {
+            const float Gd = a.globals[t.expert * 4 + 2];
+            float* y = ws_at<float>(a, a.W.y);
+            const int jrow = t.mt * BM + r;
+            const int q_per_tok = a.S + a.k;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int c = c0 + j, src = c - cg * 32;
+              const int tok = __shfl_sync(0xffffffffu, ctok, src);
+              const int qq = __shfl_sync(0xffffffffu, cq, src);
+              const float wv = __shfl_sync(0xffffffffu, cw, src);
+              if (c < t.n) y[((size_t)tok * q_per_tok + qq) * a.H + jrow] = wv * (__uint_as_float(v[j]) * Gd);
+            }
           }
         }
-      } else {
-        const float Gd = a.globals[expert * 4 + 2];
-        float* y = ws_at<float>(a, a.W.y);
-        const int jrow = mt * BM + r;
-        const int q_per_tok = a.S + a.k;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int c = c0 + j;
-          if (c < n)
-            y[((size_t)G.col_tok[c] * q_per_tok + G.col_q[c]) * a.H + jrow] =
-                G.col_w[c] * (__uint_as_float(v[j]) * Gd);
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&G.acc_empty[ab]);
       }
     }
-    tc_fence_before();
-    __syncthreads();  // tensor memory and the column tables are free for the next tile
-    tc_fence_after();
   }
 
-  if (failed) {  // let in-flight copies and MMAs land before the memory goes away
-    cp_async_wait<0>();
-    for (uint32_t g = (gk >= STAGES ? gk - STAGES : 0); g < gk; ++g) {
-      mbar_drain(&G.mma_done[g % STAGES], (g / STAGES) & 1);
-      if (MODE != ROUTER) mbar_drain(&G.raw_full[g % STAGES], (g / STAGES) & 1);
-    }
-  }
-  cp_async_wait<0>();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// Grouped activation rows of the routed (token, expert) pairs: row p of the
+// grouped matrix = x of the token of grouped row S B + p.
+__global__ void __launch_bounds__(256) k_pf_gather(PfArgs a) {
+  const int per_row = a.H / 8;  // 16-byte words
+  const size_t n = (size_t)a.B * a.k * per_row;
+  const int* list_tok = ws_at<const int>(a, a.W.list_tok) + (size_t)a.S * a.B;
+  uint4* dst = ws_at<uint4>(a, a.W.xg);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = i / per_row, wd = i % per_row;
+    const int tok = __ldcg(list_tok + row);
+    dst[i] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)tok * a.H) + wd);
   }
 }
 
@@ -674,8 +773,40 @@ static int sm_count() {
   return v;
 }
 
+// cuTensorMapEncodeTiled, reached through the runtime (no link against the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn tensor_map_encoder() {
+  static std::atomic<void*> fn{nullptr};
+  void* f = fn.load();
+  if (!f) {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return nullptr;
+    fn.store(f);
+  }
+  return reinterpret_cast<EncodeTiledFn>(f);
+}
+
+// bf16 matrix [rows][cols] (row stride cols * 2 bytes), boxes of 64 columns x
+// 128 rows written in the 128-byte swizzle; rows past the end read as zero.
+static bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  const EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc || rows == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)NT};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE>
-static cudaError_t launch_gemm(const PfArgs& a, int grid, cudaStream_t stream) {
+static cudaError_t launch_gemm(const PfArgs& a, const PfMaps& maps, int grid, cudaStream_t stream) {
   static std::atomic<int> attr_set{0};
   const size_t smem = gemm_dyn_smem();
   if (!attr_set.load()) {
@@ -683,7 +814,7 @@ static cudaError_t launch_gemm(const PfArgs& a, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set.store(1);
   }
-  k_pf_gemm<MODE><<<grid, THREADS, smem, stream>>>(a);
+  k_pf_gemm<MODE><<<grid, GEMM_THREADS, smem, stream>>>(a, maps);
   return cudaGetLastError();
 }
 
@@ -746,15 +877,29 @@ extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, cons
   a.out = out;
   if (ws_bytes < a.W.total) return FLINT_MOE_EINVAL;
 
+  // TMA descriptors of the three GEMMs (host-side encoding, passed by value).
+  PfMaps m_router, m_gateup, m_down;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  if (!encode_rows(&m_router.a, a.router, a.H, a.E) || !encode_rows(&m_router.b0, x, a.H, B) ||
+      !encode_rows(&m_gateup.b0, x, a.H, B) || !encode_rows(&m_gateup.b1, wsb + a.W.xg, a.H, (uint64_t)B * a.k) ||
+      !encode_rows(&m_down.b0, wsb + a.W.h, a.I, (uint64_t)a.W.max_rows))
+    return FLINT_MOE_ECUDA;
+  m_router.b1 = m_router.b0;
+  m_gateup.a = m_gateup.b0;
+  m_down.a = m_down.b1 = m_down.b0;
+
   const int nsm = sm_count();
   const int router_tiles = ((a.E + BM - 1) / BM) * ((B + NT - 1) / NT);
-  if (launch_gemm<ROUTER>(a, std::min(nsm, router_tiles), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
+  if (launch_gemm<ROUTER>(a, m_router, std::min(nsm, router_tiles), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
   k_pf_topk<<<(B + 7) / 8, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   k_pf_plan<<<1, PLAN_THREADS, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
-  if (launch_gemm<GATEUP>(a, std::min(nsm, a.W.max_gu), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
-  if (launch_gemm<DOWN>(a, std::min(nsm, a.W.max_dn), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
+  const int ggrid = (int)std::min<size_t>((size_t)nsm * 4, ((size_t)B * a.k * (a.H / 8) + 255) / 256);
+  k_pf_gather<<<ggrid, 256, 0, stream>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
+  if (launch_gemm<GATEUP>(a, m_gateup, std::min(nsm, a.W.max_gu), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
+  if (launch_gemm<DOWN>(a, m_down, std::min(nsm, a.W.max_dn), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
   const int cgrid = (int)std::min<size_t>((size_t)nsm * 8, ((size_t)B * a.H / 4 + 255) / 256);
   k_pf_combine<<<cgrid, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
