@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--dense-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--bf16-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--prefill-only", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--prefill-batches", default="", help=argparse.SUPPRESS)
+    p.add_argument("--prefill-layers", type=int, default=8, help=argparse.SUPPRESS)
     p.add_argument("--oracle-leg", type=int, default=0, help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -628,7 +630,10 @@ def gpu_arm(args) -> None:
 
     if args.prefill_only:
         if rank == 0:
-            print(json.dumps({"prefill": prefill_leg()}))
+            kw = {"n_layers": args.prefill_layers}
+            if args.prefill_batches:
+                kw["batches"] = tuple(int(b) for b in args.prefill_batches.split(","))
+            print(json.dumps({"prefill": prefill_leg(**kw)}))
         return
     if args.stack_only:
         if rank == 0:

@@ -31,11 +31,13 @@ namespace pf {
 constexpr int BM = 128;       // weight rows per tile (MMA M)
 constexpr int BK = 64;        // k per pipeline stage: one 128-byte swizzle row of bf16
 constexpr int NT = 128;       // tokens per tile at most (MMA N)
-constexpr int STAGES = 4;     // operand stages in shared memory
+constexpr int KPS = 2;        // k-blocks per operand stage (one handshake per stage)
+constexpr int STAGES = 2;     // operand stages in shared memory
 constexpr uint32_t TMEM_COLS = 2 * NT;  // N <= NT columns are used; the margin costs nothing at one CTA per SM
-constexpr int A_STAGE = BM * BK * 2;              // 16 KiB
-constexpr int B_STAGE = NT * BK * 2;              // 16 KiB
-constexpr int RAW_STAGE = (BM / 16) * KG_NVFP4;   // 4608 B: eight packed k-groups
+constexpr int A_KBLK = BM * BK * 2;               // 16 KiB: one k-block of the weight operand
+constexpr int B_KBLK = NT * BK * 2;               // 16 KiB: one k-block of the token operand
+constexpr int A_STAGE = KPS * A_KBLK;
+constexpr int B_STAGE = KPS * B_KBLK;
 constexpr int MAX_E = 512;
 
 enum Mode : int { ROUTER = 0, GATEUP = 1, DOWN = 2 };
@@ -44,7 +46,7 @@ enum : int { PF_STATUS = HDR_STATUS, PF_NSLOTS = 2, PF_NGU = 3, PF_NDN = 4 };
 // Workspace: header words, then 256-byte aligned regions sized for T tokens.
 struct PfLayout {
   size_t counts, logits, idx, w, pos, slot_expert, slot_row0, slot_count, list_tok, list_q, list_w, gu_tiles,
-      dn_tiles, xg, h, y, total;
+      dn_tiles, list_row, kx, x16, xg, h, y, total;
   int max_slots, max_rows, max_gu, max_dn;
 };
 
@@ -70,7 +72,10 @@ __host__ __device__ inline PfLayout make_pf_layout(int H, int E, int k, int I, i
   W.list_w = o;      o = ws_align(o + sizeof(float) * (size_t)W.max_rows);
   W.gu_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_gu);
   W.dn_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_dn);
-  W.xg = o;          o = ws_align(o + (size_t)2 * T * k * H);  // routed pairs' activation rows, grouped
+  W.list_row = o;    o = ws_align(o + sizeof(int) * (size_t)T * k);   // (token, rank) -> grouped routed row
+  W.kx = o;          o = ws_align(o + sizeof(int) * (size_t)T);       // per-token power-of-two prescale
+  W.x16 = o;         o = ws_align(o + (size_t)2 * T * H);             // x * 2^kx in f16
+  W.xg = o;          o = ws_align(o + (size_t)2 * T * k * H);         // the same rows grouped by routed expert
   W.h = o;           o = ws_align(o + (size_t)2 * W.max_rows * I);
   W.y = o;           o = ws_align(o + sizeof(float) * (size_t)W.max_rows * H);
   W.total = o;
@@ -116,11 +121,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16: D f32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits
-// 17-22, M >> 4 in bits 24-28.
-__device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16: D f32 (bits 4-5 = 1), A and B both
+// bf16 (bits 7-9 = 1, 10-12 = 1) or both f16 (0, 0), both K-major (bits 15,
+// 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__device__ __forceinline__ uint32_t idesc_f32acc(int M, int N, bool bf16) {
+  const uint32_t t = bf16 ? 1u : 0u;
+  return (1u << 4) | (t << 7) | (t << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -168,6 +174,12 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((c * 2) >> 4) ^ (r & 7)) << 4) + ((c * 2) & 15));
 }
 
+// bf16x2 -> f16x2 of the values times sc (a power of two).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc) {
+  const __half2 hv = __floats2half2_rn(bf16lo(w) * sc, bf16hi(w) * sc);
+  return *reinterpret_cast<const uint32_t*>(&hv);
+}
+
 // f16x2 holding two values exactly representable in bf16 -> bf16x2 (exact).
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
   const __half2 hv = *reinterpret_cast<const __half2*>(&h);
@@ -184,23 +196,26 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
 //
 // Warp roles, handing off through mbarriers only (no block-wide barrier in
 // the main loop):
-//   warp 16  streams the packed weight k-blocks (bulk copies) into a ring of
-//            RAW_ST slots, as far ahead as the ring allows, across tiles;
+//   warp 16  streams the packed weights into a ring of RAW_SL slots of RAW_KB
+//            k-blocks (lane p copies packed tile p's run of k-groups: few,
+//            large bulk copies), as far ahead as the ring allows, across tiles;
 //   warp 17  loads each k-block's 128 activation rows (and the router's
 //            weight rows) with TMA in the 128-byte swizzle into the stage;
 //   warp 18  issues the four MMAs of a k-block once both operands are in,
 //            commits them to the stage's mbarrier, and after a tile's last
 //            k-block to the accumulator buffer's mbarrier;
-//   warps 0-15 dequantise the packed k-block into the stage's bf16 operand
-//            (warp w: packed tile w % 8, k-steps 2 (w / 8) and 2 (w / 8) + 1)
-//            and run the epilogue of each tile from tensor memory. Two
+//   warps 0-15 dequantise the packed k-blocks into the stages' operands, two
+//            groups of 8 warps taking alternate k-blocks (warp w: packed tile
+//            w % 8), and run the epilogue of each tile from tensor memory. Two
 //            accumulator buffers (columns 0-127, 128-255) let the MMAs of the
 //            next tile start before the epilogue of this one has finished.
 // ---------------------------------------------------------------------------
 constexpr int CWARPS = 16;
 constexpr int W_RAW = 16, W_B = 17, W_MMA = 18;
 constexpr int GEMM_THREADS = 19 * 32;
-constexpr int RAW_ST = 12;  // packed weight k-blocks in flight
+constexpr int RAW_KB = 4;   // k-blocks of one packed weight slot (eight copies of RAW_KB k-groups)
+constexpr int RAW_SL = 4;   // slots in the ring: up to 16 k-blocks in flight
+constexpr int RAW_SLOT = (BM / 16) * RAW_KB * KG_NVFP4;  // 18 KiB
 
 struct PfMaps {  // TMA descriptors, bf16, 64-column x 128-row boxes, 128-byte swizzle
   CUtensorMap a;   // router rows (router GEMM)
@@ -209,8 +224,8 @@ struct PfMaps {  // TMA descriptors, bf16, 64-column x 128-row boxes, 128-byte s
 };
 
 struct GemmSmem {
-  uint64_t raw_full[RAW_ST];
-  uint64_t raw_empty[RAW_ST];
+  uint64_t raw_full[RAW_SL];
+  uint64_t raw_empty[RAW_SL];
   uint64_t b_full[STAGES];
   uint64_t a_ready[STAGES];
   uint64_t mma_done[STAGES];
@@ -221,11 +236,37 @@ struct GemmSmem {
 };
 
 constexpr size_t gemm_dyn_smem() {
-  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + (size_t)RAW_ST * RAW_STAGE;
+  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + (size_t)RAW_SL * RAW_SLOT;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// One lane of the (fully active) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 rx;\n\t.reg .pred px;\n\telect.sync rx|px, %1;\n\t@px mov.s32 %0, 1;\n\t}"
+      : "+r"(pred)
+      : "r"(0xffffffffu));
+  return pred != 0;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk copy global -> shared with an L2 cache policy, completing on bar.
+__device__ __forceinline__ void bulk_g2s_pol(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                             uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
 }
 
 // 2-D TMA tile load (box from the descriptor) into shared memory, completing on bar.
@@ -286,9 +327,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (smem_addr(dsmem) + 1023u) & ~1023u;
   uint8_t* const base_ptr = dsmem + (base - smem_addr(dsmem));
-  const uint32_t a_op = base;                                   // STAGES x 16 KiB
-  const uint32_t b_op = base + STAGES * A_STAGE;                // STAGES x 16 KiB
-  uint8_t* const raw = base_ptr + STAGES * (A_STAGE + B_STAGE);  // RAW_ST x 4608 B
+  const uint32_t a_op = base;                                   // STAGES x 32 KiB
+  const uint32_t b_op = base + STAGES * A_STAGE;                // STAGES x 32 KiB
+  uint8_t* const raw = base_ptr + STAGES * (A_STAGE + B_STAGE);  // RAW_SL x 18 KiB
   int* status = ws_at<int>(a, 0) + PF_STATUS;
   volatile int* abort = &G.abort;
 
@@ -299,16 +340,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   if ((int)blockIdx.x >= n_tiles) return;  // uniform: no tensor memory taken
   const int my_tiles = (n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   const int total = my_tiles * KB;  // k-blocks of this CTA
+  // Packed weights travel in slots of up to RAW_KB k-blocks of one tile: slot
+  // u of the CTA is slot u % SPT of tile u / SPT, k-blocks RAW_KB (u % SPT) ...
+  const int SPT = (KB + RAW_KB - 1) / RAW_KB;
+  const int n_slots = my_tiles * SPT;
+  // Operand stages hold KPS k-blocks: stage-block v is k-blocks KPS (v % SBT) .. of tile v / SBT.
+  const int SBT = (KB + KPS - 1) / KPS;
+  const int n_sb = my_tiles * SBT;
   auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RAW_ST; ++s) {
+    for (int s = 0; s < RAW_SL; ++s) {
       mbar_init(&G.raw_full[s], 1);
       mbar_init(&G.raw_empty[s], CWARPS);
     }
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&G.b_full[s], 1);
-      mbar_init(&G.a_ready[s], CWARPS);
+      mbar_init(&G.a_ready[s], CWARPS / 2);  // one group of 8 warps dequantises a k-block
       mbar_init(&G.mma_done[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -330,136 +378,180 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   const uint32_t tmem = G.tmem_base;
 
   if (warp == W_RAW) {
-    // ---------------- packed weight k-blocks -> raw ring ----------------
-    if (MODE != ROUTER && lane == 0) {
-      int q = 0;
+    // ---------------- packed weight k-blocks -> raw ring (lane p copies packed tile p) ----------------
+    if (MODE != ROUTER) {
+      const uint64_t pol = l2_evict_first_policy();
+      int u = 0;
       TileInfo nxt = tile_info<MODE>(a, tile_of(0));
-      const uint8_t* wbase = nullptr;
-      int64_t wtile = 0;
-      for (; q < total; ++q) {
-        const int slot = q % RAW_ST, i = q / KB, kb = q % KB;
-        if (q >= RAW_ST && !wait_ab(&G.raw_empty[slot], ((q / RAW_ST) - 1) & 1, abort, status)) break;
-        if (kb == 0) {
+      const uint8_t* wsrc = nullptr;  // this lane's packed tile
+      const int64_t wtile = MODE == GATEUP ? a.L.gu_tile : a.L.dn_tile;
+      for (; u < n_slots; ++u) {
+        const int sl = u % RAW_SL, i = u / SPT, kb0 = (u % SPT) * RAW_KB;
+        const int nk = min(RAW_KB, KB - kb0);
+        bool ok = u < RAW_SL || wait_ab(&G.raw_empty[sl], ((u / RAW_SL) - 1) & 1, abort, status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (kb0 == 0) {
           const TileInfo t = nxt;
           if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
-          const uint8_t* eb = a.packed + (int64_t)t.expert * a.L.expert_bytes;
-          wtile = MODE == GATEUP ? a.L.gu_tile : a.L.dn_tile;
-          wbase = eb + (MODE == GATEUP ? 0 : a.L.gu_bytes) + (int64_t)(t.mt * 8) * wtile;
+          wsrc = a.packed + (int64_t)t.expert * a.L.expert_bytes + (MODE == GATEUP ? 0 : a.L.gu_bytes) +
+                 (int64_t)(t.mt * 8 + (lane & 7)) * wtile;
         }
-        mbar_arrive_expect_tx(&G.raw_full[slot], (uint32_t)RAW_STAGE);
-        for (int p = 0; p < BM / 16; ++p)
-          bulk_g2s_stream(raw + slot * RAW_STAGE + p * KG_NVFP4, wbase + p * wtile + (int64_t)kb * KG_NVFP4,
-                          (uint32_t)KG_NVFP4, &G.raw_full[slot]);
+        if (lane == 0) mbar_arrive_expect_tx(&G.raw_full[sl], (uint32_t)((BM / 16) * nk * KG_NVFP4));
+        __syncwarp();
+        if (lane < BM / 16)
+          bulk_g2s_pol(smem_addr(raw + sl * RAW_SLOT + lane * RAW_KB * KG_NVFP4), wsrc + (int64_t)kb0 * KG_NVFP4,
+                       (uint32_t)(nk * KG_NVFP4), &G.raw_full[sl], pol);
       }
       // The CTA's memory must outlive every copy this warp started.
-      for (int r = (q > RAW_ST ? q - RAW_ST : 0); r < q; ++r) mbar_drain(&G.raw_full[r % RAW_ST], (r / RAW_ST) & 1);
+      if (lane == 0)
+        for (int r = (u > RAW_SL ? u - RAW_SL : 0); r < u; ++r) mbar_drain(&G.raw_full[r % RAW_SL], (r / RAW_SL) & 1);
     }
   } else if (warp == W_B) {
     // ---------------- activation (and router weight) k-blocks -> stages, TMA ----------------
     if (lane == 0) {
-      int q = 0;
+      int v = 0;
       TileInfo nxt = tile_info<MODE>(a, tile_of(0)), t = nxt;
-      for (; q < total; ++q) {
-        const int s = q % STAGES, i = q / KB, kb = q % KB;
-        if (q >= STAGES && !wait_ab(&G.mma_done[s], ((q / STAGES) - 1) & 1, abort, status)) break;
-        if (kb == 0) {
+      for (; v < n_sb; ++v) {
+        const int s = v % STAGES, i = v / SBT, kb0 = (v % SBT) * KPS, nkv = min(KPS, KB - kb0);
+        if (v >= STAGES && !wait_ab(&G.mma_done[s], ((v / STAGES) - 1) & 1, abort, status)) break;
+        if (kb0 == 0) {
           t = nxt;
           if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
         }
-        mbar_arrive_expect_tx(&G.b_full[s], (uint32_t)(MODE == ROUTER ? A_STAGE + B_STAGE : B_STAGE));
-        if (MODE == ROUTER) {
-          tma_load_2d(a_op + s * A_STAGE, &maps.a, kb * BK, t.mt * BM, &G.b_full[s]);
-          tma_load_2d(b_op + s * B_STAGE, &maps.b0, kb * BK, t.row0, &G.b_full[s]);
-        } else if (MODE == GATEUP) {
-          if (t.slot < a.S)  // a shared expert's rows are the tokens in order
-            tma_load_2d(b_op + s * B_STAGE, &maps.b0, kb * BK, t.row0 - t.slot * a.B, &G.b_full[s]);
-          else
-            tma_load_2d(b_op + s * B_STAGE, &maps.b1, kb * BK, t.row0 - a.S * a.B, &G.b_full[s]);
-        } else {
-          tma_load_2d(b_op + s * B_STAGE, &maps.b0, kb * BK, t.row0, &G.b_full[s]);
+        mbar_arrive_expect_tx(&G.b_full[s], (uint32_t)(nkv * (MODE == ROUTER ? A_KBLK + B_KBLK : B_KBLK)));
+        for (int j = 0; j < nkv; ++j) {
+          const int x = (kb0 + j) * BK;
+          const uint32_t bdst = b_op + s * B_STAGE + j * B_KBLK;
+          if (MODE == ROUTER) {
+            tma_load_2d(a_op + s * A_STAGE + j * A_KBLK, &maps.a, x, t.mt * BM, &G.b_full[s]);
+            tma_load_2d(bdst, &maps.b0, x, t.row0, &G.b_full[s]);
+          } else if (MODE == GATEUP) {
+            if (t.slot < a.S)  // a shared expert's rows are the tokens in order
+              tma_load_2d(bdst, &maps.b0, x, t.row0 - t.slot * a.B, &G.b_full[s]);
+            else
+              tma_load_2d(bdst, &maps.b1, x, t.row0 - a.S * a.B, &G.b_full[s]);
+          } else {
+            tma_load_2d(bdst, &maps.b0, x, t.row0, &G.b_full[s]);
+          }
         }
       }
-      for (int r = (q > STAGES ? q - STAGES : 0); r < q; ++r) mbar_drain(&G.b_full[r % STAGES], (r / STAGES) & 1);
+      for (int r = (v > STAGES ? v - STAGES : 0); r < v; ++r) mbar_drain(&G.b_full[r % STAGES], (r / STAGES) & 1);
     }
   } else if (warp == W_MMA) {
-    // ---------------- tensor-core issue ----------------
-    if (lane == 0) {
-      int g = 0;
-      TileInfo nxt = tile_info<MODE>(a, tile_of(0));
-      uint32_t idesc = 0, acc = tmem;
-      for (; g < total; ++g) {
-        const int s = g % STAGES, i = g / KB, kb = g % KB;
-        if (kb == 0) {
-          const TileInfo t = nxt;
-          if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
-          idesc = idesc_bf16_f32(BM, (t.n + 15) & ~15);
-          acc = tmem + (uint32_t)((i & 1) * NT);
-          if (i >= 2 && !wait_ab(&G.acc_empty[i & 1], ((i / 2) - 1) & 1, abort, status)) break;
-        }
-        if (!wait_ab(&G.b_full[s], (g / STAGES) & 1, abort, status)) break;
-        if (MODE != ROUTER && !wait_ab(&G.a_ready[s], (g / STAGES) & 1, abort, status)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < BK / 16; ++ks)
-          tc_mma(acc, sw128_desc(a_op + s * A_STAGE + ks * 32), sw128_desc(b_op + s * B_STAGE + ks * 32), idesc,
-                 (kb > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(&G.mma_done[s]);
-        if (kb == KB - 1) tc_commit(&G.acc_full[i & 1]);
+    // ---------------- tensor-core issue (one elected lane) ----------------
+    int v = 0;
+    TileInfo nxt = tile_info<MODE>(a, tile_of(0));
+    uint32_t idesc = 0, acc = tmem;
+    const uint64_t adesc0 = sw128_desc(a_op), bdesc0 = sw128_desc(b_op);
+    for (; v < n_sb; ++v) {
+      const int s = v % STAGES, i = v / SBT, kb0 = (v % SBT) * KPS, nkv = min(KPS, KB - kb0);
+      bool ok = true;
+      if (kb0 == 0) {
+        const TileInfo t = nxt;
+        if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
+        idesc = idesc_f32acc(BM, (t.n + 15) & ~15, MODE != GATEUP);  // gate/up runs in f16
+        acc = tmem + (uint32_t)((i & 1) * NT);
+        ok = i < 2 || wait_ab(&G.acc_empty[i & 1], ((i / 2) - 1) & 1, abort, status);
       }
-      // Let the MMAs in flight finish before the memory goes away.
-      for (int r = (g > STAGES ? g - STAGES : 0); r < g; ++r) mbar_drain(&G.mma_done[r % STAGES], (r / STAGES) & 1);
+      ok = ok && wait_ab(&G.b_full[s], (v / STAGES) & 1, abort, status);
+      ok = ok && (MODE == ROUTER || wait_ab(&G.a_ready[s], (v / STAGES) & 1, abort, status));
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      // Descriptor start addresses advance by the stage, the k-block (16 KiB) and the k-step (32 B).
+      const uint64_t ad = adesc0 + (uint64_t)((s * A_STAGE) >> 4), bd = bdesc0 + (uint64_t)((s * B_STAGE) >> 4);
+      if (elect_one()) {
+        for (int j = 0; j < nkv; ++j)
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)
+            tc_mma(acc, ad + (uint64_t)((j * A_KBLK) >> 4) + 2 * ks, bd + (uint64_t)((j * B_KBLK) >> 4) + 2 * ks, idesc,
+                   (kb0 + j > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(&G.mma_done[s]);
+        if (kb0 + nkv == KB) tc_commit(&G.acc_full[i & 1]);
+      }
+      __syncwarp();
     }
+    // Let the MMAs in flight finish before the memory goes away.
+    if (lane == 0)
+      for (int r = (v > STAGES ? v - STAGES : 0); r < v; ++r) mbar_drain(&G.mma_done[r % STAGES], (r / STAGES) & 1);
   } else {
     // ---------------- consumers: dequantise, epilogue ----------------
+    // Two groups of 8 warps take alternate k-blocks of each weight slot; warp
+    // w dequantises packed tile w % 8 (all four k-steps) of its group's
+    // k-blocks. Every consumer warp frees the slot once, after its k-blocks.
     TileInfo nxt = tile_info<MODE>(a, tile_of(0)), t = nxt;
+    const int gid = warp >> 3, dq_p = warp & 7, dq_g = lane >> 2, dq_t = lane & 3;
     const int q4 = warp & 3, cg = warp >> 2;  // epilogue: lanes 32 q4.., columns 32 cg..
+    uint32_t doff[4][4];  // this lane's swizzled 4-byte destinations in a stage
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const int r0 = dq_p * 16 + dq_g, c0 = ks * 16 + 2 * dq_t;
+      doff[ks][0] = sw128_off(r0, c0);
+      doff[ks][1] = sw128_off(r0 + 8, c0);
+      doff[ks][2] = sw128_off(r0, c0 + 8);
+      doff[ks][3] = sw128_off(r0 + 8, c0 + 8);
+    }
+    const uint32_t tile_off = (uint32_t)(dq_p * RAW_KB * KG_NVFP4);
     int ctok = 0, cq = 0;
-    float cw = 0.f;
-    for (int g = 0; g < total; ++g) {
-      const int s = g % STAGES, i = g / KB, kb = g % KB;
-      if (kb == 0) {
+    float cw = 0.f, cinv = 1.f;
+    bool failed = false;
+    for (int u = 0; u < n_slots && !failed; ++u) {
+      const int i = u / SPT, kb0 = (u % SPT) * RAW_KB, nk = min(RAW_KB, KB - kb0);
+      if (kb0 == 0) {
         t = nxt;
         if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
-        if (MODE == DOWN && cg * 32 + lane < t.n) {  // this lane's epilogue column
-          const int row = t.row0 + cg * 32 + lane;
+        const int c = cg * 32 + lane;  // this lane's epilogue column
+        if (MODE == GATEUP && c < t.n) {  // 2^-kx of its token
+          const int tok = t.slot < a.S ? t.row0 - t.slot * a.B + c : __ldcg(ws_at<const int>(a, a.W.list_tok) + t.row0 + c);
+          cinv = exp2i(-__ldcg(ws_at<const int>(a, a.W.kx) + tok));
+        }
+        if (MODE == DOWN && c < t.n) {
+          const int row = t.row0 + c;
           ctok = __ldcg(ws_at<const int>(a, a.W.list_tok) + row);
           cq = __ldcg(ws_at<const int>(a, a.W.list_q) + row);
           cw = __ldcg(ws_at<const float>(a, a.W.list_w) + row);
         }
       }
       if (MODE != ROUTER) {
-        bool ok = g < STAGES || wait_ab(&G.mma_done[s], ((g / STAGES) - 1) & 1, abort, status);
-        ok = ok && wait_ab(&G.raw_full[g % RAW_ST], (g / RAW_ST) & 1, abort, status);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const int p = warp & 7, hs = warp >> 3;
-        const uint8_t* kp = raw + (g % RAW_ST) * RAW_STAGE + p * KG_NVFP4;
-        uint2 codes;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(codes.x), "=r"(codes.y)
-                     : "r"(smem_addr(kp + lane * 16 + hs * 8)));
-        const int gr = lane >> 2, t4 = lane & 3;
-        const uint32_t sg = lds32(kp + KG_CODE_BYTES + gr * 4);
-        const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (gr + 8) * 4);
-        uint8_t* ap = base_ptr + s * A_STAGE;
-        const int r0 = p * 16 + gr;
+        const uint8_t* slot_p = raw + (u % RAW_SL) * RAW_SLOT + tile_off;
+        // Stage-block sb = gid of the slot: k-blocks 2 gid, 2 gid + 1 of the slot.
+        const int nsb = (nk + KPS - 1) / KPS;
+        bool ok = gid >= nsb || wait_ab(&G.raw_full[u % RAW_SL], (u / RAW_SL) & 1, abort, status);
+        if (gid < nsb) {
+          const int v = i * SBT + kb0 / KPS + gid, s = v % STAGES;
+          const int nkv = min(KPS, nk - gid * KPS);
+          ok = ok && (v < STAGES || wait_ab(&G.mma_done[s], ((v / STAGES) - 1) & 1, abort, status));
+          if (__all_sync(0xffffffffu, ok)) {
+            for (int j = 0; j < nkv; ++j) {
+              const uint8_t* kp = slot_p + (gid * KPS + j) * KG_NVFP4;
+              const uint4 codes = lds128(kp + lane * 16);
+              const uint32_t sg = lds32(kp + KG_CODE_BYTES + dq_g * 4);
+              const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (dq_g + 8) * 4);
+              const uint32_t cw4[4] = {codes.x, codes.y, codes.z, codes.w};
+              const uint32_t ap = a_op + s * A_STAGE + j * A_KBLK;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int ks = 2 * hs + h;
-          uint32_t af[4];
-          nvfp4_afrag(h ? codes.y : codes.x, sg, sg8, ks, af);
-          const int c0 = ks * 16 + 2 * t4;
-          *reinterpret_cast<uint32_t*>(ap + sw128_off(r0, c0)) = f16x2_to_bf16x2(af[0]);
-          *reinterpret_cast<uint32_t*>(ap + sw128_off(r0 + 8, c0)) = f16x2_to_bf16x2(af[1]);
-          *reinterpret_cast<uint32_t*>(ap + sw128_off(r0, c0 + 8)) = f16x2_to_bf16x2(af[2]);
-          *reinterpret_cast<uint32_t*>(ap + sw128_off(r0 + 8, c0 + 8)) = f16x2_to_bf16x2(af[3]);
+              for (int ks = 0; ks < 4; ++ks) {
+                uint32_t af[4];
+                nvfp4_afrag(cw4[ks], sg, sg8, ks, af);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  asm volatile("st.shared.u32 [%0], %1;" ::"r"(ap + doff[ks][q]),
+                               "r"(MODE == GATEUP ? af[q] : f16x2_to_bf16x2(af[q]))
+                               : "memory");
+              }
+            }
+            fence_proxy_async();  // these st.shared -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&G.a_ready[s]);
+          }
         }
-        fence_proxy_async();  // these st.shared -> visible to the tensor core
+        if (failed || !__all_sync(0xffffffffu, ok)) {
+          failed = true;
+          break;
+        }
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&G.raw_empty[g % RAW_ST]);
-          mbar_arrive(&G.a_ready[s]);
-        }
+        if (lane == 0) mbar_arrive(&G.raw_empty[u % RAW_SL]);  // this warp is done with the slot
       }
-      if (kb == KB - 1) {  // the tile's epilogue
+      if (kb0 + nk == KB) {  // the tile's epilogue
         const int ab = i & 1;
         const bool ok = wait_ab(&G.acc_full[ab], (i / 2) & 1, abort, status);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -477,20 +569,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
               if (e < a.E && c0 + j < t.n) logits[(size_t)(t.row0 + c0 + j) * a.E + e] = __uint_as_float(v[j]);
           } else if (MODE == GATEUP) {
             // Rows 16 u .. 16 u + 7 of packed tile u are gate rows, the next 8 the
-            // up rows of the same intermediate indices 8 (8 mt + u) + r % 8.
+            // up rows of the same intermediate indices 8 (8 mt + u) + r % 8: lane
+            // L and lane L ^ 8 hold (gate, up) of one index. The gate lane
+            // finishes the even columns, the up lane the odd ones.
             const float Gg = a.globals[t.expert * 4 + 0], Gu = a.globals[t.expert * 4 + 1];
             const bool gate = (lane & 8) == 0;
             const int ii = (t.mt * 8 + q4 * 2 + (lane >> 4)) * 8 + (lane & 7);
             uint16_t* hbuf = ws_at<uint16_t>(a, a.W.h);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[j]), 8);
-              if (gate && c0 + j < t.n) {
-                const float gv = __uint_as_float(v[j]) * Gg;
-                const float uv = up * Gu;
-                const float sv = gv / (1.0f + expf(-gv));
+            for (int j = 0; j < 16; j += 2) {
+              const float v0 = __uint_as_float(v[j]), v1 = __uint_as_float(v[j + 1]);
+              const float mine = gate ? v0 : v1;
+              const float other = __shfl_xor_sync(0xffffffffu, gate ? v1 : v0, 8);
+              const int c = c0 + j + (gate ? 0 : 1);
+              const float inv = __shfl_sync(0xffffffffu, cinv, c - cg * 32);
+              const float gv = (gate ? mine : other) * inv * Gg;
+              const float uv = (gate ? other : mine) * inv * Gu;
+              const float sv = __fdividef(gv, 1.0f + __expf(-gv));
+              if (c < t.n) {
                 const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
-                hbuf[(size_t)(t.row0 + c0 + j) * a.I + ii] = *reinterpret_cast<const uint16_t*>(&hb);
+                hbuf[(size_t)(t.row0 + c) * a.I + ii] = *reinterpret_cast<const uint16_t*>(&hb);
               }
             }
           } else {
@@ -523,17 +621,44 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   }
 }
 
-// Grouped activation rows of the routed (token, expert) pairs: row p of the
-// grouped matrix = x of the token of grouped row S B + p.
-__global__ void __launch_bounds__(256) k_pf_gather(PfArgs a) {
-  const int per_row = a.H / 8;  // 16-byte words
-  const size_t n = (size_t)a.B * a.k * per_row;
-  const int* list_tok = ws_at<const int>(a, a.W.list_tok) + (size_t)a.S * a.B;
-  uint4* dst = ws_at<uint4>(a, a.W.xg);
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t row = i / per_row, wd = i % per_row;
-    const int tok = __ldcg(list_tok + row);
-    dst[i] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)tok * a.H) + wd);
+// Gate/up activations in f16 for the tensor cores: per token a power of two
+// 2^kx maps the row's largest |x| into [2^14, 2^15), so every bf16 value is
+// exact in f16 (down to 2^-24 of that bound, below which the tail flushes;
+// the epilogue multiplies by 2^-kx). One block per token writes its row of x16
+// and its copies at the grouped rows of its k routed (token, expert) pairs.
+__global__ void __launch_bounds__(256) k_pf_x16(PfArgs a) {
+  __shared__ float red[8];
+  const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H);
+  const int nw = a.H / 8;
+  float m = 0.f;
+  for (int i = threadIdx.x; i < nw; i += blockDim.x) {
+    const uint4 v = __ldg(src + i);
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(w4[j])), fabsf(bf16hi(w4[j]))));
+  }
+  m = warp_max(m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+  const int kx = prescale_exp(m);
+  const float sc = exp2i(kx);
+  if (threadIdx.x == 0) ws_at<int>(a, a.W.kx)[t] = kx;
+  int rows[MAX_TOPK];
+  for (int j = 0; j < a.k; ++j) rows[j] = __ldcg(ws_at<const int>(a, a.W.list_row) + (size_t)t * a.k + j);
+  uint4* x16 = ws_at<uint4>(a, a.W.x16) + (size_t)t * nw;
+  uint4* xg = ws_at<uint4>(a, a.W.xg);
+  for (int i = threadIdx.x; i < nw; i += blockDim.x) {
+    const uint4 v = __ldg(src + i);
+    uint4 o;
+    o.x = bf16x2_to_f16x2_scaled(v.x, sc);
+    o.y = bf16x2_to_f16x2_scaled(v.y, sc);
+    o.z = bf16x2_to_f16x2_scaled(v.z, sc);
+    o.w = bf16x2_to_f16x2_scaled(v.w, sc);
+    x16[i] = o;
+    for (int j = 0; j < a.k; ++j) xg[(size_t)rows[j] * nw + i] = o;
   }
 }
 
@@ -709,6 +834,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_pf_plan(PfArgs a) {
     list_tok[row] = p / a.k;
     list_q[row] = a.S + p % a.k;
     list_w[row] = __ldcg(w + p);
+    ws_at<int>(a, a.W.list_row)[p] = row - a.S * a.B;
   }
   if (e < a.E) counts[e] = 0;  // ready for the next call (every read of counts is above)
 }
@@ -793,14 +919,14 @@ static EncodeTiledFn tensor_map_encoder() {
 
 // bf16 matrix [rows][cols] (row stride cols * 2 bytes), boxes of 64 columns x
 // 128 rows written in the 128-byte swizzle; rows past the end read as zero.
-static bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+static bool encode_rows(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, bool f16 = false) {
   const EncodeTiledFn enc = tensor_map_encoder();
   if (!enc || rows == 0) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
   const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)NT};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -881,7 +1007,8 @@ extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, cons
   PfMaps m_router, m_gateup, m_down;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   if (!encode_rows(&m_router.a, a.router, a.H, a.E) || !encode_rows(&m_router.b0, x, a.H, B) ||
-      !encode_rows(&m_gateup.b0, x, a.H, B) || !encode_rows(&m_gateup.b1, wsb + a.W.xg, a.H, (uint64_t)B * a.k) ||
+      !encode_rows(&m_gateup.b0, wsb + a.W.x16, a.H, B, true) ||
+      !encode_rows(&m_gateup.b1, wsb + a.W.xg, a.H, (uint64_t)B * a.k, true) ||
       !encode_rows(&m_down.b0, wsb + a.W.h, a.I, (uint64_t)a.W.max_rows))
     return FLINT_MOE_ECUDA;
   m_router.b1 = m_router.b0;
@@ -895,8 +1022,7 @@ extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, cons
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   k_pf_plan<<<1, PLAN_THREADS, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
-  const int ggrid = (int)std::min<size_t>((size_t)nsm * 4, ((size_t)B * a.k * (a.H / 8) + 255) / 256);
-  k_pf_gather<<<ggrid, 256, 0, stream>>>(a);
+  k_pf_x16<<<B, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   if (launch_gemm<GATEUP>(a, m_gateup, std::min(nsm, a.W.max_gu), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
   if (launch_gemm<DOWN>(a, m_down, std::min(nsm, a.W.max_dn), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
