@@ -46,7 +46,7 @@ enum : int { PF_STATUS = HDR_STATUS, PF_NSLOTS = 2, PF_NGU = 3, PF_NDN = 4 };
 // Workspace: header words, then 256-byte aligned regions sized for T tokens.
 struct PfLayout {
   size_t counts, logits, idx, w, pos, slot_expert, slot_row0, slot_count, list_tok, list_q, list_w, gu_tiles,
-      dn_tiles, list_row, kx, x16, xg, h, y, total;
+      dn_tiles, rowbase, kx, x16, xg, h, y, total;
   int max_slots, max_rows, max_gu, max_dn;
 };
 
@@ -72,7 +72,7 @@ __host__ __device__ inline PfLayout make_pf_layout(int H, int E, int k, int I, i
   W.list_w = o;      o = ws_align(o + sizeof(float) * (size_t)W.max_rows);
   W.gu_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_gu);
   W.dn_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_dn);
-  W.list_row = o;    o = ws_align(o + sizeof(int) * (size_t)T * k);   // (token, rank) -> grouped routed row
+  W.rowbase = o;     o = ws_align(o + sizeof(int) * E);                // first grouped row of each routed expert
   W.kx = o;          o = ws_align(o + sizeof(int) * (size_t)T);       // per-token power-of-two prescale
   W.x16 = o;         o = ws_align(o + (size_t)2 * T * H);             // x * 2^kx in f16
   W.xg = o;          o = ws_align(o + (size_t)2 * T * k * H);         // the same rows grouped by routed expert
@@ -226,8 +226,7 @@ struct PfMaps {  // TMA descriptors, bf16, 64-column x 128-row boxes, 128-byte s
 struct GemmSmem {
   uint64_t raw_full[RAW_SL];
   uint64_t raw_empty[RAW_SL];
-  uint64_t b_full[STAGES];
-  uint64_t a_ready[STAGES];
+  uint64_t full[STAGES];      // the stage's token rows landed (TMA) and its weights are dequantised
   uint64_t mma_done[STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
@@ -355,8 +354,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
       mbar_init(&G.raw_empty[s], CWARPS);
     }
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&G.b_full[s], 1);
-      mbar_init(&G.a_ready[s], CWARPS / 2);  // one group of 8 warps dequantises a k-block
+      // the TMA warp's expect-tx arrival, plus one arrival per warp of the
+      // dequantising group (8 warps) when the weights come from the raw ring
+      mbar_init(&G.full[s], MODE == ROUTER ? 1 : 1 + CWARPS / 2);
       mbar_init(&G.mma_done[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -418,33 +418,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
           t = nxt;
           if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
         }
-        mbar_arrive_expect_tx(&G.b_full[s], (uint32_t)(nkv * (MODE == ROUTER ? A_KBLK + B_KBLK : B_KBLK)));
+        mbar_arrive_expect_tx(&G.full[s], (uint32_t)(nkv * (MODE == ROUTER ? A_KBLK + B_KBLK : B_KBLK)));
         for (int j = 0; j < nkv; ++j) {
           const int x = (kb0 + j) * BK;
           const uint32_t bdst = b_op + s * B_STAGE + j * B_KBLK;
           if (MODE == ROUTER) {
-            tma_load_2d(a_op + s * A_STAGE + j * A_KBLK, &maps.a, x, t.mt * BM, &G.b_full[s]);
-            tma_load_2d(bdst, &maps.b0, x, t.row0, &G.b_full[s]);
+            tma_load_2d(a_op + s * A_STAGE + j * A_KBLK, &maps.a, x, t.mt * BM, &G.full[s]);
+            tma_load_2d(bdst, &maps.b0, x, t.row0, &G.full[s]);
           } else if (MODE == GATEUP) {
             if (t.slot < a.S)  // a shared expert's rows are the tokens in order
-              tma_load_2d(bdst, &maps.b0, x, t.row0 - t.slot * a.B, &G.b_full[s]);
+              tma_load_2d(bdst, &maps.b0, x, t.row0 - t.slot * a.B, &G.full[s]);
             else
-              tma_load_2d(bdst, &maps.b1, x, t.row0 - a.S * a.B, &G.b_full[s]);
+              tma_load_2d(bdst, &maps.b1, x, t.row0 - a.S * a.B, &G.full[s]);
           } else {
-            tma_load_2d(bdst, &maps.b0, x, t.row0, &G.b_full[s]);
+            tma_load_2d(bdst, &maps.b0, x, t.row0, &G.full[s]);
           }
         }
       }
-      for (int r = (v > STAGES ? v - STAGES : 0); r < v; ++r) mbar_drain(&G.b_full[r % STAGES], (r / STAGES) & 1);
+      for (int r = (v > STAGES ? v - STAGES : 0); r < v; ++r) mbar_drain(&G.full[r % STAGES], (r / STAGES) & 1);
     }
   } else if (warp == W_MMA) {
     // ---------------- tensor-core issue (one elected lane) ----------------
     int v = 0;
     TileInfo nxt = tile_info<MODE>(a, tile_of(0));
     uint32_t idesc = 0, acc = tmem;
-    const uint64_t adesc0 = sw128_desc(a_op), bdesc0 = sw128_desc(b_op);
+    // Descriptors of stage 0 and 1; k-block j and k-step ks add (j 16 KiB + ks 32 B) >> 4.
+    const uint64_t ad0 = sw128_desc(a_op), ad1 = sw128_desc(a_op + A_STAGE);
+    const uint64_t bd0 = sw128_desc(b_op), bd1 = sw128_desc(b_op + B_STAGE);
+    int s = 0, phase = 0, i = 0, kb0 = 0;  // stage, its phase parity, tile, first k-block of the stage-block
     for (; v < n_sb; ++v) {
-      const int s = v % STAGES, i = v / SBT, kb0 = (v % SBT) * KPS, nkv = min(KPS, KB - kb0);
+      const int nkv = min(KPS, KB - kb0);
       bool ok = true;
       if (kb0 == 0) {
         const TileInfo t = nxt;
@@ -453,22 +456,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
         acc = tmem + (uint32_t)((i & 1) * NT);
         ok = i < 2 || wait_ab(&G.acc_empty[i & 1], ((i / 2) - 1) & 1, abort, status);
       }
-      ok = ok && wait_ab(&G.b_full[s], (v / STAGES) & 1, abort, status);
-      ok = ok && (MODE == ROUTER || wait_ab(&G.a_ready[s], (v / STAGES) & 1, abort, status));
+      ok = ok && wait_ab(&G.full[s], (uint32_t)phase, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      // Descriptor start addresses advance by the stage, the k-block (16 KiB) and the k-step (32 B).
-      const uint64_t ad = adesc0 + (uint64_t)((s * A_STAGE) >> 4), bd = bdesc0 + (uint64_t)((s * B_STAGE) >> 4);
+      const uint64_t ad = s ? ad1 : ad0, bd = s ? bd1 : bd0;
       if (elect_one()) {
-        for (int j = 0; j < nkv; ++j)
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks)
-            tc_mma(acc, ad + (uint64_t)((j * A_KBLK) >> 4) + 2 * ks, bd + (uint64_t)((j * B_KBLK) >> 4) + 2 * ks, idesc,
-                   (kb0 + j > 0 || ks > 0) ? 1u : 0u);
+        for (int j = 0; j < KPS; ++j)
+          if (j < nkv) {
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks)
+              tc_mma(acc, ad + (uint64_t)((j * A_KBLK + ks * 32) >> 4), bd + (uint64_t)((j * B_KBLK + ks * 32) >> 4),
+                     idesc, (kb0 + j > 0 || ks > 0) ? 1u : 0u);
+          }
         tc_commit(&G.mma_done[s]);
         if (kb0 + nkv == KB) tc_commit(&G.acc_full[i & 1]);
       }
       __syncwarp();
+      kb0 += KPS;
+      if (kb0 >= KB) {
+        kb0 = 0;
+        ++i;
+      }
+      if (++s == STAGES) {
+        s = 0;
+        phase ^= 1;
+      }
     }
     // Let the MMAs in flight finish before the memory goes away.
     if (lane == 0)
@@ -521,27 +534,35 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
           const int nkv = min(KPS, nk - gid * KPS);
           ok = ok && (v < STAGES || wait_ab(&G.mma_done[s], ((v / STAGES) - 1) & 1, abort, status));
           if (__all_sync(0xffffffffu, ok)) {
-            for (int j = 0; j < nkv; ++j) {
-              const uint8_t* kp = slot_p + (gid * KPS + j) * KG_NVFP4;
-              const uint4 codes = lds128(kp + lane * 16);
-              const uint32_t sg = lds32(kp + KG_CODE_BYTES + dq_g * 4);
-              const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (dq_g + 8) * 4);
-              const uint32_t cw4[4] = {codes.x, codes.y, codes.z, codes.w};
-              const uint32_t ap = a_op + s * A_STAGE + j * A_KBLK;
+            uint4 codes[KPS];
+            uint32_t sg[KPS], sg8[KPS];
 #pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                uint32_t af[4];
-                nvfp4_afrag(cw4[ks], sg, sg8, ks, af);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  asm volatile("st.shared.u32 [%0], %1;" ::"r"(ap + doff[ks][q]),
-                               "r"(MODE == GATEUP ? af[q] : f16x2_to_bf16x2(af[q]))
-                               : "memory");
+            for (int j = 0; j < KPS; ++j)
+              if (j < nkv) {
+                const uint8_t* kp = slot_p + (gid * KPS + j) * KG_NVFP4;
+                codes[j] = lds128(kp + lane * 16);
+                sg[j] = lds32(kp + KG_CODE_BYTES + dq_g * 4);
+                sg8[j] = lds32(kp + KG_CODE_BYTES + (dq_g + 8) * 4);
               }
-            }
+#pragma unroll
+            for (int j = 0; j < KPS; ++j)
+              if (j < nkv) {
+                const uint32_t cw4[4] = {codes[j].x, codes[j].y, codes[j].z, codes[j].w};
+                const uint32_t ap = a_op + s * A_STAGE + j * A_KBLK;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                  uint32_t af[4];
+                  nvfp4_afrag(cw4[ks], sg[j], sg8[j], ks, af);
+#pragma unroll
+                  for (int q = 0; q < 4; ++q)
+                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(ap + doff[ks][q]),
+                                 "r"(MODE == GATEUP ? af[q] : f16x2_to_bf16x2(af[q]))
+                                 : "memory");
+                }
+              }
             fence_proxy_async();  // these st.shared -> visible to the tensor core
             __syncwarp();
-            if (lane == 0) mbar_arrive(&G.a_ready[s]);
+            if (lane == 0) mbar_arrive(&G.full[s]);
           }
         }
         if (failed || !__all_sync(0xffffffffu, ok)) {
@@ -621,12 +642,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   }
 }
 
-// Gate/up activations in f16 for the tensor cores: per token a power of two
-// 2^kx maps the row's largest |x| into [2^14, 2^15), so every bf16 value is
-// exact in f16 (down to 2^-24 of that bound, below which the tail flushes;
-// the epilogue multiplies by 2^-kx). One block per token writes its row of x16
-// and its copies at the grouped rows of its k routed (token, expert) pairs.
-__global__ void __launch_bounds__(256) k_pf_x16(PfArgs a) {
+// One block per token, after the plan: the token's entries of the grouped
+// row lists (token, slot rank, routing weight), and its gate/up activations in
+// f16 for the tensor cores: a power of two 2^kx maps the row's largest |x|
+// into [2^14, 2^15), so every bf16 value is exact in f16 (down to 2^-24 of
+// that bound, below which the tail flushes; the epilogue multiplies by
+// 2^-kx). The row goes to x16 and to the grouped rows of its k routed pairs.
+__global__ void __launch_bounds__(256) k_pf_token_rows(PfArgs a) {
   __shared__ float red[8];
   const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H);
@@ -646,8 +668,29 @@ __global__ void __launch_bounds__(256) k_pf_x16(PfArgs a) {
   const int kx = prescale_exp(m);
   const float sc = exp2i(kx);
   if (threadIdx.x == 0) ws_at<int>(a, a.W.kx)[t] = kx;
+  // This token's entries of the grouped lists: its S shared rows s B + t and
+  // its k routed rows rowbase[e_j] + pos_j (the token's place in expert e_j's list).
   int rows[MAX_TOPK];
-  for (int j = 0; j < a.k; ++j) rows[j] = __ldcg(ws_at<const int>(a, a.W.list_row) + (size_t)t * a.k + j);
+  for (int j = 0; j < a.k; ++j) {
+    const size_t p = (size_t)t * a.k + j;
+    const int e = __ldcg(ws_at<const int>(a, a.W.idx) + p);
+    rows[j] = __ldcg(ws_at<const int>(a, a.W.rowbase) + e) + __ldcg(ws_at<const int>(a, a.W.pos) + p);
+  }
+  if (threadIdx.x < a.S + a.k) {
+    const int q = threadIdx.x;
+    int row;
+    float w = 1.0f;
+    if (q < a.S) {
+      row = q * a.B + t;
+    } else {
+      row = rows[q - a.S];
+      w = __ldcg(ws_at<const float>(a, a.W.w) + (size_t)t * a.k + (q - a.S));
+    }
+    ws_at<int>(a, a.W.list_tok)[row] = t;
+    ws_at<int>(a, a.W.list_q)[row] = q;
+    ws_at<float>(a, a.W.list_w)[row] = w;
+  }
+  for (int j = 0; j < a.k; ++j) rows[j] -= a.S * a.B;  // grouped routed row (activation copy)
   uint4* x16 = ws_at<uint4>(a, a.W.x16) + (size_t)t * nw;
   uint4* xg = ws_at<uint4>(a, a.W.xg);
   for (int i = threadIdx.x; i < nw; i += blockDim.x) {
@@ -816,26 +859,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_pf_plan(PfArgs a) {
     hdr[PF_NGU] = s_ntiles * mgu;
     hdr[PF_NDN] = s_ntiles * mdn;
   }
-  // Token lists: grouped row -> (token, slot rank q, routing weight).
-  int* list_tok = ws_at<int>(a, a.W.list_tok);
-  int* list_q = ws_at<int>(a, a.W.list_q);
-  float* list_w = ws_at<float>(a, a.W.list_w);
-  for (int p = threadIdx.x; p < a.S * a.B; p += PLAN_THREADS) {
-    list_tok[p] = p % a.B;
-    list_q[p] = p / a.B;
-    list_w[p] = 1.0f;
-  }
-  const int* idx = ws_at<int>(a, a.W.idx);
-  const float* w = ws_at<float>(a, a.W.w);
-  const int* pos = ws_at<int>(a, a.W.pos);
-  for (int p = threadIdx.x; p < a.B * a.k; p += PLAN_THREADS) {
-    const int ex = __ldcg(idx + p);
-    const int row = s_rowbase[ex] + __ldcg(pos + p);
-    list_tok[row] = p / a.k;
-    list_q[row] = a.S + p % a.k;
-    list_w[row] = __ldcg(w + p);
-    ws_at<int>(a, a.W.list_row)[p] = row - a.S * a.B;
-  }
+  if (e < a.E) ws_at<int>(a, a.W.rowbase)[e] = s_rowbase[e];
   if (e < a.E) counts[e] = 0;  // ready for the next call (every read of counts is above)
 }
 
@@ -1022,7 +1046,7 @@ extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, cons
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   k_pf_plan<<<1, PLAN_THREADS, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
-  k_pf_x16<<<B, 256, 0, stream>>>(a);
+  k_pf_token_rows<<<B, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   if (launch_gemm<GATEUP>(a, m_gateup, std::min(nsm, a.W.max_gu), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
   if (launch_gemm<DOWN>(a, m_down, std::min(nsm, a.W.max_dn), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
