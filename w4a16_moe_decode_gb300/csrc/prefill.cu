@@ -4,17 +4,18 @@
 //
 // With many tokens per expert the weights are worth staging: every 128-row x
 // 64-column weight block is dequantised once (E2M1 x E4M3 products are exact in
-// bf16) into shared memory in the 128-byte-swizzled K-major layout that
-// tcgen05.mma reads, the expert's tokens are gathered into the same layout with
-// cp.async, and one thread issues the tensor-core MMAs (M = 128 weight rows,
+// f16 and in bf16) into shared memory in the 128-byte-swizzled K-major layout
+// that tcgen05.mma reads, the expert's token rows arrive in the same layout by
+// TMA, and one elected thread issues the tensor-core MMAs (M = 128 weight rows,
 // N = up to 128 tokens, K = 16 per instruction) that accumulate in FP32 in
 // tensor memory. The epilogue reads the accumulators back with tcgen05.ld.
 //
-//   k_pf_gemm<ROUTER>  logits = Wr x^T      (bf16 router rows, cp.async)
+//   k_pf_gemm<ROUTER>  logits = Wr x^T      (bf16 router rows and tokens by TMA)
 //   k_pf_topk          sigmoid top-k per token; tokens counted per expert
-//   k_pf_plan          expert-grouped token lists, tile lists
-//   k_pf_gemm<GATEUP>  h = bf16(silu(G_g g) * G_u u) per (token, expert)
-//   k_pf_gemm<DOWN>    y[t][q] = w * G_d (c_d h) per (token, expert)
+//   k_pf_plan          slots, grouped-row bases, tile lists (one block)
+//   k_pf_token_rows    per token: its grouped-list entries, its f16 rows
+//   k_pf_gemm<GATEUP>  h = bf16(silu(G_g g) * G_u u) per (token, expert), f16 MMA
+//   k_pf_gemm<DOWN>    y[t][q] = w * G_d (c_d h) per (token, expert), bf16 MMA
 //   k_pf_combine       out = bf16(sum_q y[t][q]) in slot order
 #include <algorithm>
 #include <atomic>
@@ -199,13 +200,14 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
 //   warp 16  streams the packed weights into a ring of RAW_SL slots of RAW_KB
 //            k-blocks (lane p copies packed tile p's run of k-groups: few,
 //            large bulk copies), as far ahead as the ring allows, across tiles;
-//   warp 17  loads each k-block's 128 activation rows (and the router's
-//            weight rows) with TMA in the 128-byte swizzle into the stage;
-//   warp 18  issues the four MMAs of a k-block once both operands are in,
-//            commits them to the stage's mbarrier, and after a tile's last
-//            k-block to the accumulator buffer's mbarrier;
+//   warp 17  loads each stage's 128 activation rows per k-block (and the
+//            router's weight rows) with TMA in the 128-byte swizzle;
+//   warp 18  issues the MMAs of a stage (KPS k-blocks x 4 k-steps) once its
+//            single mbarrier reports both operands in, commits them to the
+//            stage's mbarrier, and after a tile's last k-block to the
+//            accumulator buffer's mbarrier;
 //   warps 0-15 dequantise the packed k-blocks into the stages' operands, two
-//            groups of 8 warps taking alternate k-blocks (warp w: packed tile
+//            groups of 8 warps taking alternate stages (warp w: packed tile
 //            w % 8), and run the epilogue of each tile from tensor memory. Two
 //            accumulator buffers (columns 0-127, 128-255) let the MMAs of the
 //            next tile start before the epilogue of this one has finished.
