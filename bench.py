@@ -17,6 +17,7 @@ the same workload instead (a bounded sample per step).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -191,11 +192,12 @@ def measured_peak_tflops() -> tuple[float, str]:
 
 def recorded_traffic(batch: int):
     """DRAM bytes per decode from the committed ncu summary, if it was taken on
-    the current kernel sources (the summary records their hash)."""
+    the current sources of the decode kernels (common.cuh, decode.cu; the
+    summary records their hash)."""
     import hashlib
     csrc = os.path.join(ROOT, "w4a16_moe_decode_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
+    for f in ("common.cuh", "decode.cu"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     digest = h.hexdigest()[:16]
@@ -379,31 +381,52 @@ def gpu_arm(args) -> None:
 
     def e2e(pool, B, steps):
         """Through the C ABI with host buffers: each step copies x from pinned
-        host memory, decodes, and copies out back to pinned host memory."""
+        host memory, decodes, and copies out back to pinned host memory. The
+        steps of one rotation (copy in, flint_moe_decode, copy out per layer)
+        are captured once into a CUDA graph and replayed, as a serving loop
+        would, so the number is not the Python launch overhead. (Copies on a
+        second stream with double buffers measured no faster: the copy nodes
+        break the programmatic launch chain between layers either way.)"""
         xh = [layers.synth_x(B, cfg.hidden, args.seed, L, dev).cpu().pin_memory() for L in range(P)]
         oh = [torch.empty(B, cfg.hidden, dtype=torch.int16).pin_memory() for _ in range(P)]
         xd = torch.empty(B, cfg.hidden, dtype=torch.int16, device=dev)
         od = torch.empty_like(xd)
         ws = layers.workspace(cfg, B, dev)
-        stream = torch.cuda.current_stream()
-        for s in range(min(steps, 50)):
-            L = s % P
-            xd.copy_(xh[L], non_blocking=True)
-            fb.flint_moe_decode(pool[L].handle, xd, B, od, ws, stream)
-            oh[L].copy_(od, non_blocking=True)
+        stream = torch.cuda.Stream(device=dev)
+        stream.wait_stream(torch.cuda.current_stream())
+        # plain cudaMemcpyAsync (one per copy) from the runtime the library uses
+        cudart = ctypes.CDLL("libcudart.so.13")
+        cudart.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                                           ctypes.c_void_p]
+        nbytes = B * cfg.hidden * 2
+
+        def memcpy(dst, src, kind):  # kind 1: host to device, 2: device to host
+            if cudart.cudaMemcpyAsync(dst.data_ptr(), src.data_ptr(), nbytes, kind, stream.cuda_stream) != 0:
+                raise RuntimeError("cudaMemcpyAsync failed")
+
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for L in range(P):
+                    memcpy(xd, xh[L], 1)
+                    fb.flint_moe_decode(pool[L].handle, xd, B, od, ws, stream)
+                    memcpy(oh[L], od, 2)
+            for _ in range(3):
+                g.replay()
+            barrier()
+            reps = max(1, steps // P)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            stream.synchronize()
         barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for s in range(steps):
-            L = s % P
-            xd.copy_(xh[L], non_blocking=True)
-            fb.flint_moe_decode(pool[L].handle, xd, B, od, ws, stream)
-            oh[L].copy_(od, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        return job_us_per_layer(slowest(e0.elapsed_time(e1)), steps, world)
+        st, bits = fb.flint_moe_read_status(ws)
+        if st != fb.OK or bits:
+            raise RuntimeError(f"device status {bits} in the end-to-end leg")
+        return job_us_per_layer(slowest(e0.elapsed_time(e1)), reps * P, world)
 
     def stack_leg(batches=(1, 2, 4, 8, 16, 32), passes=20):
         """The 47-layer stack: distinct layers (generator seed 1000 + L) as
