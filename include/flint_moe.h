@@ -255,7 +255,7 @@ flint_moe_status flint_moe_read_status(const void* workspace, int32_t* host_stat
  * other threads) race on the array: serialise them. Returns
  * FLINT_MOE_EUNSUPPORTED when the workspace this shape and batch need
  * (flint_moe_workspace_bytes) exceeds FLINT_MOE_NOALLOC_SCRATCH_BYTES (the
- * Flint-shape layer needs 6.1 MiB at B = 32, 0.39 MiB at B = 8). Device status bits are not
+ * Flint-shape layer needs 6.1 MiB at B = 32, 0.40 MiB at B = 8). Device status bits are not
  * reported; use flint_moe_decode with a workspace to read them. */
 flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* layer, const uint16_t* x_bf16,
                                           int32_t B, uint16_t* out_bf16, cudaStream_t stream);

@@ -83,12 +83,13 @@ __host__ __device__ inline Layout make_dense_layout(int N, int K, int fmt) {
 // ---------------------------------------------------------------------------
 enum : int { HDR_COUNTER = 0, HDR_STATUS = 1, HDR_NSLOTS = 2, HDR_NROWS = 3, HDR_BATCH = 4 };
 
-// Regions: router logits [B][E]; the routing of the last decode ([B][k]
+// Regions: router logits [B][E] and the selection keys the router derives
+// from them ([B][E], order-preserving unsigned form); the routing of the last decode ([B][k]
 // indices and weights, for read-back); the largest |h| per (slot, token) row;
 // h in bf16 [rows][I] in fragment order. Slot s (shared experts first, then
 // the distinct selected experts in ascending id) owns rows s * B .. s * B + B - 1.
 struct WsLayout {
-  size_t logits, topk_idx, topk_w, hmax, h, total;
+  size_t logits, keys, topk_idx, topk_w, hmax, h, total;
   int max_slots, max_rows;
 };
 
@@ -100,6 +101,7 @@ __host__ __device__ inline WsLayout make_ws_layout(int H, int E, int k, int I, i
   W.max_rows = W.max_slots * maxB;
   size_t o = 256;
   W.logits = o;   o = ws_align(o + sizeof(float) * maxB * E);
+  W.keys = o;     o = ws_align(o + sizeof(uint32_t) * maxB * E);
   W.topk_idx = o; o = ws_align(o + sizeof(int) * maxB * k);
   W.topk_w = o;   o = ws_align(o + sizeof(float) * maxB * k);
   W.hmax = o;     o = ws_align(o + sizeof(unsigned) * W.max_rows);

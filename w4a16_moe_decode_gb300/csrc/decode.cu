@@ -64,6 +64,7 @@ struct DecodeArgs {
 
 __device__ __forceinline__ int* ws_hdr(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws); }
 __device__ __forceinline__ float* ws_logits(const DecodeArgs& a) { return reinterpret_cast<float*>(a.ws + a.W.logits); }
+__device__ __forceinline__ uint32_t* ws_keys(const DecodeArgs& a) { return reinterpret_cast<uint32_t*>(a.ws + a.W.keys); }
 __device__ __forceinline__ int* ws_topk_idx(const DecodeArgs& a) { return reinterpret_cast<int*>(a.ws + a.W.topk_idx); }
 __device__ __forceinline__ float* ws_topk_w(const DecodeArgs& a) { return reinterpret_cast<float*>(a.ws + a.W.topk_w); }
 __device__ __forceinline__ unsigned* ws_hmax(const DecodeArgs& a) { return reinterpret_cast<unsigned*>(a.ws + a.W.hmax); }
@@ -316,46 +317,29 @@ __device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane
                                   bool write_debug, int tb, const float* logits) {
   constexpr int EPL = 8;
   const float* lg = logits + (size_t)t * a.E;
+  const uint32_t* kt = ws_keys(a) + (size_t)t * a.E;  // keys the router derived from the logits
   const int e0 = lane * EPL;
-  float lv[EPL];
+  uint32_t kv[EPL];
   if (a.E == 256) {  // 32 contiguous, 16-byte aligned bytes per lane
-    const uint4 p = ld_cg_v4(lg + e0), q = ld_cg_v4(lg + e0 + 4);
-    lv[0] = __uint_as_float(p.x); lv[1] = __uint_as_float(p.y); lv[2] = __uint_as_float(p.z);
-    lv[3] = __uint_as_float(p.w); lv[4] = __uint_as_float(q.x); lv[5] = __uint_as_float(q.y);
-    lv[6] = __uint_as_float(q.z); lv[7] = __uint_as_float(q.w);
+    const uint4 p = ld_cg_v4(kt + e0), q = ld_cg_v4(kt + e0 + 4);
+    kv[0] = p.x; kv[1] = p.y; kv[2] = p.z; kv[3] = p.w; kv[4] = q.x; kv[5] = q.y; kv[6] = q.z; kv[7] = q.w;
   } else {
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) lv[j] = __ldcg(lg + min(e0 + j, a.E - 1));  // clamped: all issue at once
+    for (int j = 0; j < EPL; ++j) kv[j] = __ldcg(kt + min(e0 + j, a.E - 1));  // clamped: all issue at once
   }
 #ifdef FLINT_MOE_TRACE
-  if (t == 0 && tb >= 0 && __float_as_uint(lv[0]) != 0x7FC00001u && __float_as_uint(lv[7]) != 0x7FC00001u)
-    FLINT_TRACE(a, 4);  // logits arrived (the condition makes the timer wait for them)
+  if (t == 0 && tb >= 0 && kv[0] != 1u && kv[7] != 1u) {
+    FLINT_TRACE(a, 4);  // keys arrived (the condition makes the timer wait for them)
+    FLINT_TRACE(a, 5);
+  }
 #endif
-  // Scores of the lane's 8 experts: the fast reciprocal for all of them, the
-  // IEEE division only where its range ends (rare, out of the common path).
-  float sc[EPL], y[EPL];
-  bool slow = false;
-#pragma unroll
-  for (int j = 0; j < EPL; ++j) {
-    y[j] = 1.0f + expf(-lv[j]);
-    sc[j] = rcp_nr(y[j]);
-    slow |= !(y[j] < RCP_NR_MAX);
-  }
-  if (slow) {
-#pragma unroll
-    for (int j = 0; j < EPL; ++j)
-      if (!(y[j] < RCP_NR_MAX)) sc[j] = rcp_ieee(y[j]);
-  }
+  // (key, complemented index) words: larger word = larger key, then lower index.
   uint64_t v[EPL];
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int e = e0 + j;
-    const float kf = a.bias ? sc[j] + __ldg(a.bias + min(e, a.E - 1)) : sc[j];
-    v[j] = e < a.E ? ((uint64_t)ordered_key(kf) << 32) | (uint32_t)(0xFFFF - e) : 0ull;
+    v[j] = e < a.E ? ((uint64_t)kv[j] << 32) | (uint32_t)(0xFFFF - e) : 0ull;
   }
-#ifdef FLINT_MOE_TRACE
-  if (t == 0 && tb >= 0 && v[0] != 1ull && v[7] != 1ull) FLINT_TRACE(a, 5);  // keys computed
-#endif
   ce_desc(v[0], v[2]); ce_desc(v[1], v[3]); ce_desc(v[4], v[6]); ce_desc(v[5], v[7]);
   ce_desc(v[0], v[4]); ce_desc(v[1], v[5]); ce_desc(v[2], v[6]); ce_desc(v[3], v[7]);
   ce_desc(v[0], v[1]); ce_desc(v[2], v[3]); ce_desc(v[4], v[5]); ce_desc(v[6], v[7]);
@@ -492,7 +476,8 @@ __device__ __forceinline__ SlotInfo slot_info(const DecodeArgs& a, const RouteSm
 // Tokens t0, t0 + ts, ... (NT of them) of the x chunk.
 template <int NCH, int NT>
 __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* xsm, int H, int lane, float* lg,
-                                            int E, int e, int t0, int ts, bool dry) {
+                                            uint32_t* kc, const float* bias, int E, int e, int t0, int ts,
+                                            bool dry) {
   float acc[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t] = 0.f;
@@ -503,10 +488,16 @@ __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* 
     for (int t = 0; t < NT; ++t)
       acc[t] = dot8_bf16(w, lds128(xsm + (size_t)(t0 + t * ts) * H * 2 + (lane + 32 * c) * 16), acc[t]);
   }
+  // Lane t stores token t's logit and its selection key (sigmoid + bias, in
+  // the order-preserving unsigned form the top-k compares), so the blocks that
+  // route after the dependency wait only compare.
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const float v = warp_sum(acc[t]);
-    if (lane == 0 && !dry) lg[(t0 + t * ts) * E + e] = v;
+    if (lane == t && !dry) {
+      lg[(t0 + t * ts) * E + e] = v;
+      kc[(t0 + t * ts) * E + e] = ordered_key(route_key(v, bias, e));
+    }
   }
 }
 
@@ -586,15 +577,16 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
       const int ntw = tg < nt ? (nt - tg + G - 1) / G : 0;  // this warp's tokens in the chunk
       if (e < a.E && ntw > 0) {
         float* lgc = lg + (size_t)t0 * a.E;
+        uint32_t* kcc = ws_keys(a) + (size_t)t0 * a.E;
         switch (ntw) {  // one code path per token count: no predicated-off work
-          case 1: router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
-          case 2: router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
-          case 3: router_dots<NCH, 3>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
-          case 4: router_dots<NCH, 4>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
-          case 5: router_dots<NCH, 5>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
-          case 6: router_dots<NCH, 6>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
-          case 7: router_dots<NCH, 7>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
-          default: router_dots<NCH, 8>(wrow, xsm, a.H, lane, lgc, a.E, e, tg, G, dry); break;
+          case 1: router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
+          case 2: router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
+          case 3: router_dots<NCH, 3>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
+          case 4: router_dots<NCH, 4>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
+          case 5: router_dots<NCH, 5>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
+          case 6: router_dots<NCH, 6>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
+          case 7: router_dots<NCH, 7>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
+          default: router_dots<NCH, 8>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
         }
         if (!dry) FLINT_TRACE(a, 7);
       }
