@@ -285,6 +285,15 @@ __device__ __forceinline__ uint32_t hmul2_bcast_hi(uint32_t q, uint32_t s) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// f16x2 holding two values exactly representable in bf16 -> bf16x2 (exact):
+// the dequantised NVFP4 weights (at most 6 significant bits, in [2^-10, 2688]).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h);
+  const float2 f = __half22float2(hv);
+  const __nv_bfloat162 b = __float22bfloat162_rn(f);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
 // codes_word: the 4 fragment bytes of one k-step; sg, sg8: the 4-byte scale
 // words of rows g and g + 8 in this k-group; ks selects the k-step's byte.
 __device__ __forceinline__ void nvfp4_afrag(uint32_t codes_word, uint32_t sg, uint32_t sg8, int ks,

@@ -601,8 +601,10 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
 
 // One k-group (64 columns) of a 16-row tile against NTMAX token tiles.
 // Even and odd k-groups accumulate into separate registers (cs) so that
-// consecutive mma.sync need not wait for one another.
-template <int FMT, int NTMAX>
+// consecutive mma.sync need not wait for one another. BF16B: the token
+// fragments are bf16 (the NVFP4 weights, exact in f16, are converted to bf16
+// exactly), so bf16 activations need no prescale or conversion.
+template <int FMT, int NTMAX, bool BF16B = false>
 __device__ __forceinline__ void tile_kgroup(const uint8_t* kp, const uint4 (&bx)[NTMAX][2], int nt_used, int lane,
                                             float (&acc)[NTMAX][4]) {
   const int g = lane >> 2;
@@ -615,11 +617,18 @@ __device__ __forceinline__ void tile_kgroup(const uint8_t* kp, const uint4 (&bx)
     for (int ks = 0; ks < 4; ++ks) {
       uint32_t af[4];
       nvfp4_afrag(cw[ks], sg, sg8, ks, af);
+      if (BF16B) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) af[j] = f16x2_to_bf16x2(af[j]);
+      }
 #pragma unroll
       for (int nt = 0; nt < NTMAX; ++nt) {
         if (nt < nt_used) {
           const uint4& q = bx[nt][ks >> 1];
-          mma_f16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
+          if (BF16B)
+            mma_bf16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
+          else
+            mma_f16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
         }
       }
     }
@@ -652,8 +661,6 @@ __device__ __forceinline__ void tile_kgroup(const uint8_t* kp, const uint4 (&bx)
 // previous layer's output, which had completed before the router (which lets
 // this kernel launch only after its own wait) started.
 // ===========================================================================
-constexpr int GU_MAX_GROUPS = 4;
-
 struct GateupPlan {
   size_t wbuf_off, xs_off, red_off, inv_off, bar_off, total;
 };
@@ -965,9 +972,11 @@ __device__ __forceinline__ void row_to_f16(uint8_t* row, int I, int kh, int lane
 // ===========================================================================
 // K3 for small batches (at most 4 tokens, NVFP4): each warp keeps nbuf items
 // in flight, each buffer holding the item's down tile and its h rows, so a
-// warp copies, converts and consumes its own items with no block barrier
-// before the final sum. Measured faster than the staged kernel below at
-// batch 1 (fewer instructions on the cold path after the wait).
+// warp copies and consumes its own items with no block barrier before the
+// final sum. The products run in bf16 (the dequantised weights are exact in
+// bf16), so h is used as stored, without the prescale pass of the staged
+// kernel. Measured faster than the staged kernel below at batch 1 (fewer
+// instructions on the cold path after the wait).
 // ===========================================================================
 struct DownItemsPlan {
   int buf_bytes, hrows, hstride;
@@ -1008,8 +1017,6 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
   const int dn_bytes = (int)a.L.dn_tile;
   float* acc_s = reinterpret_cast<float*>(smem + P.acc_off);
   int* s_items = reinterpret_cast<int*>(smem + P.items_off);  // per item: slot << 16 | tile << 8 | tokens, expert
-  float* s_hmax = reinterpret_cast<float*>(smem + P.hmax_off);
-  float* s_inv = reinterpret_cast<float*>(smem + P.inv_off) + warp * NBUF * 8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off) + warp * NBUF;
   auto buf = [&](int b) { return smem + (size_t)(warp * NBUF + b) * P.buf_bytes; };
   int* status = ws_hdr(a) + HDR_STATUS;
@@ -1110,13 +1117,14 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
   pdl_trigger();
   FLINT_TRACE(a, 18);
   for (int j = 0; j < NBUF && warp + nw * j < n_items; ++j) issue_h(j);
-  for (int i = threadIdx.x; i < n_slots * a.B; i += blockDim.x) s_hmax[i] = __uint_as_float(__ldcg(ws_hmax(a) + i));
-  __syncthreads();
+  // h is consumed as stored (bf16 products with the weights converted to bf16):
+  // no per-row prescale, so no max |h| to read, no conversion pass and no
+  // block barrier between the wait and the products.
   for (int j = 0; warp + nw * j < n_items; ++j) {
     int s, nt, expert;
     uint32_t bits;
     item_of(j, s, nt, bits, expert);
-    const int r0 = s * a.B + 8 * nt, Tc = min(8, a.B - 8 * nt);
+    const int Tc = min(8, a.B - 8 * nt);
     const int b = j % NBUF;
     const uint32_t parity = (uint32_t)((j / NBUF) & 1);
     if (!mbar_wait(&bars[b], parity, status)) {
@@ -1127,17 +1135,6 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
     if (j == 0) FLINT_TRACE(a, 19);
     uint8_t* wb = buf(b);
     uint8_t* hb = wb + dn_bytes;
-    if (FMT == FLINT_MOE_NVFP4) {
-      for (int n = 0; n < Tc; ++n) {
-        if (!((bits >> n) & 1u)) continue;
-        const int kh = prescale_exp(s_hmax[r0 + n]);
-        row_to_f16(hb + n * P.hstride, a.I, kh, lane);
-        if (lane == 0) s_inv[b * 8 + n] = exp2i(-kh);
-      }
-    } else if (lane < Tc) {
-      s_inv[b * 8 + lane] = 1.0f;
-    }
-    __syncwarp();
     float acc[2][1][4];
 #pragma unroll
     for (int c = 0; c < 2; ++c)
@@ -1151,9 +1148,9 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
       bx[0][0] = lds128(rp);
       bx[0][1] = lds128(rp + 16);
       if (kg & 1)
-        tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[1]);
+        tile_kgroup<FMT, 1, true>(wb + kg * KGB, bx, 1, lane, acc[1]);
       else
-        tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
+        tile_kgroup<FMT, 1, true>(wb + kg * KGB, bx, 1, lane, acc[0]);
     }
     const float Gd = a.globals[expert * 4 + 2];
 #pragma unroll
@@ -1165,10 +1162,9 @@ __global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
         if (s >= a.S)
           for (int r = 0; r < a.k; ++r)
             if (R.idx[tok * a.k + r] == expert) wt = R.w[tok * a.k + r];
-        const float inv = s_inv[b * 8 + n];
         float* dst = acc_s + (warp * a.B + tok) * 16;
-        dst[g] += wt * (((acc[0][0][hh] + acc[1][0][hh]) * inv) * Gd);
-        dst[g + 8] += wt * (((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * inv) * Gd);
+        dst[g] += wt * ((acc[0][0][hh] + acc[1][0][hh]) * Gd);
+        dst[g + 8] += wt * ((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * Gd);
       }
     }
     __syncwarp();

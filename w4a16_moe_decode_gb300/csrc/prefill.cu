@@ -181,13 +181,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc)
   return *reinterpret_cast<const uint32_t*>(&hv);
 }
 
-// f16x2 holding two values exactly representable in bf16 -> bf16x2 (exact).
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
-  const __half2 hv = *reinterpret_cast<const __half2*>(&h);
-  const float2 f = __half22float2(hv);
-  const __nv_bfloat162 b = __float22bfloat162_rn(f);
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
 
 // ---------------------------------------------------------------------------
 // The grouped GEMM. A tile is (slot, m-tile of 128 weight rows, first grouped
