@@ -144,3 +144,20 @@ def test_prefill_and_decode_agree_at_32_tokens():
     check_out(ref[keep], bits_to_f64(out_d)[tokens][keep], "decode B=32")
     decided = [t for t in range(B) if routing.gap[t] >= 1e-6]
     assert np.array_equal(idx_p[decided], idx_d.cpu().numpy()[decided])
+
+
+def test_prefill_parity_at_the_largest_bench_size():
+    """4096 tokens, the bench's largest prefill point: the routing of every
+    token against the oracle, and the outputs of sampled tokens spread over
+    the batch (first, last, and tokens in different token tiles)."""
+    d, B = FLINT, 4096
+    tokens = [0, 127, 128, 2047, 4095]
+    cfg = cfg_of(d)
+    dl = layers.synth_layer(cfg, 13, 0, DEV)
+    x, out, idx, w, _ = gpu_prefill(cfg, dl, B, 13, 0)
+    xo, router = oracle_inputs(d, 13, 0, B)
+    ref, routing = moe.moe_layer(xo, router, oracle_experts(d, 13, 0), oracle_config(d), None, tokens)
+    excluded = check_routing(routing, idx, w)  # every token
+    assert len(excluded) <= B // 100
+    keep = [i for i, t in enumerate(tokens) if t not in excluded]
+    check_out(ref[keep], bits_to_f64(out)[tokens][keep], "prefill B=4096")
