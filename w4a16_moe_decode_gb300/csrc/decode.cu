@@ -141,7 +141,7 @@ __device__ __forceinline__ uint4 norm8(const uint4 x, const uint4 w, float inv) 
 // every block that needs it from the logits in the workspace; the result is
 // a deterministic function of the logits, so all blocks agree.
 // ===========================================================================
-constexpr int MAX_WARPS = 16;
+constexpr int MAX_WARPS = 20;
 constexpr int USED_WORDS = MAX_EXPERTS / 32;
 
 // Routing result in shared memory. Slots are the S shared experts, then the
@@ -1682,9 +1682,11 @@ void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) 
   const size_t budget = B <= 2 ? 110 * 1024 : SMEM_LIMIT;
   const int want_nb = units_per_block <= 3 ? 1 : 2;
   // Up to 2 tokens a gate/up block stays small (3 groups) so that a down block
-  // runs beside it; larger batches take a fourth group of warps.
-  const int first = B <= 2 ? 2 : 0;
-  const int cand[][2] = {{4, want_nb}, {4, 1}, {3, want_nb}, {3, 1}, {2, 2}, {2, 1}, {1, 3}, {1, 2}, {1, 1}};
+  // runs beside it; larger batches take a fourth and fifth group of warps
+  // (five groups of 4 warps at 96 registers fill the register file).
+  const int first = B <= 2 ? 4 : 0;
+  const int cand[][2] = {{5, want_nb}, {5, 1}, {4, want_nb}, {4, 1}, {3, want_nb}, {3, 1}, {2, 2}, {2, 1},
+                         {1, 3},       {1, 2}, {1, 1}};
   for (int i = first; i < (int)(sizeof(cand) / sizeof(cand[0])); ++i) {
     const auto& c = cand[i];
     if (gateup_plan(H, B, fmt, ntmax, c[0], c[1]).total + route <= budget) {
