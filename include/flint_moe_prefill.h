@@ -36,8 +36,9 @@ extern "C" {
 /* Bytes of the prefill workspace for calls of up to max_tokens tokens
  * (1..FLINT_MOE_PREFILL_MAX_TOKENS); 0 if the configuration or count is not
  * supported (NVFP4 expert weights only). It holds the logits, the routing, the
- * expert-grouped token lists and tile lists, h (bf16) of every (token, expert)
- * pair and the FP32 expert outputs y [B][S + k][H] that the combine sums. */
+ * expert-grouped token lists and tile lists, the normalised (pre-norm block)
+ * and f16 token rows, h (bf16) of every (token, expert) pair and the FP32
+ * expert outputs y [B][S + k][H] that the combine sums. */
 size_t flint_moe_prefill_workspace_bytes(const flint_moe_config* cfg, int32_t max_tokens);
 
 /* Zeroes a prefill workspace's header and per-expert counters; call once
@@ -49,21 +50,38 @@ flint_moe_status flint_moe_prefill_workspace_init(const flint_moe_config* cfg, i
  * a no-op). x: bf16 [B][H]; out: bf16 [B][H] (must not overlap x); workspace:
  * workspace_bytes >= flint_moe_prefill_workspace_bytes(cfg, B), 256-byte
  * aligned, initialised once with flint_moe_prefill_workspace_init, not shared
- * with another call in flight. Six kernels in stream order:
+ * with another call in flight. Seven kernels in stream order:
  *   1. router GEMM on the tensor cores (bf16 router rows x tokens, FP32);
  *   2. sigmoid top-k per token, counting the tokens of every expert;
- *   3. plan: expert-grouped token lists and the (expert, 128-row tile,
- *      token tile) work lists;
- *   4. gate/up grouped GEMM: NVFP4 tiles dequantised to bf16 in shared memory,
- *      tcgen05.mma against the expert's gathered tokens, SiLU * up epilogue
- *      writing h (bf16);
- *   5. down grouped GEMM on h, epilogue writing w_j * y into y[B][S + k][H];
- *   6. combine: out = bf16(sum over the S + k rows of y), in that fixed order.
+ *   3. plan: slots, the first grouped row of every expert, and the (expert,
+ *      128-row tile, token tile) work lists;
+ *   4. per token: its entries of the expert-grouped row lists, and its row in
+ *      f16 (times a power of two that keeps every bf16 value exact) at its
+ *      grouped rows;
+ *   5. gate/up grouped GEMM: NVFP4 tiles dequantised to f16 in shared memory,
+ *      tcgen05.mma against the expert's token rows (loaded by TMA), SiLU * up
+ *      epilogue writing h (bf16);
+ *   6. down grouped GEMM on h (bf16 products), epilogue writing w_j * y into
+ *      y[B][S + k][H];
+ *   7. combine: out = bf16(sum over the S + k rows of y), in that fixed order.
  * NVFP4 layers only (FLINT_MOE_EUNSUPPORTED for BF16 weights). Inputs must be
  * finite. x and out 16-byte aligned. */
 flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, const uint16_t* x_bf16, int32_t B,
                                    uint16_t* out_bf16, void* workspace, size_t workspace_bytes,
                                    cudaStream_t stream);
+
+/* The layer as a pre-norm sublayer of the residual stream, for B tokens, with
+ * the same definition as flint_moe_decode_prenorm ("Day-0 Support for Flint on
+ * vLLM", section "Model architecture": a pre-norm MoE): for every row r,
+ *   x  = bf16(r * w / sqrt(mean(r^2) + eps))   (RMSNorm, w = the layer's norm weight)
+ *   r' = bf16(r + flint_moe_prefill(x))
+ * One more kernel normalises the rows into the workspace first; the combine
+ * adds the residual. residual_out may be residual_in (in-place update) but must
+ * not overlap it otherwise. FLINT_MOE_EINVAL if the layer has no norm weight
+ * (flint_moe_layer_set_norm). Otherwise as flint_moe_prefill. */
+flint_moe_status flint_moe_prefill_prenorm(const flint_moe_layer* layer, const uint16_t* residual_in_bf16,
+                                           int32_t B, uint16_t* residual_out_bf16, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream);
 
 /* Copies the routing of the last flint_moe_prefill of B tokens on this
  * workspace: idx int32 [B][k], w float32 [B][k], and (if logits is not NULL)

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import synth
 from oracle import moe
 from w4a16_moe_decode_gb300 import binding as fb
 from w4a16_moe_decode_gb300 import layers
@@ -161,3 +162,45 @@ def test_prefill_parity_at_the_largest_bench_size():
     assert len(excluded) <= B // 100
     keep = [i for i, t in enumerate(tokens) if t not in excluded]
     check_out(ref[keep], bits_to_f64(out)[tokens][keep], "prefill B=4096")
+
+
+def run_prefill_prenorm(d, B, seed, tokens=None, bias=None, inplace=False, scale=8.0, layer=0):
+    """The pre-norm block r' = r + layer(rmsnorm(r)) on the tensor-core path
+    against the oracle; the residual stream is the seeded x times a power of two."""
+    cfg = cfg_of(d)
+    bias_t = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).to(DEV)
+    dl = layers.synth_layer(cfg, seed, layer, DEV, bias=bias_t, norm_eps=1e-6)
+    r = (layers.synth_x(B, cfg.hidden, seed, layer, DEV).view(torch.bfloat16) * scale).view(torch.int16)
+    r_in = r.clone()
+    out = r if inplace else torch.full_like(r, 0x7FC0)
+    ws = layers.prefill_workspace(cfg, B, DEV)
+    fb.flint_moe_prefill_prenorm(dl.handle, r, B, out, ws)
+    idx = torch.empty(B, cfg.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(B, cfg.top_k, dtype=torch.float32, device=DEV)
+    fb.flint_moe_prefill_debug_routing(cfg, ws, B, idx, w)
+    st, bits = fb.flint_moe_read_status(ws)
+    assert st == fb.OK and bits == 0
+    xo, router = oracle_inputs(d, seed, layer, B)
+    ro = xo * scale
+    assert np.array_equal(bits_to_f64(r_in), ro)
+    gamma = moe.bf16_bits_to_f64(synth.norm_bf16(seed, layer, d["hidden"]))
+    tokens = list(range(B)) if tokens is None else tokens
+    ref, routing = moe.moe_block(ro, router, oracle_experts(d, seed, layer), oracle_config(d), gamma, 1e-6, bias,
+                                 tokens)
+    excluded = check_routing(routing, idx.cpu().numpy(), w.cpu().numpy(), tokens)
+    keep = [i for i, t in enumerate(tokens) if t not in excluded]
+    check_out(ref[keep], bits_to_f64(out)[tokens][keep], f"prefill prenorm B={B} seed={seed}")
+    return excluded
+
+
+@pytest.mark.parametrize("B,inplace", [(1, False), (37, True), (200, False)])
+def test_prefill_prenorm_tiny(B, inplace):
+    excluded = run_prefill_prenorm(TINY, B, seed=40 + B, inplace=inplace)
+    assert len(excluded) <= max(1, B // 20)
+
+
+def test_prefill_prenorm_flint_with_stack_bias():
+    bias = np.zeros(256, np.float32)
+    bias[:26] = np.float32(0.134765625)
+    excluded = run_prefill_prenorm(FLINT, 64, seed=1005, layer=5, tokens=[0, 31, 63], bias=bias, inplace=True)
+    assert not excluded

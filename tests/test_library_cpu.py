@@ -173,10 +173,11 @@ def test_prefill_workspace_bytes(lib):
     assert fb.flint_moe_prefill_workspace_bytes(flint_cfg(weight_fmt=fb.BF16), 64) == 0  # NVFP4 only
     w16, w512, w4096 = (fb.flint_moe_prefill_workspace_bytes(c, t) for t in (16, 512, 4096))
     assert 0 < w16 < w512 < w4096
-    # the FP32 expert outputs y [T][S + k][H], h [T (S + k)][I] bf16 and the
-    # routed pairs' grouped activation rows [T k][H] bf16 dominate
-    big = 4096 * (7 * (2048 * 4 + 512 * 2) + 6 * 2048 * 2)
-    assert big <= w4096 < big * 1.1
+    # the FP32 expert outputs y [T][S + k][H], h [T (S + k)][I] bf16, the
+    # routed pairs' grouped activation rows [T k][H] f16 and the normalised and
+    # f16 token rows [T][H] (two of them) dominate
+    big = 4096 * (7 * (2048 * 4 + 512 * 2) + 6 * 2048 * 2 + 2 * 2048 * 2)
+    assert big <= w4096 < big * 1.05
 
 
 def test_prefill_rejects_bad_arguments_on_the_host(lib):
@@ -199,5 +200,12 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert P(ctypes.byref(layer), x, 64, out, ws, need - 1, None) == fb.EINVAL   # workspace too small
     assert P(ctypes.byref(layer), x, 64, x + 4096, ws, need, None) == fb.EINVAL  # out overlaps x
     assert P(None, x, 64, out, ws, need, None) == fb.EINVAL
+    PN = L.flint_moe_prefill_prenorm
+    assert PN(ctypes.byref(layer), x, 64, out, ws, need, None) == fb.EINVAL  # no norm weight set
+    layer.norm_weight = 0x400000
+    layer.norm_eps = 1e-6
+    assert PN(ctypes.byref(layer), x, 64, x + 4096, ws, need, None) == fb.EINVAL  # partial overlap
+    layer.norm_weight = 0x400008
+    assert PN(ctypes.byref(layer), x, 64, out, ws, need, None) == fb.EINVAL  # misaligned norm weight
     layer.cfg.weight_fmt = fb.BF16
     assert P(ctypes.byref(layer), x, 64, out, ws, need, None) == fb.EUNSUPPORTED

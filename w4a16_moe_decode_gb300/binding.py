@@ -98,6 +98,8 @@ def lib() -> ctypes.CDLL:
             "flint_moe_prefill_workspace_init": (c_int32, [P(flint_moe_config), c_int32, c_void_p, c_void_p]),
             "flint_moe_prefill": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p, c_size_t,
                                             c_void_p]),
+            "flint_moe_prefill_prenorm": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p,
+                                                    c_size_t, c_void_p]),
             "flint_moe_prefill_debug_routing": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_void_p, c_void_p,
                                                           c_void_p, c_void_p]),
             "flint_synth_stream_key": (ctypes.c_uint64, [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
@@ -229,6 +231,14 @@ def flint_moe_prefill(layer: flint_moe_layer, x, B: int, out, workspace, workspa
     nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     _check("flint_moe_prefill", lib().flint_moe_prefill(ctypes.byref(layer), _ptr(x), B, _ptr(out), _ptr(workspace),
                                                         nbytes, _stream(stream)))
+
+
+def flint_moe_prefill_prenorm(layer: flint_moe_layer, residual_in, B: int, residual_out, workspace,
+                              workspace_bytes=None, stream=None) -> None:
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    _check("flint_moe_prefill_prenorm",
+           lib().flint_moe_prefill_prenorm(ctypes.byref(layer), _ptr(residual_in), B, _ptr(residual_out),
+                                           _ptr(workspace), nbytes, _stream(stream)))
 
 
 def flint_moe_prefill_debug_routing(cfg, workspace, B, idx, w, logits=None, stream=None) -> None:

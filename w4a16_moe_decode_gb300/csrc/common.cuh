@@ -344,4 +344,37 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// RMSNorm pieces (pre-norm sublayer), used identically by every kernel that
+// normalises a row, so all of them derive bit-identical normalised
+// activations: lane l owns the 16-byte chunks l, l + 32, ... of a row; its sum
+// of squares runs over them in that order, the warp total is a butterfly (the
+// same value in every lane), then 1 / sqrt(mean + eps) with IEEE square root
+// and division, and each value becomes bf16((x * inv) * w).
+__device__ __forceinline__ float sumsq8(const uint4 u, float acc) {
+  acc = fmaf(bf16lo(u.x), bf16lo(u.x), acc);
+  acc = fmaf(bf16hi(u.x), bf16hi(u.x), acc);
+  acc = fmaf(bf16lo(u.y), bf16lo(u.y), acc);
+  acc = fmaf(bf16hi(u.y), bf16hi(u.y), acc);
+  acc = fmaf(bf16lo(u.z), bf16lo(u.z), acc);
+  acc = fmaf(bf16hi(u.z), bf16hi(u.z), acc);
+  acc = fmaf(bf16lo(u.w), bf16lo(u.w), acc);
+  acc = fmaf(bf16hi(u.w), bf16hi(u.w), acc);
+  return acc;
+}
+
+__device__ __forceinline__ float rms_inv(float part, int H, float eps) {
+  const float ss = warp_sum(part);
+  return 1.0f / sqrtf(ss / (float)H + eps);
+}
+
+__device__ __forceinline__ uint32_t norm2(uint32_t x, uint32_t w, float inv) {
+  const __nv_bfloat162 r = __floats2bfloat162_rn((bf16lo(x) * inv) * bf16lo(w), (bf16hi(x) * inv) * bf16hi(w));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint4 norm8(const uint4 x, const uint4 w, float inv) {
+  return make_uint4(norm2(x.x, w.x, inv), norm2(x.y, w.y, inv), norm2(x.z, w.z, inv), norm2(x.w, w.w, inv));
+}
+
+
 }  // namespace flint

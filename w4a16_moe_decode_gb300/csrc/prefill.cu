@@ -47,7 +47,7 @@ enum : int { PF_STATUS = HDR_STATUS, PF_NSLOTS = 2, PF_NGU = 3, PF_NDN = 4 };
 // Workspace: header words, then 256-byte aligned regions sized for T tokens.
 struct PfLayout {
   size_t counts, logits, idx, w, pos, slot_expert, slot_row0, slot_count, list_tok, list_q, list_w, gu_tiles,
-      dn_tiles, rowbase, kx, x16, xg, h, y, total;
+      dn_tiles, rowbase, kx, xn, x16, xg, h, y, total;
   int max_slots, max_rows, max_gu, max_dn;
 };
 
@@ -75,6 +75,7 @@ __host__ __device__ inline PfLayout make_pf_layout(int H, int E, int k, int I, i
   W.dn_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_dn);
   W.rowbase = o;     o = ws_align(o + sizeof(int) * E);                // first grouped row of each routed expert
   W.kx = o;          o = ws_align(o + sizeof(int) * (size_t)T);       // per-token power-of-two prescale
+  W.xn = o;          o = ws_align(o + (size_t)2 * T * H);             // RMS-normalised x (pre-norm block)
   W.x16 = o;         o = ws_align(o + (size_t)2 * T * H);             // x * 2^kx in f16
   W.xg = o;          o = ws_align(o + (size_t)2 * T * k * H);         // the same rows grouped by routed expert
   W.h = o;           o = ws_align(o + (size_t)2 * W.max_rows * I);
@@ -95,6 +96,12 @@ struct PfArgs {
   uint8_t* ws;
   PfLayout W;
   uint16_t* out;           // [B][H]
+  // Pre-norm block: x is the normalised residual stream (in the workspace),
+  // res the residual stream itself, added to the output by the combine.
+  int prenorm;
+  const uint16_t* res;     // [B][H]
+  const uint16_t* gamma;   // [H]
+  float eps;
 };
 
 template <typename T>
@@ -858,7 +865,24 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_pf_plan(PfArgs a) {
   if (e < a.E) counts[e] = 0;  // ready for the next call (every read of counts is above)
 }
 
-// out[t][j] = bf16(sum over q of y[t][q][j]), q = shared experts, then top-k ranks.
+// Pre-norm block: xn = bf16(r * gamma / sqrt(mean(r^2) + eps)), one warp per
+// token, with the same lane order and arithmetic as the decode kernels.
+__global__ void __launch_bounds__(256) k_pf_norm(PfArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= a.B) return;
+  const uint4* r = reinterpret_cast<const uint4*>(a.res + (size_t)t * a.H);
+  const uint4* w = reinterpret_cast<const uint4*>(a.gamma);
+  uint4* xn = ws_at<uint4>(a, a.W.xn) + (size_t)t * (a.H / 8);
+  const int nch = a.H / 256;  // 16-byte chunks per lane
+  float part = 0.f;
+  for (int c = 0; c < nch; ++c) part = sumsq8(__ldg(r + lane + 32 * c), part);
+  const float inv = rms_inv(part, a.H, a.eps);
+  for (int c = 0; c < nch; ++c) xn[lane + 32 * c] = norm8(__ldg(r + lane + 32 * c), __ldg(w + lane + 32 * c), inv);
+}
+
+// out[t][j] = bf16(sum over q of y[t][q][j]), q = shared experts, then top-k ranks;
+// for the pre-norm block out = bf16(r + that).
 __global__ void __launch_bounds__(256) k_pf_combine(PfArgs a) {
   const int Q = a.S + a.k;
   const size_t n4 = (size_t)a.B * a.H / 4;
@@ -873,7 +897,12 @@ __global__ void __launch_bounds__(256) k_pf_combine(PfArgs a) {
       acc.z += v.z;
       acc.w += v.w;
     }
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    if (a.prenorm) {  // residual stream: r + bf16(layer output), rounded to bf16
+      const uint2 rv = *reinterpret_cast<const uint2*>(a.res + t * a.H + j4 * 4);
+      lo = __floats2bfloat162_rn(bf16lo(rv.x) + __low2float(lo), bf16hi(rv.x) + __high2float(lo));
+      hi = __floats2bfloat162_rn(bf16lo(rv.y) + __low2float(hi), bf16hi(rv.y) + __high2float(hi));
+    }
     uint2 o;
     o.x = *reinterpret_cast<const uint32_t*>(&lo);
     o.y = *reinterpret_cast<const uint32_t*>(&hi);
@@ -987,8 +1016,8 @@ extern "C" flint_moe_status flint_moe_prefill_workspace_init(const flint_moe_con
   return FLINT_MOE_OK;
 }
 
-extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, const uint16_t* x, int32_t B,
-                                              uint16_t* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+static flint_moe_status prefill_impl(const flint_moe_layer* layer, const uint16_t* x, int32_t B, uint16_t* out,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream, bool prenorm) {
   if (!layer) return FLINT_MOE_EINVAL;
   const flint_moe_config* c = &layer->cfg;
   const flint_moe_status st = cfg_supported(c);
@@ -1001,7 +1030,9 @@ extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, cons
     return FLINT_MOE_EALIGN;
   const size_t xb = (size_t)B * c->hidden * 2;
   const uintptr_t xa = (uintptr_t)x, oa = (uintptr_t)out;
-  if (xa < oa + xb && oa < xa + xb) return FLINT_MOE_EINVAL;
+  // the pre-norm block may update the residual stream in place; otherwise x and out are disjoint
+  if (xa < oa + xb && oa < xa + xb && !(prenorm && xa == oa)) return FLINT_MOE_EINVAL;
+  if (prenorm && (!layer->norm_weight || (uintptr_t)layer->norm_weight % 16)) return FLINT_MOE_EINVAL;
   PfArgs a;
   a.H = c->hidden;
   a.I = c->inter;
@@ -1020,12 +1051,21 @@ extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, cons
   a.ws = static_cast<uint8_t*>(ws);
   a.W = make_pf_layout(a.H, a.E, a.k, a.I, a.S, B);
   a.out = out;
+  a.prenorm = prenorm ? 1 : 0;
+  a.res = x;
+  a.gamma = layer->norm_weight;
+  a.eps = layer->norm_eps;
   if (ws_bytes < a.W.total) return FLINT_MOE_EINVAL;
+  if (prenorm) {  // the layer runs on the normalised rows
+    k_pf_norm<<<(B + 7) / 8, 256, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
+    a.x = reinterpret_cast<const uint16_t*>(static_cast<uint8_t*>(ws) + a.W.xn);
+  }
 
   // TMA descriptors of the three GEMMs (host-side encoding, passed by value).
   PfMaps m_router, m_gateup, m_down;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  if (!encode_rows(&m_router.a, a.router, a.H, a.E) || !encode_rows(&m_router.b0, x, a.H, B) ||
+  if (!encode_rows(&m_router.a, a.router, a.H, a.E) || !encode_rows(&m_router.b0, a.x, a.H, B) ||
       !encode_rows(&m_gateup.b0, wsb + a.W.x16, a.H, B, true) ||
       !encode_rows(&m_gateup.b1, wsb + a.W.xg, a.H, (uint64_t)B * a.k, true) ||
       !encode_rows(&m_down.b0, wsb + a.W.h, a.I, (uint64_t)a.W.max_rows))
@@ -1049,6 +1089,17 @@ extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, cons
   k_pf_combine<<<cgrid, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   return FLINT_MOE_OK;
+}
+
+extern "C" flint_moe_status flint_moe_prefill(const flint_moe_layer* layer, const uint16_t* x, int32_t B,
+                                              uint16_t* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return prefill_impl(layer, x, B, out, ws, ws_bytes, stream, false);
+}
+
+extern "C" flint_moe_status flint_moe_prefill_prenorm(const flint_moe_layer* layer, const uint16_t* residual_in,
+                                                      int32_t B, uint16_t* residual_out, void* ws, size_t ws_bytes,
+                                                      cudaStream_t stream) {
+  return prefill_impl(layer, residual_in, B, residual_out, ws, ws_bytes, stream, true);
 }
 
 extern "C" flint_moe_status flint_moe_prefill_debug_routing(const flint_moe_config* c, const void* ws, int32_t B,
