@@ -481,6 +481,31 @@ def gpu_arm(args) -> None:
                             "frac": ub / (us_layer * 1e-6) / 1e9 / measured_peak_gbs()[0],
                             "mean_distinct_experts": statistics.mean(dl), "unique_bytes_per_layer": ub,
                             "biased_pick_fraction": biased / picks, "passes": passes}
+            if Bs >= 16:  # the same stack on the expert-grouped tensor-core path
+                ws_p = layers.prefill_workspace(cfg, Bs, dev)
+                with torch.cuda.stream(stream):
+                    gp = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gp, stream=stream):
+                        for L in range(P):
+                            fb.flint_moe_prefill_prenorm(stack[L].handle, bufs[L], Bs, bufs[L + 1], ws_p, None,
+                                                         stream)
+                    for _ in range(3):
+                        gp.replay()
+                    stream.synchronize()
+                    times = []
+                    for _ in range(passes):
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        gp.replay()
+                        e1.record(stream)
+                        stream.synchronize()
+                        times.append(e0.elapsed_time(e1))
+                st, bits = fb.flint_moe_read_status(ws_p)
+                if st != fb.OK or bits:
+                    raise RuntimeError(f"device status {bits} in the stack (tensor-core path)")
+                res[str(Bs)]["prefill_path_us_per_layer"] = statistics.median(times) * 1000.0 / P
+                del gp, ws_p
             del bufs
         del stack, ws_s
         torch.cuda.empty_cache()
