@@ -949,7 +949,7 @@ __device__ __forceinline__ void row_to_f16(uint8_t* row, int I, int kh, int lane
 // ===========================================================================
 struct DownItemsPlan {
   int buf_bytes, hrows, hstride;
-  size_t acc_off, items_off, hmax_off, inv_off, bar_off, total;
+  size_t acc_off, items_off, bar_off, total;
 };
 
 __host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, int max_slots, int fmt, int nbuf, int nw) {
@@ -962,9 +962,6 @@ __host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, in
   size_t o = (size_t)nw * nbuf * p.buf_bytes;
   p.acc_off = o;    o += sizeof(float) * nw * B * 16;
   p.items_off = o;  o += sizeof(int) * 2 * max_slots * nt;
-  p.hmax_off = o;   o += sizeof(float) * max_slots * B;
-  o = (o + 15) & ~(size_t)15;
-  p.inv_off = o;    o += sizeof(float) * nw * nbuf * 8;
   o = (o + 15) & ~(size_t)15;
   p.bar_off = o;    o += sizeof(uint64_t) * nw * nbuf;
   p.total = o;
