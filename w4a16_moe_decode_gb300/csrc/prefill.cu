@@ -32,9 +32,10 @@ namespace pf {
 constexpr int BM = 128;       // weight rows per tile (MMA M)
 constexpr int BK = 64;        // k per pipeline stage: one 128-byte swizzle row of bf16
 constexpr int NT = 128;       // tokens per tile at most (MMA N)
-constexpr int KPS = 2;        // k-blocks per operand stage (one handshake per stage)
-constexpr int STAGES = 2;     // operand stages in shared memory
-constexpr uint32_t TMEM_COLS = 2 * NT;  // N <= NT columns are used; the margin costs nothing at one CTA per SM
+constexpr int NPIPE = 2;      // independent GEMM pipelines per CTA (one CTA per SM)
+constexpr int KPS = 1;        // k-blocks per operand stage
+constexpr int STAGES = 2;     // operand stages per pipeline
+constexpr uint32_t TMEM_COLS = 512;  // per pipeline two accumulator buffers of NT columns
 constexpr int A_KBLK = BM * BK * 2;               // 16 KiB: one k-block of the weight operand
 constexpr int B_KBLK = NT * BK * 2;               // 16 KiB: one k-block of the token operand
 constexpr int A_STAGE = KPS * A_KBLK;
@@ -212,12 +213,14 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc)
 //            accumulator buffers (columns 0-127, 128-255) let the MMAs of the
 //            next tile start before the epilogue of this one has finished.
 // ---------------------------------------------------------------------------
-constexpr int CWARPS = 16;
-constexpr int W_RAW = 16, W_B = 17, W_MMA = 18;
-constexpr int GEMM_THREADS = 19 * 32;
+constexpr int PCW = 8;                      // dequantising warps per pipeline
+constexpr int W_PROD0 = NPIPE * PCW;         // producer warp of pipeline p: W_PROD0 + p
+constexpr int W_MMA0 = W_PROD0 + NPIPE;      // MMA-issue warp of pipeline p: W_MMA0 + p
+constexpr int GEMM_THREADS = (W_MMA0 + NPIPE) * 32;
 constexpr int RAW_KB = 4;   // k-blocks of one packed weight slot (eight copies of RAW_KB k-groups)
-constexpr int RAW_SL = 4;   // slots in the ring: up to 16 k-blocks in flight
+constexpr int RAW_SL = 2;   // slots per pipeline: up to 8 k-blocks in flight
 constexpr int RAW_SLOT = (BM / 16) * RAW_KB * KG_NVFP4;  // 18 KiB
+constexpr int PIPE_BYTES = STAGES * (A_STAGE + B_STAGE) + RAW_SL * RAW_SLOT;  // 100 KiB
 
 struct PfMaps {  // TMA descriptors, bf16, 64-column x 128-row boxes, 128-byte swizzle
   CUtensorMap a;   // router rows (router GEMM)
@@ -225,20 +228,18 @@ struct PfMaps {  // TMA descriptors, bf16, 64-column x 128-row boxes, 128-byte s
   CUtensorMap b1;  // the routed pairs' grouped activation rows (gate/up)
 };
 
-struct GemmSmem {
-  uint64_t raw_full[RAW_SL];
-  uint64_t raw_empty[RAW_SL];
-  uint64_t full[STAGES];      // the stage's token rows landed (TMA) and its weights are dequantised
-  uint64_t mma_done[STAGES];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+struct GemmSmem {  // per pipeline
+  uint64_t raw_full[NPIPE][RAW_SL];
+  uint64_t raw_empty[NPIPE][RAW_SL];
+  uint64_t full[NPIPE][STAGES];      // the stage's token rows landed (TMA) and its weights are dequantised
+  uint64_t mma_done[NPIPE][STAGES];
+  uint64_t acc_full[NPIPE][2];
+  uint64_t acc_empty[NPIPE][2];
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t gemm_dyn_smem() {
-  return 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + (size_t)RAW_SL * RAW_SLOT;
-}
+constexpr size_t gemm_dyn_smem() { return 1024 + (size_t)NPIPE * PIPE_BYTES; }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -326,10 +327,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   extern __shared__ uint8_t dsmem[];
   __shared__ GemmSmem G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t base = (smem_addr(dsmem) + 1023u) & ~1023u;
+  // Pipeline of this warp, its shared memory and tensor-memory columns.
+  const int p = warp < W_PROD0 ? warp / PCW : (warp < W_MMA0 ? warp - W_PROD0 : warp - W_MMA0);
+  const uint32_t base = ((smem_addr(dsmem) + 1023u) & ~1023u) + (uint32_t)(p * PIPE_BYTES);
   uint8_t* const base_ptr = dsmem + (base - smem_addr(dsmem));
-  const uint32_t a_op = base;                                   // STAGES x 32 KiB
-  const uint32_t b_op = base + STAGES * A_STAGE;                // STAGES x 32 KiB
+  const uint32_t a_op = base;                                   // STAGES x 16 KiB
+  const uint32_t b_op = base + STAGES * A_STAGE;                // STAGES x 16 KiB
   uint8_t* const raw = base_ptr + STAGES * (A_STAGE + B_STAGE);  // RAW_SL x 18 KiB
   int* status = ws_at<int>(a, 0) + PF_STATUS;
   volatile int* abort = &G.abort;
@@ -339,31 +342,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   const int n_tiles = MODE == ROUTER ? ((a.E + BM - 1) / BM) * ((a.B + NT - 1) / NT)
                                      : __ldcg(ws_at<int>(a, 0) + (MODE == GATEUP ? PF_NGU : PF_NDN));
   if ((int)blockIdx.x >= n_tiles) return;  // uniform: no tensor memory taken
-  const int my_tiles = (n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-  const int total = my_tiles * KB;  // k-blocks of this CTA
-  // Packed weights travel in slots of up to RAW_KB k-blocks of one tile: slot
-  // u of the CTA is slot u % SPT of tile u / SPT, k-blocks RAW_KB (u % SPT) ...
+  const int cta_tiles = (n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  // Pipeline p takes the CTA's tiles p, p + NPIPE, ...
+  const int my_tiles = cta_tiles > p ? (cta_tiles - p + NPIPE - 1) / NPIPE : 0;
+  const int total = my_tiles * KB;  // k-blocks of this pipeline
+  auto tile_of = [&](int i) { return (int)blockIdx.x + (p + NPIPE * i) * (int)gridDim.x; };
+  // Packed weights travel in slots of up to RAW_KB k-blocks of one tile.
   const int SPT = (KB + RAW_KB - 1) / RAW_KB;
   const int n_slots = my_tiles * SPT;
-  // Operand stages hold KPS k-blocks: stage-block v is k-blocks KPS (v % SBT) .. of tile v / SBT.
-  const int SBT = (KB + KPS - 1) / KPS;
-  const int n_sb = my_tiles * SBT;
-  auto tile_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RAW_SL; ++s) {
-      mbar_init(&G.raw_full[s], 1);
-      mbar_init(&G.raw_empty[s], CWARPS);
-    }
-    for (int s = 0; s < STAGES; ++s) {
-      // the TMA warp's expect-tx arrival, plus one arrival per warp of the
-      // dequantising group (8 warps) when the weights come from the raw ring
-      mbar_init(&G.full[s], MODE == ROUTER ? 1 : 1 + CWARPS / 2);
-      mbar_init(&G.mma_done[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&G.acc_full[b], 1);
-      mbar_init(&G.acc_empty[b], CWARPS);
+    for (int q = 0; q < NPIPE; ++q) {
+      for (int s = 0; s < RAW_SL; ++s) {
+        mbar_init(&G.raw_full[q][s], 1);
+        mbar_init(&G.raw_empty[q][s], PCW);
+      }
+      for (int s = 0; s < STAGES; ++s) {
+        // the TMA lane's expect-tx arrival, plus one arrival per dequantising warp
+        mbar_init(&G.full[q][s], MODE == ROUTER ? 1 : 1 + PCW);
+        mbar_init(&G.mma_done[q][s], 1);
+      }
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&G.acc_full[q][b], 1);
+        mbar_init(&G.acc_empty[q][b], PCW);
+      }
     }
     G.abort = 0;
     fence_mbar_init();
@@ -377,107 +379,92 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = G.tmem_base;
+  const uint32_t tmem = G.tmem_base + (uint32_t)(p * 2 * NT);  // this pipeline's two accumulators
 
-  if (warp == W_RAW) {
-    // ---------------- packed weight k-blocks -> raw ring (lane p copies packed tile p) ----------------
-    if (MODE != ROUTER) {
+  if (warp >= W_PROD0 && warp < W_MMA0) {
+    if (lane == 0 && MODE != ROUTER) {
+      // ---------------- packed weights -> raw ring (one lane issues the slot's eight copies) ----------------
       const uint64_t pol = l2_evict_first_policy();
-      int u = 0;
-      TileInfo nxt = tile_info<MODE>(a, tile_of(0));
-      const uint8_t* wsrc = nullptr;  // this lane's packed tile
       const int64_t wtile = MODE == GATEUP ? a.L.gu_tile : a.L.dn_tile;
+      int u = 0;
+      TileInfo nxt = my_tiles > 0 ? tile_info<MODE>(a, tile_of(0)) : TileInfo{};
+      const uint8_t* wsrc = nullptr;
       for (; u < n_slots; ++u) {
         const int sl = u % RAW_SL, i = u / SPT, kb0 = (u % SPT) * RAW_KB;
         const int nk = min(RAW_KB, KB - kb0);
-        bool ok = u < RAW_SL || wait_ab(&G.raw_empty[sl], ((u / RAW_SL) - 1) & 1, abort, status);
-        if (!__all_sync(0xffffffffu, ok)) break;
+        if (u >= RAW_SL && !wait_ab(&G.raw_empty[p][sl], ((u / RAW_SL) - 1) & 1, abort, status)) break;
         if (kb0 == 0) {
           const TileInfo t = nxt;
           if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
           wsrc = a.packed + (int64_t)t.expert * a.L.expert_bytes + (MODE == GATEUP ? 0 : a.L.gu_bytes) +
-                 (int64_t)(t.mt * 8 + (lane & 7)) * wtile;
+                 (int64_t)(t.mt * 8) * wtile;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&G.raw_full[sl], (uint32_t)((BM / 16) * nk * KG_NVFP4));
-        __syncwarp();
-        if (lane < BM / 16)
-          bulk_g2s_pol(smem_addr(raw + sl * RAW_SLOT + lane * RAW_KB * KG_NVFP4), wsrc + (int64_t)kb0 * KG_NVFP4,
-                       (uint32_t)(nk * KG_NVFP4), &G.raw_full[sl], pol);
+        mbar_arrive_expect_tx(&G.raw_full[p][sl], (uint32_t)((BM / 16) * nk * KG_NVFP4));
+        for (int q = 0; q < BM / 16; ++q)
+          bulk_g2s_pol(smem_addr(raw + sl * RAW_SLOT + q * RAW_KB * KG_NVFP4), wsrc + q * wtile + (int64_t)kb0 * KG_NVFP4,
+                       (uint32_t)(nk * KG_NVFP4), &G.raw_full[p][sl], pol);
       }
-      // The CTA's memory must outlive every copy this warp started.
-      if (lane == 0)
-        for (int r = (u > RAW_SL ? u - RAW_SL : 0); r < u; ++r) mbar_drain(&G.raw_full[r % RAW_SL], (r / RAW_SL) & 1);
-    }
-  } else if (warp == W_B) {
-    // ---------------- activation (and router weight) k-blocks -> stages, TMA ----------------
-    if (lane == 0) {
+      // The CTA's memory must outlive every copy this lane started.
+      for (int r = (u > RAW_SL ? u - RAW_SL : 0); r < u; ++r) mbar_drain(&G.raw_full[p][r % RAW_SL], (r / RAW_SL) & 1);
+    } else if (lane == 1) {
+      // ---------------- token rows (and router weight rows) -> stages, TMA ----------------
       int v = 0;
-      TileInfo nxt = tile_info<MODE>(a, tile_of(0)), t = nxt;
-      for (; v < n_sb; ++v) {
-        const int s = v % STAGES, i = v / SBT, kb0 = (v % SBT) * KPS, nkv = min(KPS, KB - kb0);
-        if (v >= STAGES && !wait_ab(&G.mma_done[s], ((v / STAGES) - 1) & 1, abort, status)) break;
-        if (kb0 == 0) {
+      TileInfo nxt = my_tiles > 0 ? tile_info<MODE>(a, tile_of(0)) : TileInfo{}, t = nxt;
+      for (; v < total; ++v) {
+        const int s = v % STAGES, i = v / KB, kb = v % KB;
+        if (v >= STAGES && !wait_ab(&G.mma_done[p][s], ((v / STAGES) - 1) & 1, abort, status)) break;
+        if (kb == 0) {
           t = nxt;
           if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
         }
-        mbar_arrive_expect_tx(&G.full[s], (uint32_t)(nkv * (MODE == ROUTER ? A_KBLK + B_KBLK : B_KBLK)));
-        for (int j = 0; j < nkv; ++j) {
-          const int x = (kb0 + j) * BK;
-          const uint32_t bdst = b_op + s * B_STAGE + j * B_KBLK;
-          if (MODE == ROUTER) {
-            tma_load_2d(a_op + s * A_STAGE + j * A_KBLK, &maps.a, x, t.mt * BM, &G.full[s]);
-            tma_load_2d(bdst, &maps.b0, x, t.row0, &G.full[s]);
-          } else if (MODE == GATEUP) {
-            if (t.slot < a.S)  // a shared expert's rows are the tokens in order
-              tma_load_2d(bdst, &maps.b0, x, t.row0 - t.slot * a.B, &G.full[s]);
-            else
-              tma_load_2d(bdst, &maps.b1, x, t.row0 - a.S * a.B, &G.full[s]);
-          } else {
-            tma_load_2d(bdst, &maps.b0, x, t.row0, &G.full[s]);
-          }
+        mbar_arrive_expect_tx(&G.full[p][s], (uint32_t)(MODE == ROUTER ? A_KBLK + B_KBLK : B_KBLK));
+        const int x = kb * BK;
+        const uint32_t bdst = b_op + s * B_STAGE;
+        if (MODE == ROUTER) {
+          tma_load_2d(a_op + s * A_STAGE, &maps.a, x, t.mt * BM, &G.full[p][s]);
+          tma_load_2d(bdst, &maps.b0, x, t.row0, &G.full[p][s]);
+        } else if (MODE == GATEUP) {
+          if (t.slot < a.S)  // a shared expert's rows are the tokens in order
+            tma_load_2d(bdst, &maps.b0, x, t.row0 - t.slot * a.B, &G.full[p][s]);
+          else
+            tma_load_2d(bdst, &maps.b1, x, t.row0 - a.S * a.B, &G.full[p][s]);
+        } else {
+          tma_load_2d(bdst, &maps.b0, x, t.row0, &G.full[p][s]);
         }
       }
-      for (int r = (v > STAGES ? v - STAGES : 0); r < v; ++r) mbar_drain(&G.full[r % STAGES], (r / STAGES) & 1);
+      for (int r = (v > STAGES ? v - STAGES : 0); r < v; ++r) mbar_drain(&G.full[p][r % STAGES], (r / STAGES) & 1);
     }
-  } else if (warp == W_MMA) {
+  } else if (warp >= W_MMA0) {
     // ---------------- tensor-core issue (one elected lane) ----------------
-    int v = 0;
-    TileInfo nxt = tile_info<MODE>(a, tile_of(0));
+    int g = 0;
+    TileInfo nxt = my_tiles > 0 ? tile_info<MODE>(a, tile_of(0)) : TileInfo{};
     uint32_t idesc = 0, acc = tmem;
-    // Descriptors of stage 0 and 1; k-block j and k-step ks add (j 16 KiB + ks 32 B) >> 4.
     const uint64_t ad0 = sw128_desc(a_op), ad1 = sw128_desc(a_op + A_STAGE);
     const uint64_t bd0 = sw128_desc(b_op), bd1 = sw128_desc(b_op + B_STAGE);
-    int s = 0, phase = 0, i = 0, kb0 = 0;  // stage, its phase parity, tile, first k-block of the stage-block
-    for (; v < n_sb; ++v) {
-      const int nkv = min(KPS, KB - kb0);
+    int s = 0, phase = 0, i = 0, kb = 0;  // stage, its phase parity, tile, k-block
+    for (; g < total; ++g) {
       bool ok = true;
-      if (kb0 == 0) {
+      if (kb == 0) {
         const TileInfo t = nxt;
         if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
         idesc = idesc_f32acc(BM, (t.n + 15) & ~15, MODE != GATEUP);  // gate/up runs in f16
         acc = tmem + (uint32_t)((i & 1) * NT);
-        ok = i < 2 || wait_ab(&G.acc_empty[i & 1], ((i / 2) - 1) & 1, abort, status);
+        ok = i < 2 || wait_ab(&G.acc_empty[p][i & 1], ((i / 2) - 1) & 1, abort, status);
       }
-      ok = ok && wait_ab(&G.full[s], (uint32_t)phase, abort, status);
+      ok = ok && wait_ab(&G.full[p][s], (uint32_t)phase, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint64_t ad = s ? ad1 : ad0, bd = s ? bd1 : bd0;
       if (elect_one()) {
 #pragma unroll
-        for (int j = 0; j < KPS; ++j)
-          if (j < nkv) {
-#pragma unroll
-            for (int ks = 0; ks < BK / 16; ++ks)
-              tc_mma(acc, ad + (uint64_t)((j * A_KBLK + ks * 32) >> 4), bd + (uint64_t)((j * B_KBLK + ks * 32) >> 4),
-                     idesc, (kb0 + j > 0 || ks > 0) ? 1u : 0u);
-          }
-        tc_commit(&G.mma_done[s]);
-        if (kb0 + nkv == KB) tc_commit(&G.acc_full[i & 1]);
+        for (int ks = 0; ks < BK / 16; ++ks)
+          tc_mma(acc, ad + (uint64_t)((ks * 32) >> 4), bd + (uint64_t)((ks * 32) >> 4), idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(&G.mma_done[p][s]);
+        if (kb == KB - 1) tc_commit(&G.acc_full[p][i & 1]);
       }
       __syncwarp();
-      kb0 += KPS;
-      if (kb0 >= KB) {
-        kb0 = 0;
+      if (++kb == KB) {
+        kb = 0;
         ++i;
       }
       if (++s == STAGES) {
@@ -487,15 +474,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
     }
     // Let the MMAs in flight finish before the memory goes away.
     if (lane == 0)
-      for (int r = (v > STAGES ? v - STAGES : 0); r < v; ++r) mbar_drain(&G.mma_done[r % STAGES], (r / STAGES) & 1);
+      for (int r = (g > STAGES ? g - STAGES : 0); r < g; ++r) mbar_drain(&G.mma_done[p][r % STAGES], (r / STAGES) & 1);
   } else {
     // ---------------- consumers: dequantise, epilogue ----------------
-    // Two groups of 8 warps take alternate k-blocks of each weight slot; warp
-    // w dequantises packed tile w % 8 (all four k-steps) of its group's
-    // k-blocks. Every consumer warp frees the slot once, after its k-blocks.
-    TileInfo nxt = tile_info<MODE>(a, tile_of(0)), t = nxt;
-    const int gid = warp >> 3, dq_p = warp & 7, dq_g = lane >> 2, dq_t = lane & 3;
-    const int q4 = warp & 3, cg = warp >> 2;  // epilogue: lanes 32 q4.., columns 32 cg..
+    // Warp lw of the pipeline dequantises packed tile lw (all four k-steps) of
+    // every k-block and reads tensor-memory lanes 32 (lw % 4) .., columns
+    // 64 (lw / 4) .. of each tile's accumulator.
+    const int lw = warp - p * PCW;
+    TileInfo nxt = my_tiles > 0 ? tile_info<MODE>(a, tile_of(0)) : TileInfo{}, t = nxt;
+    const int dq_p = lw, dq_g = lane >> 2, dq_t = lane & 3;
+    const int q4 = lw & 3, cg = lw >> 2;
     uint32_t doff[4][4];  // this lane's swizzled 4-byte destinations in a stage
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
@@ -506,82 +494,75 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
       doff[ks][3] = sw128_off(r0 + 8, c0 + 8);
     }
     const uint32_t tile_off = (uint32_t)(dq_p * RAW_KB * KG_NVFP4);
-    int ctok = 0, cq = 0;
-    float cw = 0.f, cinv = 1.f;
+    int ctok[2] = {0, 0}, cq[2] = {0, 0};  // this lane's two epilogue columns: 64 cg + lane, + 32
+    float cw[2] = {0.f, 0.f}, cinv[2] = {1.f, 1.f};
     bool failed = false;
     for (int u = 0; u < n_slots && !failed; ++u) {
       const int i = u / SPT, kb0 = (u % SPT) * RAW_KB, nk = min(RAW_KB, KB - kb0);
       if (kb0 == 0) {
         t = nxt;
         if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
-        const int c = cg * 32 + lane;  // this lane's epilogue column
-        if (MODE == GATEUP && c < t.n) {  // 2^-kx of its token
-          const int tok = t.slot < a.S ? t.row0 - t.slot * a.B + c : __ldcg(ws_at<const int>(a, a.W.list_tok) + t.row0 + c);
-          cinv = exp2i(-__ldcg(ws_at<const int>(a, a.W.kx) + tok));
-        }
-        if (MODE == DOWN && c < t.n) {
-          const int row = t.row0 + c;
-          ctok = __ldcg(ws_at<const int>(a, a.W.list_tok) + row);
-          cq = __ldcg(ws_at<const int>(a, a.W.list_q) + row);
-          cw = __ldcg(ws_at<const float>(a, a.W.list_w) + row);
+#pragma unroll
+        for (int hcol = 0; hcol < 2; ++hcol) {
+          const int c = cg * 64 + hcol * 32 + lane;
+          if (MODE == GATEUP && c < t.n) {  // 2^-kx of its token
+            const int tok = t.slot < a.S ? t.row0 - t.slot * a.B + c : __ldcg(ws_at<const int>(a, a.W.list_tok) + t.row0 + c);
+            cinv[hcol] = exp2i(-__ldcg(ws_at<const int>(a, a.W.kx) + tok));
+          }
+          if (MODE == DOWN && c < t.n) {
+            const int row = t.row0 + c;
+            ctok[hcol] = __ldcg(ws_at<const int>(a, a.W.list_tok) + row);
+            cq[hcol] = __ldcg(ws_at<const int>(a, a.W.list_q) + row);
+            cw[hcol] = __ldcg(ws_at<const float>(a, a.W.list_w) + row);
+          }
         }
       }
       if (MODE != ROUTER) {
         const uint8_t* slot_p = raw + (u % RAW_SL) * RAW_SLOT + tile_off;
-        // Stage-block sb = gid of the slot: k-blocks 2 gid, 2 gid + 1 of the slot.
-        const int nsb = (nk + KPS - 1) / KPS;
-        bool ok = gid >= nsb || wait_ab(&G.raw_full[u % RAW_SL], (u / RAW_SL) & 1, abort, status);
-        if (gid < nsb) {
-          const int v = i * SBT + kb0 / KPS + gid, s = v % STAGES;
-          const int nkv = min(KPS, nk - gid * KPS);
-          ok = ok && (v < STAGES || wait_ab(&G.mma_done[s], ((v / STAGES) - 1) & 1, abort, status));
-          if (__all_sync(0xffffffffu, ok)) {
-            uint4 codes[KPS];
-            uint32_t sg[KPS], sg8[KPS];
-#pragma unroll
-            for (int j = 0; j < KPS; ++j)
-              if (j < nkv) {
-                const uint8_t* kp = slot_p + (gid * KPS + j) * KG_NVFP4;
-                codes[j] = lds128(kp + lane * 16);
-                sg[j] = lds32(kp + KG_CODE_BYTES + dq_g * 4);
-                sg8[j] = lds32(kp + KG_CODE_BYTES + (dq_g + 8) * 4);
-              }
-#pragma unroll
-            for (int j = 0; j < KPS; ++j)
-              if (j < nkv) {
-                const uint32_t cw4[4] = {codes[j].x, codes[j].y, codes[j].z, codes[j].w};
-                const uint32_t ap = a_op + s * A_STAGE + j * A_KBLK;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                  uint32_t af[4];
-                  nvfp4_afrag(cw4[ks], sg[j], sg8[j], ks, af);
-#pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(ap + doff[ks][q]),
-                                 "r"(MODE == GATEUP ? af[q] : f16x2_to_bf16x2(af[q]))
-                                 : "memory");
-                }
-              }
-            fence_proxy_async();  // these st.shared -> visible to the tensor core
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&G.full[s]);
+        bool ok = wait_ab(&G.raw_full[p][u % RAW_SL], (u / RAW_SL) & 1, abort, status);
+        for (int j = 0; j < nk; ++j) {
+          const int g = i * KB + kb0 + j, s = g % STAGES;
+          ok = ok && (g < STAGES || wait_ab(&G.mma_done[p][s], ((g / STAGES) - 1) & 1, abort, status));
+          if (!__all_sync(0xffffffffu, ok)) {
+            failed = true;
+            break;
           }
+          const uint8_t* kp = slot_p + j * KG_NVFP4;
+          const uint4 codes = lds128(kp + lane * 16);
+          const uint32_t sg = lds32(kp + KG_CODE_BYTES + dq_g * 4);
+          const uint32_t sg8 = lds32(kp + KG_CODE_BYTES + (dq_g + 8) * 4);
+          const uint32_t cw4[4] = {codes.x, codes.y, codes.z, codes.w};
+          const uint32_t ap = a_op + s * A_STAGE;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            uint32_t af[4];
+            nvfp4_afrag(cw4[ks], sg, sg8, ks, af);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              asm volatile("st.shared.u32 [%0], %1;" ::"r"(ap + doff[ks][q]),
+                           "r"(MODE == GATEUP ? af[q] : f16x2_to_bf16x2(af[q]))
+                           : "memory");
+          }
+          fence_proxy_async();  // these st.shared -> visible to the tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&G.full[p][s]);
         }
         if (failed || !__all_sync(0xffffffffu, ok)) {
           failed = true;
           break;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&G.raw_empty[u % RAW_SL]);  // this warp is done with the slot
+        if (lane == 0) mbar_arrive(&G.raw_empty[p][u % RAW_SL]);  // this warp is done with the slot
       }
       if (kb0 + nk == KB) {  // the tile's epilogue
         const int ab = i & 1;
-        const bool ok = wait_ab(&G.acc_full[ab], (i / 2) & 1, abort, status);
+        const bool ok = wait_ab(&G.acc_full[p][ab], (i / 2) & 1, abort, status);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         const int r = q4 * 32 + lane;  // weight row within the m-tile
         const uint32_t tacc = tmem + (uint32_t)(ab * NT) + ((uint32_t)(q4 * 32) << 16);
-        for (int c0 = cg * 32; c0 < cg * 32 + 32 && c0 < t.n; c0 += 16) {
+        for (int c0 = cg * 64; c0 < cg * 64 + 64 && c0 < t.n; c0 += 16) {
+          const int hcol = (c0 - cg * 64) >> 5;  // which of the lane's two column registers
           uint32_t v[16];
           tc_ld16(tacc + (uint32_t)c0, v);
           if (MODE == ROUTER) {
@@ -599,13 +580,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
             const bool gate = (lane & 8) == 0;
             const int ii = (t.mt * 8 + q4 * 2 + (lane >> 4)) * 8 + (lane & 7);
             uint16_t* hbuf = ws_at<uint16_t>(a, a.W.h);
+            const float cinv_h = hcol ? cinv[1] : cinv[0];
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
               const float v0 = __uint_as_float(v[j]), v1 = __uint_as_float(v[j + 1]);
               const float mine = gate ? v0 : v1;
               const float other = __shfl_xor_sync(0xffffffffu, gate ? v1 : v0, 8);
               const int c = c0 + j + (gate ? 0 : 1);
-              const float inv = __shfl_sync(0xffffffffu, cinv, c - cg * 32);
+              const float inv = __shfl_sync(0xffffffffu, cinv_h, c & 31);
               const float gv = (gate ? mine : other) * inv * Gg;
               const float uv = (gate ? other : mine) * inv * Gu;
               const float sv = __fdividef(gv, 1.0f + __expf(-gv));
@@ -619,19 +601,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
             float* y = ws_at<float>(a, a.W.y);
             const int jrow = t.mt * BM + r;
             const int q_per_tok = a.S + a.k;
+            const int ctok_h = hcol ? ctok[1] : ctok[0], cq_h = hcol ? cq[1] : cq[0];
+            const float cw_h = hcol ? cw[1] : cw[0];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int c = c0 + j, src = c - cg * 32;
-              const int tok = __shfl_sync(0xffffffffu, ctok, src);
-              const int qq = __shfl_sync(0xffffffffu, cq, src);
-              const float wv = __shfl_sync(0xffffffffu, cw, src);
+              const int c = c0 + j, src = c & 31;
+              const int tok = __shfl_sync(0xffffffffu, ctok_h, src);
+              const int qq = __shfl_sync(0xffffffffu, cq_h, src);
+              const float wv = __shfl_sync(0xffffffffu, cw_h, src);
               if (c < t.n) y[((size_t)tok * q_per_tok + qq) * a.H + jrow] = wv * (__uint_as_float(v[j]) * Gd);
             }
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&G.acc_empty[ab]);
+        if (lane == 0) mbar_arrive(&G.acc_empty[p][ab]);
       }
     }
   }
@@ -640,7 +624,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(G.tmem_base), "r"(TMEM_COLS) : "memory");
   }
 }
 
