@@ -231,6 +231,13 @@ flint_moe_status flint_moe_trace(int32_t op, uint64_t* host_events, cudaStream_t
 flint_moe_status flint_moe_debug_rcp_check(uint32_t lo_bits, uint32_t hi_bits,
                                            uint64_t* host_mismatches, cudaStream_t stream);
 
+/* Self-check of the failure path every kernel wait takes: one block waits on
+ * an mbarrier that nothing completes, gives up after the same bounded wait
+ * (about 200 ms of %globaltimer), sets FLINT_MOE_DEV_ERR_TIMEOUT in
+ * *dev_status (device int32) and returns, leaving the context usable.
+ * Asynchronous on stream. */
+flint_moe_status flint_moe_debug_wait_timeout(int32_t* dev_status, cudaStream_t stream);
+
 /* Reads the workspace status word into *host_status and clears it.
  * SYNCHRONISES the stream. Returns FLINT_MOE_ETIMEOUT if the timeout bit
  * was set, FLINT_MOE_OK otherwise (other bits are reported in *host_status). */

@@ -360,3 +360,17 @@ def test_decode_deterministic_and_chained_through_a_graph():
     check_out(ref[keep], bits_to_f64(serial[1])[keep], "layer 0")
     st, bits = fb.flint_moe_read_status(ws)
     assert st == fb.OK and bits == 0
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """The failure path of every kernel wait, without a fault: a wait that
+    nothing completes times out (about 200 ms), sets the timeout bit and
+    returns; the context stays usable for the next decode."""
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.time()
+    fb.flint_moe_debug_wait_timeout(status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x1  # FLINT_MOE_DEV_ERR_TIMEOUT
+    assert time.time() - t0 < 10.0
+    worst, excluded, _ = run_parity(TINY, 3, seed=5)  # the GPU still decodes correctly

@@ -209,3 +209,7 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
     assert PN(ctypes.byref(layer), x, 64, out, ws, need, None) == fb.EINVAL  # misaligned norm weight
     layer.cfg.weight_fmt = fb.BF16
     assert P(ctypes.byref(layer), x, 64, out, ws, need, None) == fb.EUNSUPPORTED
+
+
+def test_wait_timeout_check_validates_on_the_host(lib):
+    assert fb.lib().flint_moe_debug_wait_timeout(None, None) == fb.EINVAL

@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
             "flint_moe_read_status": (c_int32, [c_void_p, P(c_int32), c_void_p]),
             "flint_moe_trace": (c_int32, [c_int32, c_void_p, c_void_p]),
             "flint_moe_debug_rcp_check": (c_int32, [ctypes.c_uint32, ctypes.c_uint32, P(ctypes.c_uint64), c_void_p]),
+            "flint_moe_debug_wait_timeout": (c_int32, [c_void_p, c_void_p]),
             "flint_moe_quantize_nvfp4": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                                    c_void_p]),
             "flint_gemv_packed_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
@@ -284,6 +285,10 @@ def flint_moe_debug_rcp_check(lo_bits: int, hi_bits: int, stream=None) -> int:
     _check("flint_moe_debug_rcp_check", lib().flint_moe_debug_rcp_check(lo_bits, hi_bits, ctypes.byref(n),
                                                                         _stream(stream)))
     return n.value
+
+
+def flint_moe_debug_wait_timeout(dev_status, stream=None) -> None:
+    _check("flint_moe_debug_wait_timeout", lib().flint_moe_debug_wait_timeout(_ptr(dev_status), _stream(stream)))
 
 
 def flint_moe_quantize_nvfp4(w, n_mat, rows, cols, codes, scales, global_, stream=None) -> None:

@@ -1936,6 +1936,24 @@ extern "C" flint_moe_status flint_moe_debug_rcp_check(uint32_t lo_bits, uint32_t
   return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
 }
 
+// One block waits on an mbarrier that nothing completes: the bounded wait of
+// every kernel gives up, records the timeout and the block returns.
+__global__ void k_wait_timeout(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, status);
+}
+
+extern "C" flint_moe_status flint_moe_debug_wait_timeout(int32_t* dev_status, cudaStream_t stream) {
+  if (!dev_status) return FLINT_MOE_EINVAL;
+  k_wait_timeout<<<1, 64, 0, stream>>>(dev_status);
+  return cudaGetLastError() == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
+}
+
 extern "C" flint_moe_status flint_gemv(const void* packed, int32_t N, int32_t K, int32_t fmt, const uint16_t* x,
                                        int32_t B, uint16_t* y, const uint16_t* norm_weight, float eps,
                                        int32_t* dev_status, cudaStream_t stream) {
