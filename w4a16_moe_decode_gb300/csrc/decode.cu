@@ -460,12 +460,17 @@ __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* 
   // Lane t stores token t's logit and its selection key (sigmoid + bias, in
   // the order-preserving unsigned form the top-k compares), so the blocks that
   // route after the dependency wait only compare.
+// The key is computed in the warm-up pass too (only the stores are skipped),
+  // so its code is hot when the real pass runs.
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const float v = warp_sum(acc[t]);
-    if (lane == t && !dry) {
-      lg[(t0 + t * ts) * E + e] = v;
-      kc[(t0 + t * ts) * E + e] = ordered_key(route_key(v, bias, e));
+    if (lane == t) {
+      const uint32_t key = ordered_key(route_key(v, bias, e));
+      if (!dry) {
+        lg[(t0 + t * ts) * E + e] = v;
+        kc[(t0 + t * ts) * E + e] = key;
+      }
     }
   }
 }
