@@ -974,7 +974,7 @@ __host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, in
 }
 
 template <int FMT, int NBUF>
-__global__ void __launch_bounds__(256) k_down_items(DecodeArgs a) {
+__global__ void __launch_bounds__(512) k_down_items(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   __shared__ int s_wsum[MAX_WARPS];
@@ -1712,9 +1712,14 @@ cudaError_t launch_down(const DecodeArgs& a, cudaStream_t stream, const DownPlan
   return launch_pdl(k_down<FMT>, dim3(a.H / 16), dim3(32 * P.nw), P.total, stream, a);
 }
 
-constexpr int DOWN_ITEMS_NW = 8, DOWN_ITEMS_NBUF = 2;
+// Up to 2 tokens the block shares its SM with a gate/up block: 8 warps, two
+// buffers each. From 3 tokens on it runs alone: 16 warps, one buffer each.
+constexpr int DOWN_ITEMS_NW = 8, DOWN_ITEMS_NBUF = 2, DOWN_ITEMS_WIDE_NW = 16, DOWN_ITEMS_WIDE_NBUF = 1;
 size_t down_items_smem(const DecodeArgs& a) {
-  return down_items_plan(a.H, a.I, a.B, a.W.max_slots, a.fmt, DOWN_ITEMS_NBUF, DOWN_ITEMS_NW).total;
+  const bool wide = a.B >= 3;
+  return down_items_plan(a.H, a.I, a.B, a.W.max_slots, a.fmt, wide ? DOWN_ITEMS_WIDE_NBUF : DOWN_ITEMS_NBUF,
+                         wide ? DOWN_ITEMS_WIDE_NW : DOWN_ITEMS_NW)
+      .total;
 }
 
 cudaError_t launch_router(const DecodeArgs& a, cudaStream_t stream) {
@@ -1839,7 +1844,8 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   // residual values), as the compiler laid it out: static plus dynamic must
   // stay within the per-block limit.
   static const size_t route_smem = std::max({static_smem(k_down<FLINT_MOE_NVFP4>), static_smem(k_down<FLINT_MOE_BF16>),
-                                             static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF>)});
+                                             static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF>),
+                                             static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF>)});
   int gu_ng = 0;
   {
     const int units = a.W.max_slots * (a.I / 8), sms = sm_count();
@@ -1857,7 +1863,10 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_gateup<FLINT_MOE_NVFP4>(a, stream, gu_ng)
                                                        : launch_gateup<FLINT_MOE_BF16>(a, stream, gu_ng);
   if (e == cudaSuccess) {
-    if (small_down)
+    if (small_down && B >= 3)
+      e = launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF>, dim3(a.H / 16),
+                     dim3(32 * DOWN_ITEMS_WIDE_NW), down_items_smem(a), stream, a);
+    else if (small_down)
       e = launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF>, dim3(a.H / 16), dim3(32 * DOWN_ITEMS_NW),
                      down_items_smem(a), stream, a);
     else
