@@ -944,7 +944,7 @@ __device__ __forceinline__ void row_to_f16(uint8_t* row, int I, int kh, int lane
 }
 
 // ===========================================================================
-// K3 for small batches (at most 4 tokens, NVFP4): each warp keeps nbuf items
+// K3 for small batches (at most 8 tokens, NVFP4): each warp keeps nbuf items
 // in flight, each buffer holding the item's down tile and its h rows, so a
 // warp copies and consumes its own items with no block barrier before the
 // final sum. The products run in bf16 (the dequantised weights are exact in
@@ -1858,7 +1858,7 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
     return FLINT_MOE_EUNSUPPORTED;
   a.dn_nbuf = dp.nbuf;
   a.dn_hcap = dp.hcap;
-  const bool small_down = B <= 4 && a.fmt == FLINT_MOE_NVFP4 && down_items_smem(a) <= down_budget;
+  const bool small_down = B <= 8 && a.fmt == FLINT_MOE_NVFP4 && down_items_smem(a) <= down_budget;
   cudaError_t e = launch_router(a, stream);
   if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_gateup<FLINT_MOE_NVFP4>(a, stream, gu_ng)
                                                        : launch_gateup<FLINT_MOE_BF16>(a, stream, gu_ng);
