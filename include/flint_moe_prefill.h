@@ -51,8 +51,12 @@ flint_moe_status flint_moe_prefill_workspace_init(const flint_moe_config* cfg, i
  * workspace_bytes >= flint_moe_prefill_workspace_bytes(cfg, B), 256-byte
  * aligned, initialised once with flint_moe_prefill_workspace_init, not shared
  * with another call in flight. Seven kernels in stream order:
- *   1. router GEMM on the tensor cores (bf16 router rows x tokens, FP32);
- *   2. sigmoid top-k per token, counting the tokens of every expert;
+ *   1. router GEMM on the tensor cores (bf16 router rows x tokens, FP32),
+ *      split along H into up to 8 ranges while its tiles are fewer than the
+ *      SMs (the partial sums live in the y region until step 6);
+ *   2. the partial logits added in split order (a fixed order: the result does
+ *      not depend on timing), sigmoid top-k per token, counting the tokens of
+ *      every expert;
  *   3. plan: slots, the first grouped row of every expert, and the (expert,
  *      128-row tile, token tile) work lists;
  *   4. per token: its entries of the expert-grouped row lists, and its row in

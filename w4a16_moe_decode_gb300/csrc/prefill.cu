@@ -10,8 +10,11 @@
 // N = up to 128 tokens, K = 16 per instruction) that accumulate in FP32 in
 // tensor memory. The epilogue reads the accumulators back with tcgen05.ld.
 //
-//   k_pf_gemm<ROUTER>  logits = Wr x^T      (bf16 router rows and tokens by TMA)
-//   k_pf_topk          sigmoid top-k per token; tokens counted per expert
+//   k_pf_gemm<ROUTER>  logits = Wr x^T      (bf16 router rows and tokens by TMA;
+//                      split along H into up to 8 k-ranges while the tiles are
+//                      fewer than the SMs)
+//   k_pf_topk          adds the splits' partial logits in split order; sigmoid
+//                      top-k per token; tokens counted per expert
 //   k_pf_plan          slots, grouped-row bases, tile lists (one block)
 //   k_pf_token_rows    per token: its grouped-list entries, its f16 rows
 //   k_pf_gemm<GATEUP>  h = bf16(silu(G_g g) * G_u u) per (token, expert), f16 MMA
@@ -103,6 +106,11 @@ struct PfArgs {
   const uint16_t* res;     // [B][H]
   const uint16_t* gamma;   // [H]
   float eps;
+  // Router GEMM split along H into rsplit k-ranges (1, 2, 4 or 8): split s
+  // writes its partial logits [B][E] at y + s B E (the expert outputs y are
+  // written only later, by the down GEMM), and k_pf_topk adds the splits in
+  // order and stores the logits.
+  int rsplit;
 };
 
 template <typename T>
@@ -304,11 +312,11 @@ struct TileInfo {
 template <int MODE>
 __device__ __forceinline__ TileInfo tile_info(const PfArgs& a, int tile) {
   TileInfo t;
-  if (MODE == ROUTER) {
-    const int mtc = (a.E + BM - 1) / BM;
-    t.slot = 0;
+  if (MODE == ROUTER) {  // tile = (split * ntc + token tile) * mtc + m-tile; slot = the split
+    const int mtc = (a.E + BM - 1) / BM, ntc = (a.B + NT - 1) / NT;
     t.mt = tile % mtc;
-    t.row0 = (tile / mtc) * NT;
+    t.slot = tile / mtc / ntc;
+    t.row0 = (tile / mtc % ntc) * NT;
     t.n = min(NT, a.B - t.row0);
     t.expert = 0;
   } else {
@@ -338,8 +346,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   volatile int* abort = &G.abort;
 
   const int K = MODE == DOWN ? a.I : a.H;
-  const int KB = K / BK;
-  const int n_tiles = MODE == ROUTER ? ((a.E + BM - 1) / BM) * ((a.B + NT - 1) / NT)
+  const int KB = K / BK / (MODE == ROUTER ? a.rsplit : 1);  // k-blocks per tile
+  const int n_tiles = MODE == ROUTER ? ((a.E + BM - 1) / BM) * ((a.B + NT - 1) / NT) * a.rsplit
                                      : __ldcg(ws_at<int>(a, 0) + (MODE == GATEUP ? PF_NGU : PF_NDN));
   if ((int)blockIdx.x >= n_tiles) return;  // uniform: no tensor memory taken
   const int cta_tiles = (n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -418,7 +426,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
           if (i + 1 < my_tiles) nxt = tile_info<MODE>(a, tile_of(i + 1));
         }
         mbar_arrive_expect_tx(&G.full[p][s], (uint32_t)(MODE == ROUTER ? A_KBLK + B_KBLK : B_KBLK));
-        const int x = kb * BK;
+        const int x = ((MODE == ROUTER ? t.slot * KB : 0) + kb) * BK;
         const uint32_t bdst = b_op + s * B_STAGE;
         if (MODE == ROUTER) {
           tma_load_2d(a_op + s * A_STAGE, &maps.a, x, t.mt * BM, &G.full[p][s]);
@@ -567,7 +575,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
           tc_ld16(tacc + (uint32_t)c0, v);
           if (MODE == ROUTER) {
             const int e = t.mt * BM + r;
-            float* logits = ws_at<float>(a, a.W.logits);
+            float* logits = a.rsplit > 1 ? ws_at<float>(a, a.W.y) + (size_t)t.slot * a.B * a.E : ws_at<float>(a, a.W.logits);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (e < a.E && c0 + j < t.n) logits[(size_t)(t.row0 + c0 + j) * a.E + e] = __uint_as_float(v[j]);
@@ -705,7 +713,8 @@ __global__ void __launch_bounds__(256) k_pf_topk(PfArgs a) {
   const int t = blockIdx.x * 8 + warp;
   if (t >= a.B) return;
   constexpr int PER = MAX_E / 32;
-  const float* logits = ws_at<float>(a, a.W.logits) + (size_t)t * a.E;
+  float* logits = ws_at<float>(a, a.W.logits) + (size_t)t * a.E;
+  const float* part = ws_at<const float>(a, a.W.y) + (size_t)t * a.E;  // split partials (rsplit > 1)
   float s[PER];
   uint32_t key[PER];
   uint32_t taken = 0;
@@ -715,7 +724,14 @@ __global__ void __launch_bounds__(256) k_pf_topk(PfArgs a) {
     s[i] = 0.f;
     key[i] = 0u;
     if (e < a.E) {
-      const float l = __ldcg(logits + e);
+      float l;
+      if (a.rsplit > 1) {  // the splits' partial sums, added in split order
+        l = __ldcg(part + e);
+        for (int q = 1; q < a.rsplit; ++q) l += __ldcg(part + (size_t)q * a.B * a.E + e);
+        logits[e] = l;
+      } else {
+        l = __ldcg(logits + e);
+      }
       s[i] = 1.0f / (1.0f + expf(-l));
       key[i] = order_f32(s[i] + (a.bias ? a.bias[e] : 0.f));
     } else {
@@ -1060,7 +1076,15 @@ static flint_moe_status prefill_impl(const flint_moe_layer* layer, const uint16_
 
   const int nsm = sm_count();
   const int router_tiles = ((a.E + BM - 1) / BM) * ((B + NT - 1) / NT);
-  if (launch_gemm<ROUTER>(a, m_router, std::min(nsm, router_tiles), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
+  // Few router tiles (up to a few hundred tokens) leave most SMs idle and each
+  // tile's k-loop latency-bound: split H so that the tiles fill the SMs, while
+  // every split keeps at least STAGES k-blocks and the partials fit in y.
+  a.rsplit = 1;
+  while (a.rsplit < 8 && router_tiles * a.rsplit * 2 <= nsm && (a.H / BK) % (a.rsplit * 2) == 0 &&
+         a.H / BK / (a.rsplit * 2) >= STAGES && (size_t)a.rsplit * 2 * a.E <= (size_t)(a.S + a.k) * a.H)
+    a.rsplit *= 2;
+  if (launch_gemm<ROUTER>(a, m_router, std::min(nsm, router_tiles * a.rsplit), stream) != cudaSuccess)
+    return FLINT_MOE_ECUDA;
   k_pf_topk<<<(B + 7) / 8, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   k_pf_plan<<<1, PLAN_THREADS, 0, stream>>>(a);
