@@ -254,6 +254,28 @@ def test_routing_weights_sum_to_one():
     assert r.idx.shape == (8, 6) and all(len(set(row)) == 6 for row in r.idx.tolist())
 
 
+def test_routed_scale_with_and_without_renormalisation():
+    """The routed scale multiplies the final weights: after renormalisation a
+    token's weights sum to the scale (a scale applied before renormalising would
+    cancel); without renormalisation each weight is the scale times the sigmoid
+    of its logit, here recomputed from an exact sum, and the experts are the k
+    largest sigmoids found by brute force."""
+    scale = 2.5
+    cfg = _tiny_cfg(top_k=3, routed_scale=scale)
+    x, router = _inputs(cfg, 4, seed=3)
+    r = moe.route(x, router, cfg)
+    assert np.all(np.abs(r.w.astype(np.float64).sum(1) - scale) <= scale * 2 ** -20)
+    cfg_raw = _tiny_cfg(top_k=3, routed_scale=scale, renormalize=False)
+    r_raw = moe.route(x, router, cfg_raw)
+    for t in range(4):
+        sig = [1 / (1 + math.exp(-float(np.float32(math.fsum(float(a) * float(b) for a, b in zip(x[t], router[e]))))))
+               for e in range(cfg.num_experts)]
+        best = sorted(range(cfg.num_experts), key=lambda e: (-sig[e], e))[:3]
+        assert r_raw.idx[t].tolist() == best
+        for j, e in enumerate(best):
+            assert abs(float(r_raw.w[t, j]) - scale * sig[e]) <= scale * 2 ** -21
+
+
 def test_ties_go_to_lower_index():
     cfg = _tiny_cfg(top_k=3)
     x = np.zeros((1, cfg.hidden))            # all logits 0, all scores 0.5
