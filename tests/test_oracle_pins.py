@@ -329,6 +329,49 @@ def test_layer_matches_dense_all_experts_formulation():
     assert np.array_equal(out, dense)
 
 
+def test_expert_applies_each_matrix_scale_to_its_own_product():
+    """One expert with real block scales and three different per-tensor scales
+    (gate 0.75, up 1.25, down 0.5), against torch on the full weights
+    E2M1 * E4M3 * G built here from the codes (E4M3 through torch's float8
+    type): a dropped G_d moves y by its own size, and the gate and up scales
+    swapped move most elements of h by far more than their bf16 rounding."""
+    rng = np.random.default_rng(11)
+    H, I, B = 64, 32, 3
+    # x / 8 (exact) puts g around |g| ~ 2, where SiLU is far from linear, so
+    # silu(G_g g) * G_u u is not symmetric in the two scales
+    x = moe.bf16_bits_to_f64(synth.x_bf16(4, 0, B, H)) / 8
+
+    def rand_matrix(rows, cols, G):
+        elems = rng.integers(0, 16, (rows, cols)).astype(np.uint8)
+        scales = rng.integers(0x28, 0x48, (rows, cols // 16)).astype(np.uint8)
+        return moe.NVFP4Matrix(nvfp4.pack_codes(elems), scales, np.float32(G))
+
+    g, u, d = rand_matrix(I, H, 0.75), rand_matrix(I, H, 1.25), rand_matrix(H, I, 0.5)
+    y = moe.expert(x, (g, u, d))
+
+    E2M1 = torch.tensor([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6], dtype=torch.float64)
+
+    def W(m):
+        q = E2M1[torch.from_numpy(nvfp4.unpack_codes(m.codes).astype(np.int64))]
+        sc = torch.from_numpy(m.scales).view(torch.float8_e4m3fn).double().repeat_interleave(16, dim=1)
+        return q * sc * float(m.G)
+
+    xt = torch.from_numpy(x)
+    gg = (xt @ W(g).T).float().double()
+    uu = (xt @ W(u).T).float().double()
+    h_ref = (torch.nn.functional.silu(gg) * uu).float().to(torch.bfloat16).double()
+    ref = (h_ref @ W(d).T).numpy()
+    h_ref = h_ref.numpy()
+
+    def h_ok(h):  # within one bf16 rounding of the reference, element by element
+        return np.abs(h - h_ref) <= 2 ** -7 * np.abs(h_ref) + 2 ** -40
+
+    assert np.all(h_ok(moe.expert_hidden(x, g, u)))
+    assert np.max(np.abs(y - ref)) <= 2 ** -7 * np.max(np.abs(ref))
+    swapped = moe.expert_hidden(x, moe.NVFP4Matrix(g.codes, g.scales, u.G), moe.NVFP4Matrix(u.codes, u.scales, g.G))
+    assert np.mean(h_ok(swapped)) < 0.5
+
+
 def test_layer_reduces_to_textbook_swiglu():
     """All block scales 1.0 (E4M3 0x38) and G = 1: every weight is an E2M1
     value and the layer is a dense SwiGLU MoE, computed here with torch in
