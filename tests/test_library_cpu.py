@@ -44,6 +44,15 @@ def test_no_oracle_in_product_path():
             assert "import oracle" not in text and "from oracle" not in text, path
 
 
+def test_binding_fails_loudly_without_the_library(monkeypatch):
+    """No fallback: without the compiled library every call path stops with an
+    error that says how to build it."""
+    monkeypatch.setattr(fb, "LIB", os.path.join(os.path.dirname(fb.LIB), "missing", "libflint_moe.so"))
+    monkeypatch.setattr(fb, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        fb.lib()
+
+
 def flint_cfg(**kw):
     return fb.make_config(**kw)
 
