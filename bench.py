@@ -313,7 +313,15 @@ def gpu_arm(args) -> None:
         per_matrix = cfg.inter * cfg.hidden // 2 + cfg.inter * cfg.hidden // 16 + 4
         return cfg.num_experts * cfg.hidden * 2 + (D + cfg.n_shared) * 3 * per_matrix + 2 * B * cfg.hidden * 2
 
-    def timed_graph(pool, xs, outs, ws, B, steps, warmup, sample_clocks=False):
+    def timed_graph(pool, xs, outs, ws, B, steps, warmup, sample_clocks=False, min_ms=100.0):
+        """Times regions of exactly `steps` decodes, each region bracketed by
+        its own CUDA events on the launching stream, back to back until at
+        least `min_ms` of regions (and at least 3) are timed; returns the
+        slowest rank's median region time (ms), the number of regions and the
+        clocks. A region is steps // P replays of the rotation graph (P layers)
+        and one replay of a graph of the remaining steps. One untimed rotation
+        is queued before the first region, so the device is busy while the host
+        enqueues the regions: no event measures host launch latency."""
         stream = torch.cuda.Stream(device=dev)
         stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(stream):
@@ -331,7 +339,15 @@ def gpu_arm(args) -> None:
                 with torch.cuda.graph(tail, stream=stream):
                     for L in range(rem):
                         fb.flint_moe_decode(pool[L].handle, xs[L], B, outs[L], ws, stream)
+
+            def region():
+                for _ in range(steps // P):
+                    cycle.replay()
+                if tail is not None:
+                    tail.replay()
+
             cycle.replay()
+            region()
             stream.synchronize()
             clocks = None
             if sample_clocks:
@@ -343,24 +359,31 @@ def gpu_arm(args) -> None:
                     for _ in range(50):
                         cycle.replay()
                     stream.synchronize()
-            barrier()
+            # the number of regions: enough for min_ms, from one timed region
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            cycle.replay()
             e0.record(stream)
-            for _ in range(steps // P):
-                cycle.replay()
-            if tail is not None:
-                tail.replay()
+            region()
             e1.record(stream)
+            stream.synchronize()
+            n_regions = max(3, min(100000, int(min_ms / max(e0.elapsed_time(e1), 1e-3)) + 1))
+            barrier()
+            events = [torch.cuda.Event(enable_timing=True) for _ in range(n_regions + 1)]
+            cycle.replay()  # run-ahead: the device works while the regions are enqueued
+            events[0].record(stream)
+            for i in range(n_regions):
+                region()
+                events[i + 1].record(stream)
             stream.synchronize()
             barrier()
             if sample_clocks:
                 clocks = sampler.stop()
-        ms = e0.elapsed_time(e1)
+        times = [events[i].elapsed_time(events[i + 1]) for i in range(n_regions)]
         st, bits = fb.flint_moe_read_status(ws, stream)
         if st != fb.OK or bits:
             raise RuntimeError(f"device status {bits} after the timed region")
-        return slowest(ms), clocks
+        return slowest(statistics.median(times)), n_regions, clocks
 
     def isolated(pool, xs, outs, ws, B, reps=40):
         """One layer at a time with L2 flushed before each (256 MB write)."""
@@ -379,14 +402,17 @@ def gpu_arm(args) -> None:
             times.append(e0.elapsed_time(e1) * 1000.0)
         return statistics.median(times)
 
-    def e2e(pool, B, steps):
+    def e2e(pool, B, steps, min_ms=100.0):
         """Through the C ABI with host buffers: each step copies x from pinned
         host memory, decodes, and copies out back to pinned host memory. The
         steps of one rotation (copy in, flint_moe_decode, copy out per layer)
         are captured once into a CUDA graph and replayed, as a serving loop
-        would, so the number is not the Python launch overhead. (Copies on a
-        second stream with double buffers measured no faster: the copy nodes
-        break the programmatic launch chain between layers either way.)"""
+        would, so the number is not the Python launch overhead. Regions of
+        whole rotations are timed back to back (one untimed rotation queued
+        ahead), at least min_ms in all; the median region gives the time per
+        step. (Copies on a second stream with double buffers measured no
+        faster: the copy nodes break the programmatic launch chain between
+        layers either way.)"""
         xh = [layers.synth_x(B, cfg.hidden, args.seed, L, dev).cpu().pin_memory() for L in range(P)]
         oh = [torch.empty(B, cfg.hidden, dtype=torch.int16).pin_memory() for _ in range(P)]
         xd = torch.empty(B, cfg.hidden, dtype=torch.int16, device=dev)
@@ -413,20 +439,45 @@ def gpu_arm(args) -> None:
                     memcpy(oh[L], od, 2)
             for _ in range(3):
                 g.replay()
-            barrier()
-            reps = max(1, steps // P)
+            stream.synchronize()
+            per_region = max(1, steps // P)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            g.replay()
             e0.record(stream)
-            for _ in range(reps):
+            for _ in range(per_region):
                 g.replay()
             e1.record(stream)
+            stream.synchronize()
+            n_regions = max(3, int(min_ms / max(e0.elapsed_time(e1), 1e-3)) + 1)
+            barrier()
+            events = [torch.cuda.Event(enable_timing=True) for _ in range(n_regions + 1)]
+            g.replay()  # run-ahead
+            events[0].record(stream)
+            for i in range(n_regions):
+                for _ in range(per_region):
+                    g.replay()
+                events[i + 1].record(stream)
             stream.synchronize()
         barrier()
         st, bits = fb.flint_moe_read_status(ws)
         if st != fb.OK or bits:
             raise RuntimeError(f"device status {bits} in the end-to-end leg")
-        return job_us_per_layer(slowest(e0.elapsed_time(e1)), reps * P, world)
+        med = statistics.median(events[i].elapsed_time(events[i + 1]) for i in range(n_regions))
+        return job_us_per_layer(slowest(med), per_region * P, world)
+
+    def replay_times(g, stream, n):
+        """Milliseconds of n back-to-back replays of graph g, each between its
+        own events; one untimed replay is queued first so that the device is
+        busy while the host enqueues the rest (no event sees launch latency)."""
+        events = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        g.replay()
+        events[0].record(stream)
+        for i in range(n):
+            g.replay()
+            events[i + 1].record(stream)
+        stream.synchronize()
+        return [events[i].elapsed_time(events[i + 1]) for i in range(n)]
 
     def stack_leg(batches=(1, 2, 4, 8, 16, 32), passes=20):
         """The 47-layer stack: distinct layers (generator seed 1000 + L) as
@@ -466,15 +517,7 @@ def gpu_arm(args) -> None:
                 for _ in range(3):
                     g.replay()
                 stream.synchronize()
-                times = []
-                for _ in range(passes):
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    g.replay()
-                    e1.record(stream)
-                    stream.synchronize()
-                    times.append(e0.elapsed_time(e1))
+                times = replay_times(g, stream, passes)
             us_layer = statistics.median(times) * 1000.0 / P
             ub = statistics.mean(unique_bytes(D, Bs) for D in dl)
             res[str(Bs)] = {"us_per_layer": us_layer, "gbs": ub / (us_layer * 1e-6) / 1e9,
@@ -492,15 +535,7 @@ def gpu_arm(args) -> None:
                     for _ in range(3):
                         gp.replay()
                     stream.synchronize()
-                    times = []
-                    for _ in range(passes):
-                        e0 = torch.cuda.Event(enable_timing=True)
-                        e1 = torch.cuda.Event(enable_timing=True)
-                        e0.record(stream)
-                        gp.replay()
-                        e1.record(stream)
-                        stream.synchronize()
-                        times.append(e0.elapsed_time(e1))
+                    times = replay_times(gp, stream, passes)
                 st, bits = fb.flint_moe_read_status(ws_p)
                 if st != fb.OK or bits:
                     raise RuntimeError(f"device status {bits} in the stack (tensor-core path)")
@@ -700,14 +735,14 @@ def gpu_arm(args) -> None:
     pool, xs, outs, ws = build_pool(B)
     ds = distinct_per_layer(pool, xs, outs, ws, B)
     bytes_per_step = statistics.mean(unique_bytes(D, B) for D in ds)
-    ms, clocks = timed_graph(pool, xs, outs, ws, B, K, W, sample_clocks=True)
+    ms, n_regions, clocks = timed_graph(pool, xs, outs, ws, B, K, W, sample_clocks=True)
     us = job_us_per_layer(ms, K, world)
     us_rank = ms * 1000.0 / K
     gbs = bytes_per_step / (us_rank * 1e-6) / 1e9
     peak, peak_kind = measured_peak_gbs()
-    extra = {}
+    legs, tail_legs = {}, {}
     if not args.quick:
-        extra["isolated_l2_flushed_us"] = isolated(pool, xs, outs, ws, B)
+        legs["isolated_l2_flushed_us"] = isolated(pool, xs, outs, ws, B)
         e2e_us = e2e(pool, B, min(K, 4000))
     else:
         e2e_us = None
@@ -717,18 +752,20 @@ def gpu_arm(args) -> None:
         pool8, xs8, outs8, ws8 = build_pool(8)
         ds8 = distinct_per_layer(pool8, xs8, outs8, ws8, 8)
         b8 = statistics.mean(unique_bytes(D, 8) for D in ds8)
-        ms8, _ = timed_graph(pool8, xs8, outs8, ws8, 8, min(K, 4700), W)
-        us8 = ms8 * 1000.0 / min(K, 4700)
-        extra["batch8"] = {"us_per_layer": us8, "gbs": b8 / (us8 * 1e-6) / 1e9, "frac": b8 / (us8 * 1e-6) / 1e9 / peak,
-                           "mean_distinct_experts": statistics.mean(ds8), "unique_bytes_per_layer": b8,
-                           "isolated_l2_flushed_us": isolated(pool8, xs8, outs8, ws8, 8)}
+        ms8, n8, _ = timed_graph(pool8, xs8, outs8, ws8, 8, K, W)
+        us8 = ms8 * 1000.0 / K
+        tail_legs["batch8"] = {"us_per_layer": us8, "gbs": b8 / (us8 * 1e-6) / 1e9,
+                               "frac": b8 / (us8 * 1e-6) / 1e9 / peak, "mean_distinct_experts": statistics.mean(ds8),
+                               "unique_bytes_per_layer": b8, "regions": n8,
+                               "isolated_l2_flushed_us": isolated(pool8, xs8, outs8, ws8, 8)}
         del pool8, xs8, outs8, ws8
         torch.cuda.empty_cache()
     if not args.quick and B == 1 and world == 1:
-        extra["stack"] = stack_leg()
-        extra["dense_gemv"] = dense_leg()
-        extra["bf16_experts"] = bf16_leg()
-        extra["prefill"] = prefill_leg()
+        legs["prefill"] = prefill_leg()
+        legs["dense_gemv"] = dense_leg()
+        legs["bf16_experts"] = bf16_leg()
+        legs["stack"] = stack_leg()
+        tail_legs["stack_us_per_layer"] = {b: v["us_per_layer"] for b, v in legs["stack"]["per_batch"].items()}
 
     if rank != 0:
         if world > 1:
@@ -751,7 +788,9 @@ def gpu_arm(args) -> None:
         "config": {"workload": WORKLOAD, "batch": B, "layers_in_rotation": P,
                    "l2": f"inputs larger than L2: {P} distinct layers rotated, "
                          f"{P * bytes_per_step / 1e6:.0f} MB touched per rotation",
-                   "launch": "3 kernels per layer, programmatic dependent launch, CUDA graph replay"},
+                   "launch": "3 kernels per layer, programmatic dependent launch, CUDA graph replay",
+                   "timing": f"median over {n_regions} back-to-back regions of exactly {K} steps, each between "
+                             f"its own CUDA events (at least 100 ms timed in all)"},
         "gbs": gbs,
         "unique_bytes_per_layer": bytes_per_step,
         "mean_distinct_experts": statistics.mean(ds),
@@ -762,10 +801,11 @@ def gpu_arm(args) -> None:
         "e2e": None if e2e_us is None else {"value": e2e_us, "unit": "us/layer",
                                             "h2d_bytes_per_step": B * cfg.hidden * 2,
                                             "d2h_bytes_per_step": B * cfg.hidden * 2},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 3 * K * n_regions,
         "cpu_baseline": cpu,
     }
-    line.update(extra)
+    line.update(legs)
+    line.update(tail_legs)  # last, so that a reader of the line's tail sees batch 8 and the stack
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()

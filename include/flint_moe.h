@@ -256,16 +256,20 @@ flint_moe_status flint_moe_read_status(const void* workspace, int32_t* host_stat
  * in this library's device memory, held by every GPU that loads the library
  * until the process exits. It allocates nothing and calls no allocating
  * routine. The first call on a device looks up the array's device address
- * (with that device current); make that first call before any stream capture.
+ * (with that device current); make that first call before any stream capture:
+ * while `stream` is being captured that first call returns FLINT_MOE_EINVAL.
  * Every call shares the array and leaves its contents behind; the call clears
  * what must start at zero. Calls whose work overlaps on the GPU (other streams,
  * other threads) race on the array: serialise them. Returns
  * FLINT_MOE_EUNSUPPORTED when the workspace this shape and batch need
  * (flint_moe_workspace_bytes) exceeds FLINT_MOE_NOALLOC_SCRATCH_BYTES (the
- * Flint-shape layer needs 6.1 MiB at B = 32, 0.40 MiB at B = 8). Device status bits are not
- * reported; use flint_moe_decode with a workspace to read them. */
+ * Flint-shape layer needs 6.1 MiB at B = 32, 0.40 MiB at B = 8), checked before
+ * anything else touches the device. dev_status (device int32, 4-byte aligned,
+ * may be NULL): the device status bits of this call (FLINT_MOE_DEV_ERR_*) are
+ * ORed into it by one more small kernel after the decode. */
 flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* layer, const uint16_t* x_bf16,
-                                          int32_t B, uint16_t* out_bf16, cudaStream_t stream);
+                                          int32_t B, uint16_t* out_bf16, int32_t* dev_status,
+                                          cudaStream_t stream);
 
 /* ---- loading helpers (checkpoint side, off the decode path) ---- */
 

@@ -13,6 +13,22 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: takes more than a few seconds on the CPU")
 
 
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # Worst output error of every oracle comparison: the fixed rule's ratio
+    # and the error in bf16 ulps of the reference.
+    try:
+        from _common import RESULTS
+    except ImportError:  # pragma: no cover
+        return
+    if not RESULTS:
+        return
+    tr = terminalreporter
+    tr.section("output errors against the oracle")
+    tr.write_line(f"{'comparison':56s} {'elements':>9s} {'err/tol':>8s} {'worst ulp':>10s} {'median ulp':>10s}")
+    for label, n, ratio, worst, med in RESULTS:
+        tr.write_line(f"{label[:56]:56s} {n:9d} {ratio:8.3f} {worst:10.2f} {med:10.2f}")
+
+
 def pytest_collection_modifyitems(config, items):
     # GPU tests are skipped, not failed, on a machine without a GPU, unless
     # they were selected explicitly with -m gpu (then they must run).

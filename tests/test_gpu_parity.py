@@ -15,8 +15,8 @@ from w4a16_moe_decode_gb300 import binding as fb
 from w4a16_moe_decode_gb300 import layers
 from w4a16_moe_decode_gb300.build import build
 
-from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, oracle_config, oracle_experts,
-                     oracle_inputs)
+from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, needed_experts, oracle_config,
+                     oracle_experts, oracle_inputs)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -47,6 +47,9 @@ def gpu_decode(cfg, dl, B, seed, layer, ws=None):
 
 
 def run_parity(d, B, seed=0, layer=0, fmt=fb.NVFP4, tokens=None, bias=None, renormalize=True, routed_scale=1.0):
+    """Decode B tokens on the GPU and compare with the oracle: the routing of
+    every token (indices bit-exact, weights within 1e-6, tokens whose key gap is
+    below 1e-6 excluded), and the outputs of `tokens` (default: all)."""
     cfg = cfg_of(d, fmt, renormalize=renormalize, routed_scale=routed_scale)
     bias_t = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).to(DEV)
     dl = layers.synth_layer(cfg, seed, layer, DEV, bias=bias_t)
@@ -55,12 +58,23 @@ def run_parity(d, B, seed=0, layer=0, fmt=fb.NVFP4, tokens=None, bias=None, reno
     assert np.array_equal(bits_to_f64(x), xo)  # both generators drew the same activations
     oc = oracle_config(d, renormalize, routed_scale)
     tokens = list(range(B)) if tokens is None else tokens
-    ref, routing = moe.moe_layer(xo, router, oracle_experts(d, seed, layer, fmt == fb.BF16), oc, bias, tokens)
-    excluded = check_routing(routing, idx, w, tokens)
+    routing = moe.route(xo, router, oc, bias)
+    excluded = check_routing(routing, idx, w)  # every token
+    get = oracle_experts(d, seed, layer, fmt == fb.BF16, prefetch=needed_experts(d, routing, tokens))
+    ref, routing2 = moe.moe_layer(xo, router, get, oc, bias, tokens)
+    assert np.array_equal(routing2.idx, routing.idx)
     keep = [i for i, t in enumerate(tokens) if t not in excluded]
     got = bits_to_f64(out)[tokens]
-    worst = check_out(ref[keep], got[keep], f"B={B} seed={seed}")
+    worst = check_out(ref[keep], got[keep], f"decode {d['hidden']}x{d['num_experts']} B={B} seed={seed}")
     return worst, excluded, routing
+
+
+def tile_samples(B):
+    """Output tokens checked at batch B: all of them up to 8; beyond, two of
+    every 8-token tile (its first and last column) and the batch's last token."""
+    if B <= 8:
+        return list(range(B))
+    return sorted({t for base in range(0, B, 8) for t in (base, min(base + 7, B - 1))} | {B - 1})
 
 
 # ---------------------------------------------------------------- inputs and formats
@@ -158,18 +172,20 @@ def test_decode_flint_batch1():
     assert not excluded
 
 
-def test_decode_flint_batch8_sampled():
-    run_parity(FLINT, 8, seed=0, tokens=[0, 3, 7])
+@pytest.mark.parametrize("B,seed", [(2, 1), (4, 2), (8, 0)])
+def test_decode_flint_every_token(B, seed):
+    """Flint shape at 2, 4 and 8 tokens: every token's routing and output."""
+    run_parity(FLINT, B, seed=seed)
 
 
-def test_decode_flint_batch2_and_4_sampled():
-    run_parity(FLINT, 2, seed=1, tokens=[1])
-    run_parity(FLINT, 4, seed=2, tokens=[0, 2])
+def test_decode_flint_batch32_routing_of_every_token():
+    """32 tokens: every token's routing; outputs of two tokens per 8-token tile."""
+    run_parity(FLINT, 32, seed=5, tokens=tile_samples(32))
 
 
 def test_decode_bf16_weights():
     run_parity(FLINT, 1, seed=0, fmt=fb.BF16)
-    run_parity(FLINT, 8, seed=0, fmt=fb.BF16, tokens=[5])
+    run_parity(FLINT, 8, seed=0, fmt=fb.BF16)
     run_parity(TINY, 5, seed=1, fmt=fb.BF16)
 
 
@@ -232,13 +248,15 @@ def _stack_bias_vector(E=256):
     return b
 
 
-def test_decode_flint_stack_layers_with_selection_bias():
+@pytest.mark.parametrize("B,L", [(1, 0), (2, 1), (4, 2), (8, 3), (32, 46)])
+def test_decode_flint_stack_layers_with_selection_bias(B, L):
     """Layers of the skewed 47-layer stack workload (generator seed 1000 + L,
-    selection bias on experts 0..25) at batch 8 and 32, sampled tokens."""
+    selection bias on experts 0..25): every token's routing; outputs of every
+    token up to 8, of two tokens per 8-token tile at 32."""
     bias = _stack_bias_vector()
-    _, _, routing = run_parity(FLINT, 8, seed=1003, layer=3, bias=bias, tokens=[0, 5])
-    assert (routing.idx < 26).any()
-    run_parity(FLINT, 32, seed=1046, layer=46, bias=bias, tokens=[31])
+    _, _, routing = run_parity(FLINT, B, seed=1000 + L, layer=L, bias=bias, tokens=tile_samples(B))
+    if B >= 4:
+        assert (routing.idx < 26).any()
 
 
 def test_flint_stack_chain_graph_equals_serial():
@@ -295,11 +313,14 @@ def run_parity_prenorm(d, B, seed=0, layer=0, tokens=None, bias=None, inplace=Fa
     gamma = moe.bf16_bits_to_f64(synth.norm_bf16(seed, layer, d["hidden"]))
     assert np.array_equal(bits_to_f64(dl.norm), gamma)
     tokens = list(range(B)) if tokens is None else tokens
-    ref, routing = moe.moe_block(ro, router, oracle_experts(d, seed, layer), oracle_config(d), gamma, 1e-6, bias,
-                                 tokens)
-    excluded = check_routing(routing, idx.cpu().numpy(), w.cpu().numpy(), tokens)
+    oc = oracle_config(d)
+    routing = moe.route(moe.rmsnorm(ro, gamma, 1e-6), router, oc, bias)
+    excluded = check_routing(routing, idx.cpu().numpy(), w.cpu().numpy())  # every token
+    get = oracle_experts(d, seed, layer, prefetch=needed_experts(d, routing, tokens))
+    ref, routing2 = moe.moe_block(ro, router, get, oc, gamma, 1e-6, bias, tokens)
+    assert np.array_equal(routing2.idx, routing.idx)
     keep = [i for i, t in enumerate(tokens) if t not in excluded]
-    check_out(ref[keep], bits_to_f64(out)[tokens][keep], f"prenorm B={B} seed={seed}")
+    check_out(ref[keep], bits_to_f64(out)[tokens][keep], f"decode prenorm {d['hidden']} B={B} seed={seed}")
     return routing
 
 
@@ -310,7 +331,7 @@ def test_decode_prenorm_tiny(B, seed, inplace):
 
 def test_decode_prenorm_flint():
     run_parity_prenorm(FLINT, 1, seed=23)
-    run_parity_prenorm(FLINT, 8, seed=1004, layer=4, tokens=[2, 6], bias=_stack_bias_vector(), inplace=True)
+    run_parity_prenorm(FLINT, 8, seed=1004, layer=4, bias=_stack_bias_vector(), inplace=True)
 
 
 def test_decode_batch0_is_a_noop():

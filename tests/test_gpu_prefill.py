@@ -19,7 +19,8 @@ from w4a16_moe_decode_gb300 import binding as fb
 from w4a16_moe_decode_gb300 import layers
 from w4a16_moe_decode_gb300.build import build
 
-from _common import FLINT, TINY, bits_to_f64, check_out, check_routing, oracle_config, oracle_experts, oracle_inputs
+from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, needed_experts, oracle_config,
+                     oracle_experts, oracle_inputs)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -58,10 +59,12 @@ def run_parity(d, B, seed=0, layer=0, tokens=None, bias=None):
     xo, router = oracle_inputs(d, seed, layer, B)
     assert np.array_equal(bits_to_f64(x), xo)
     tokens = list(range(B)) if tokens is None else tokens
-    ref, routing = moe.moe_layer(xo, router, oracle_experts(d, seed, layer), oracle_config(d), bias, tokens)
-    excluded = check_routing(routing, idx, w, tokens)
+    routing = moe.route(xo, router, oracle_config(d), bias)
+    excluded = check_routing(routing, idx, w)  # every token
+    get = oracle_experts(d, seed, layer, prefetch=needed_experts(d, routing, tokens))
+    ref, _ = moe.moe_layer(xo, router, get, oracle_config(d), bias, tokens)
     keep = [i for i, t in enumerate(tokens) if t not in excluded]
-    worst = check_out(ref[keep], bits_to_f64(out)[tokens][keep], f"prefill B={B} seed={seed}")
+    worst = check_out(ref[keep], bits_to_f64(out)[tokens][keep], f"prefill {d['hidden']} B={B} seed={seed}")
     return worst, excluded, routing
 
 
@@ -86,7 +89,7 @@ def test_prefill_parity_tiny_all_tokens(B):
 @pytest.mark.parametrize("B,tokens", [(1, [0]), (16, [0, 7, 15]), (64, [0, 1, 33, 63]), (300, [0, 128, 299])])
 def test_prefill_parity_flint_sampled(B, tokens):
     worst, excluded, routing = run_parity(FLINT, B, seed=11, tokens=tokens)
-    assert not excluded
+    assert not set(excluded) & set(tokens) and len(excluded) <= max(1, B // 50)
 
 
 def test_prefill_routing_exact_for_every_token_flint():
@@ -139,7 +142,9 @@ def test_prefill_and_decode_agree_at_32_tokens():
     w_d = torch.empty(B, cfg.top_k, dtype=torch.float32, device=DEV)
     fb.flint_moe_debug_routing(cfg, ws, B, idx_d, w_d)
     xo, router = oracle_inputs(d, 8, 0, B)
-    ref, routing = moe.moe_layer(xo, router, oracle_experts(d, 8, 0), oracle_config(d), None, tokens)
+    routing = moe.route(xo, router, oracle_config(d))
+    get = oracle_experts(d, 8, 0, prefetch=needed_experts(d, routing, tokens))
+    ref, _ = moe.moe_layer(xo, router, get, oracle_config(d), None, tokens)
     keep = [i for i, t in enumerate(tokens) if routing.gap[t] >= 1e-6]
     check_out(ref[keep], bits_to_f64(out_p)[tokens][keep], "prefill B=32")
     check_out(ref[keep], bits_to_f64(out_d)[tokens][keep], "decode B=32")
@@ -157,7 +162,9 @@ def test_prefill_parity_at_the_largest_bench_size():
     dl = layers.synth_layer(cfg, 13, 0, DEV)
     x, out, idx, w, _ = gpu_prefill(cfg, dl, B, 13, 0)
     xo, router = oracle_inputs(d, 13, 0, B)
-    ref, routing = moe.moe_layer(xo, router, oracle_experts(d, 13, 0), oracle_config(d), None, tokens)
+    routing = moe.route(xo, router, oracle_config(d))
+    get = oracle_experts(d, 13, 0, prefetch=needed_experts(d, routing, tokens))
+    ref, _ = moe.moe_layer(xo, router, get, oracle_config(d), None, tokens)
     excluded = check_routing(routing, idx, w)  # every token
     assert len(excluded) <= B // 100
     keep = [i for i, t in enumerate(tokens) if t not in excluded]
@@ -185,9 +192,10 @@ def run_prefill_prenorm(d, B, seed, tokens=None, bias=None, inplace=False, scale
     assert np.array_equal(bits_to_f64(r_in), ro)
     gamma = moe.bf16_bits_to_f64(synth.norm_bf16(seed, layer, d["hidden"]))
     tokens = list(range(B)) if tokens is None else tokens
-    ref, routing = moe.moe_block(ro, router, oracle_experts(d, seed, layer), oracle_config(d), gamma, 1e-6, bias,
-                                 tokens)
-    excluded = check_routing(routing, idx.cpu().numpy(), w.cpu().numpy(), tokens)
+    routing = moe.route(moe.rmsnorm(ro, gamma, 1e-6), router, oracle_config(d), bias)
+    excluded = check_routing(routing, idx.cpu().numpy(), w.cpu().numpy())  # every token
+    get = oracle_experts(d, seed, layer, prefetch=needed_experts(d, routing, tokens))
+    ref, _ = moe.moe_block(ro, router, get, oracle_config(d), gamma, 1e-6, bias, tokens)
     keep = [i for i, t in enumerate(tokens) if t not in excluded]
     check_out(ref[keep], bits_to_f64(out)[tokens][keep], f"prefill prenorm B={B} seed={seed}")
     return excluded
@@ -203,4 +211,4 @@ def test_prefill_prenorm_flint_with_stack_bias():
     bias = np.zeros(256, np.float32)
     bias[:26] = np.float32(0.134765625)
     excluded = run_prefill_prenorm(FLINT, 64, seed=1005, layer=5, tokens=[0, 31, 63], bias=bias, inplace=True)
-    assert not excluded
+    assert not set(excluded) & {0, 31, 63} and len(excluded) <= 1

@@ -222,3 +222,20 @@ def test_prefill_rejects_bad_arguments_on_the_host(lib):
 
 def test_wait_timeout_check_validates_on_the_host(lib):
     assert fb.lib().flint_moe_debug_wait_timeout(None, None) == fb.EINVAL
+
+
+def test_noalloc_rejects_a_workspace_beyond_its_scratch(lib):
+    """flint_moe_decode_noalloc checks the workspace a shape needs against its
+    8 MiB scratch array before anything touches the device, so this runs
+    without a GPU (and null tensor pointers are never used)."""
+    big = fb.make_config(hidden=8192, num_experts=512, top_k=16, inter=4096)
+    assert fb.flint_moe_workspace_bytes(big, 32) > (8 << 20)
+    layer = fb.flint_moe_layer()
+    layer.cfg = big
+    st = lib.flint_moe_decode_noalloc(ctypes.byref(layer), None, 32, None, None, None)
+    assert st == fb.EUNSUPPORTED
+    # the Flint shape fits at every batch up to 32, so only null pointers stop it
+    flint = fb.make_config()
+    assert fb.flint_moe_workspace_bytes(flint, 32) <= (8 << 20)
+    layer.cfg = flint
+    assert lib.flint_moe_decode_noalloc(ctypes.byref(layer), None, 32, None, None, None) == fb.EINVAL

@@ -499,6 +499,63 @@ def test_moe_block_with_zero_experts_is_the_identity():
     assert np.array_equal(routing.idx, moe.route(moe.rmsnorm(r, g, 1e-6), router, cfg).idx)
 
 
+def test_moe_block_adds_the_rounded_layer_output_to_the_residual():
+    """The pre-norm block with non-zero experts, computed independently with
+    torch in float64: RMSNorm by torch's rms_norm, the layer as a textbook
+    dense SwiGLU MoE with every expert routed (k = E, block scales 2^-4, G = 1,
+    so every weight is an E2M1 value / 16), and r' = bf16(r + bf16(layer)).
+    The two agree element by element except where the two float64 sums round
+    differently (a few percent of elements, by one bf16 ulp). Rounding r + acc
+    only once, or subtracting the layer output, would differ from the torch
+    block in far more elements; the test checks that it can tell."""
+    H, I, E = 64, 32, 4
+    cfg = moe.Config(hidden=H, num_experts=E, top_k=E, inter=I, n_shared=1)
+    rng = np.random.default_rng(17)
+    B = 6
+    r = moe.bf16_bits_to_f64(synth.x_bf16(13, 0, B, H))
+    router = moe.bf16_bits_to_f64(synth.router_bf16(13, 0, E, H))
+    gamma = moe.bf16_bits_to_f64(synth.norm_bf16(13, 0, H))
+    eps = 1e-6
+
+    def rand_matrix(rows, cols):
+        elems = rng.integers(0, 16, (rows, cols)).astype(np.uint8)
+        return moe.NVFP4Matrix(nvfp4.pack_codes(elems), np.full((rows, cols // 16), 0x18, np.uint8), np.float32(1.0))
+
+    mats = {e: (rand_matrix(I, H), rand_matrix(I, H), rand_matrix(H, I)) for e in range(E + 1)}
+    out_o, _ = moe.moe_block(r, router, lambda e: mats[e], cfg, gamma, eps)
+
+    E2M1 = torch.tensor([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6], dtype=torch.float64)
+
+    def W(m):
+        return E2M1[torch.from_numpy(nvfp4.unpack_codes(m.codes).astype(np.int64))] / 16.0
+
+    def bf16(t):
+        return t.float().to(torch.bfloat16).double()
+
+    rt = torch.from_numpy(r)
+    xt = bf16(torch.nn.functional.rms_norm(rt, (H,), weight=torch.from_numpy(gamma), eps=eps))
+    s = torch.sigmoid((xt @ torch.from_numpy(router).T).float().double()).float().double()
+    wts = (s / s.sum(1, keepdim=True)).float().double()
+    acc = torch.zeros(B, H, dtype=torch.float64)
+    for e in range(E + 1):
+        g, u, d = mats[e]
+        gg = (xt @ W(g).T).float().double()
+        uu = (xt @ W(u).T).float().double()
+        h = bf16(torch.nn.functional.silu(gg) * uu)
+        acc += (wts[:, e:e + 1] if e < E else 1.0) * (h @ W(d).T)
+    block = bf16(rt + bf16(acc)).numpy()
+    once = bf16(rt + acc).numpy()          # the residual add without rounding the layer output first
+    minus = bf16(rt - bf16(acc)).numpy()   # the layer output subtracted
+
+    assert np.abs(bf16(acc).numpy()).max() > 0.5      # the layer output is of the residual's size
+    ulp = np.abs(block) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(out_o - block) <= ulp)
+    agree = np.mean(out_o == block)
+    assert agree > 0.97
+    assert np.mean(once == block) < agree - 0.05       # a single rounding would be seen
+    assert np.mean(minus == block) < 0.2
+
+
 # ------------------------------------------------------------------ dense GEMV
 
 def _dense_matrix(seed, N, K):

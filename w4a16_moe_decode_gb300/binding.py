@@ -80,7 +80,8 @@ def lib() -> ctypes.CDLL:
             "flint_moe_layer_set_norm": (c_int32, [P(flint_moe_layer), c_void_p, ctypes.c_float]),
             "flint_moe_decode_prenorm": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p,
                                                    c_void_p]),
-            "flint_moe_decode_noalloc": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p]),
+            "flint_moe_decode_noalloc": (c_int32, [P(flint_moe_layer), c_void_p, c_int32, c_void_p, c_void_p,
+                                                   c_void_p]),
             "flint_moe_debug_routing": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_void_p, c_void_p, c_void_p]),
             "flint_moe_debug_dequant": (c_int32, [P(flint_moe_config), c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
             "flint_moe_read_status": (c_int32, [c_void_p, P(c_int32), c_void_p]),
@@ -211,11 +212,12 @@ def flint_moe_decode_prenorm(layer: flint_moe_layer, residual_in, B: int, residu
                                                                       _stream(stream)))
 
 
-def flint_moe_decode_noalloc(layer: flint_moe_layer, x, B: int, out, stream=None) -> None:
+def flint_moe_decode_noalloc(layer: flint_moe_layer, x, B: int, out, dev_status=None, stream=None) -> None:
     """flint_moe_decode with the library's own 8 MiB device scratch array in
-    place of a workspace, for callers that cannot allocate device memory."""
+    place of a workspace, for callers that cannot allocate device memory.
+    dev_status (int32 device tensor, optional) receives the device status bits."""
     _check("flint_moe_decode_noalloc", lib().flint_moe_decode_noalloc(ctypes.byref(layer), _ptr(x), B, _ptr(out),
-                                                                      _stream(stream)))
+                                                                      _ptr(dev_status), _stream(stream)))
 
 
 def flint_moe_prefill_workspace_bytes(cfg: flint_moe_config, max_tokens: int) -> int:

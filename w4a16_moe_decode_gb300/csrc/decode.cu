@@ -538,11 +538,12 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
             float part = 0.f;
 #pragma unroll
             for (int c = 0; c < NCH; ++c) part = sumsq8(lds128(row + (lane + 32 * c) * 16), part);
-            const float inv = rms_inv(part, a.H, a.eps);
+            float pre;
+            const float inv = rms_factor(part, a.H, a.eps, row, true, lane, pre);
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
               const int off = (lane + 32 * c) * 16;
-              *reinterpret_cast<uint4*>(row + off) = norm8(lds128(row + off), lds128(gsm + off), inv);
+              *reinterpret_cast<uint4*>(row + off) = norm8p(lds128(row + off), lds128(gsm + off), pre, inv);
             }
           }
           __syncthreads();
@@ -716,10 +717,11 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const u
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           if (c < nch) part = sumsq8(v[c], part);
-        const float inv = rms_inv(part, K, eps);
+        float pre;
+        const float inv = rms_factor(part, K, eps, src, false, lane, pre);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          if (c < nch) v[c] = norm8(v[c], wv[c], inv);
+          if (c < nch) v[c] = norm8p(v[c], wv[c], pre, inv);
       }
       if (FMT == FLINT_MOE_NVFP4) {
 #pragma unroll
@@ -732,15 +734,15 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const u
       for (int c = 0; c < 8; ++c)
         if (c < nch) store(v[c], c, sc);
     } else {
-      float inv = 1.f;
+      float inv = 1.f, pre = 1.f;
       if (prenorm) {
         float part = 0.f;
         for (int c = 0; c < nch; ++c) part = sumsq8(ld_cg_v4(src + (lane + 32 * c) * 16), part);
-        inv = rms_inv(part, K, eps);
+        inv = rms_factor(part, K, eps, src, false, lane, pre);
       }
       auto chunk = [&](int c) {
         const uint4 u = ld_cg_v4(src + (lane + 32 * c) * 16);
-        return prenorm ? norm8(u, __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), inv) : u;
+        return prenorm ? norm8p(u, __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), pre, inv) : u;
       };
       if (FMT == FLINT_MOE_NVFP4) {
         for (int c = 0; c < nch; ++c) mx = absmax(chunk(c), mx);
@@ -2047,12 +2049,17 @@ std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device. The host-side
-// symbol is only a stand-in; the address is looked up once per device.
-flint_moe_status noalloc_scratch(void** out) {
+// symbol is only a stand-in; the address is looked up once per device. The
+// lookup is not a stream operation, so it is refused (EINVAL) while `stream`
+// is being captured into a CUDA graph.
+flint_moe_status noalloc_scratch(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FLINT_MOE_ECUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   if (!g_noalloc_ptr[dev]) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return FLINT_MOE_ECUDA;
+    if (cap != cudaStreamCaptureStatusNone) return FLINT_MOE_EINVAL;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return FLINT_MOE_ECUDA;
     g_noalloc_ptr[dev] = p;
@@ -2061,10 +2068,19 @@ flint_moe_status noalloc_scratch(void** out) {
   return FLINT_MOE_OK;
 }
 
+// Moves the status word of the scratch header into the caller's word (OR),
+// then clears it. Device code names the array directly.
+__global__ void k_noalloc_status(int32_t* dev_status) {
+  int* hdr = reinterpret_cast<int*>(g_noalloc_scratch);
+  const int v = hdr[HDR_STATUS];
+  if (v) atomicOr(dev_status, v);
+  hdr[HDR_STATUS] = 0;
+}
+
 }  // namespace
 
 extern "C" flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* layer, const uint16_t* x, int32_t B,
-                                                     uint16_t* out, cudaStream_t stream) {
+                                                     uint16_t* out, int32_t* dev_status, cudaStream_t stream) {
   if (!layer) return FLINT_MOE_EINVAL;
   const flint_moe_config* c = &layer->cfg;
   const flint_moe_status st = flint_moe_check_config(c);
@@ -2074,11 +2090,15 @@ extern "C" flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* laye
   if (make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, B).total >
       FLINT_MOE_NOALLOC_SCRATCH_BYTES)
     return FLINT_MOE_EUNSUPPORTED;
+  if (!x || !out) return FLINT_MOE_EINVAL;
+  if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3)) return FLINT_MOE_EALIGN;
   void* scratch = nullptr;
-  const flint_moe_status sst = noalloc_scratch(&scratch);
+  const flint_moe_status sst = noalloc_scratch(stream, &scratch);
   if (sst != FLINT_MOE_OK) return sst;
-  // The routing counter must start at zero; the status word is not reported
-  // by this entry point, so both header words are cleared on every call.
+  // The header (routing counter, status word) must start at zero.
   if (cudaMemsetAsync(scratch, 0, 256, stream) != cudaSuccess) return FLINT_MOE_ECUDA;
-  return flint_moe_decode(layer, x, B, out, scratch, stream);
+  const flint_moe_status dst = flint_moe_decode(layer, x, B, out, scratch, stream);
+  if (dst != FLINT_MOE_OK || !dev_status) return dst;
+  k_noalloc_status<<<1, 1, 0, stream>>>(dev_status);
+  return cudaGetLastError() == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
 }
