@@ -402,17 +402,19 @@ def gpu_arm(args) -> None:
             times.append(e0.elapsed_time(e1) * 1000.0)
         return statistics.median(times)
 
-    def e2e(pool, B, steps, min_ms=100.0):
-        """Through the C ABI with host buffers: each step copies x from pinned
-        host memory, decodes, and copies out back to pinned host memory. The
-        steps of one rotation (copy in, flint_moe_decode, copy out per layer)
-        are captured once into a CUDA graph and replayed, as a serving loop
-        would, so the number is not the Python launch overhead. Regions of
-        whole rotations are timed back to back (one untimed rotation queued
-        ahead), at least min_ms in all; the median region gives the time per
-        step. (Copies on a second stream with double buffers measured no
-        faster: the copy nodes break the programmatic launch chain between
-        layers either way.)"""
+    def e2e(pool, B, steps, mapped, min_ms=100.0):
+        """Through the C ABI with host buffers: every step's x comes from pinned
+        host memory and its out goes back to pinned host memory. With mapped,
+        flint_moe_decode is given the pinned host buffers themselves and its
+        kernels read x and write out across NVLink-C2C (the same bytes cross
+        the link, with no copy-engine operation and no break in the
+        programmatic-launch chain between steps); otherwise each step is a
+        cudaMemcpyAsync of x, the decode on device buffers and a cudaMemcpyAsync
+        of out. The steps of one rotation are captured once into a CUDA graph
+        and replayed, as a serving loop would, so the number is not the Python
+        launch overhead. Regions of whole rotations are timed back to back (one
+        untimed rotation queued ahead), at least min_ms in all; the median
+        region gives the time per step."""
         xh = [layers.synth_x(B, cfg.hidden, args.seed, L, dev).cpu().pin_memory() for L in range(P)]
         oh = [torch.empty(B, cfg.hidden, dtype=torch.int16).pin_memory() for _ in range(P)]
         xd = torch.empty(B, cfg.hidden, dtype=torch.int16, device=dev)
@@ -434,9 +436,12 @@ def gpu_arm(args) -> None:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for L in range(P):
-                    memcpy(xd, xh[L], 1)
-                    fb.flint_moe_decode(pool[L].handle, xd, B, od, ws, stream)
-                    memcpy(oh[L], od, 2)
+                    if mapped:
+                        fb.flint_moe_decode(pool[L].handle, xh[L], B, oh[L], ws, stream)
+                    else:
+                        memcpy(xd, xh[L], 1)
+                        fb.flint_moe_decode(pool[L].handle, xd, B, od, ws, stream)
+                        memcpy(oh[L], od, 2)
             for _ in range(3):
                 g.replay()
             stream.synchronize()
@@ -743,7 +748,8 @@ def gpu_arm(args) -> None:
     legs, tail_legs = {}, {}
     if not args.quick:
         legs["isolated_l2_flushed_us"] = isolated(pool, xs, outs, ws, B)
-        e2e_us = e2e(pool, B, min(K, 4000))
+        e2e_us = e2e(pool, B, min(K, 4000), mapped=True)
+        legs["e2e_copy_engine_us"] = e2e(pool, B, min(K, 4000), mapped=False)
     else:
         e2e_us = None
     del pool, xs, outs, ws
@@ -800,7 +806,10 @@ def gpu_arm(args) -> None:
         "clocks": clocks,
         "e2e": None if e2e_us is None else {"value": e2e_us, "unit": "us/layer",
                                             "h2d_bytes_per_step": B * cfg.hidden * 2,
-                                            "d2h_bytes_per_step": B * cfg.hidden * 2},
+                                            "d2h_bytes_per_step": B * cfg.hidden * 2,
+                                            "transfer": "x read and out written in pinned host memory by the "
+                                                        "decode kernels over NVLink-C2C (no copy-engine operation); "
+                                                        "the copy-engine variant is e2e_copy_engine_us"},
         "gpu_launches": 3 * K * n_regions,
         "cpu_baseline": cpu,
     }

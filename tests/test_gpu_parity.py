@@ -395,3 +395,27 @@ def test_bounded_wait_gives_up_and_reports():
     assert int(status.item()) & 0x1  # FLINT_MOE_DEV_ERR_TIMEOUT
     assert time.time() - t0 < 10.0
     worst, excluded, _ = run_parity(TINY, 3, seed=5)  # the GPU still decodes correctly
+
+
+@pytest.mark.parametrize("d,B,prenorm", [(TINY, 3, False), (FLINT, 1, False), (FLINT, 8, False), (FLINT, 4, True)])
+def test_decode_with_x_and_out_in_pinned_host_memory(d, B, prenorm):
+    """x and out in pinned host memory (the kernels read and write them across
+    the host link): bit-identical to the same decode on device buffers, with
+    the pre-norm block updating the residual stream in host memory in place."""
+    cfg = cfg_of(d)
+    dl = layers.synth_layer(cfg, 41, 0, DEV, norm_eps=1e-6 if prenorm else None)
+    ws = layers.workspace(cfg, B, DEV)
+    x = layers.synth_x(B, cfg.hidden, 41, 0, DEV)
+    ref = torch.empty_like(x)
+    call = fb.flint_moe_decode_prenorm if prenorm else fb.flint_moe_decode
+    call(dl.handle, x, B, ref, ws)
+    xh = x.cpu().pin_memory()
+    oh = xh if prenorm else torch.full((B, cfg.hidden), 0x7FC0, dtype=torch.int16).pin_memory()
+    call(dl.handle, xh, B, oh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref.cpu())
+    st, bits = fb.flint_moe_read_status(ws)
+    assert st == fb.OK and bits == 0
+    unpinned = torch.zeros(B, cfg.hidden, dtype=torch.int16)  # ordinary host memory: refused before any launch
+    with pytest.raises(fb.FlintMoeError):
+        call(dl.handle, unpinned, B, ref, ws)

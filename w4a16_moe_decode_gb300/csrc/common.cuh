@@ -349,7 +349,8 @@ __device__ __forceinline__ float warp_max(float v) {
 // activations: lane l owns the 16-byte chunks l, l + 32, ... of a row; its sum
 // of squares runs over them in that order, the warp total is a butterfly (the
 // same value in every lane), then 1 / sqrt(mean + eps) with IEEE square root
-// and division (rms_factor), and each value becomes bf16((x * inv) * w).
+// and division, and each value becomes bf16((x * inv) * w); a row whose sum
+// of squares overflows FP32 takes the scaled path below.
 __device__ __forceinline__ float sumsq8(const uint4 u, float acc) {
   acc = fmaf(bf16lo(u.x), bf16lo(u.x), acc);
   acc = fmaf(bf16hi(u.x), bf16hi(u.x), acc);
@@ -362,6 +363,7 @@ __device__ __forceinline__ float sumsq8(const uint4 u, float acc) {
   return acc;
 }
 
+
 __device__ __forceinline__ uint32_t norm2(uint32_t x, uint32_t w, float inv) {
   const __nv_bfloat162 r = __floats2bfloat162_rn((bf16lo(x) * inv) * bf16lo(w), (bf16hi(x) * inv) * bf16hi(w));
   return *reinterpret_cast<const uint32_t*>(&r);
@@ -371,11 +373,15 @@ __device__ __forceinline__ uint4 norm8(const uint4 x, const uint4 w, float inv) 
   return make_uint4(norm2(x.x, w.x, inv), norm2(x.y, w.y, inv), norm2(x.z, w.z, inv), norm2(x.w, w.w, inv));
 }
 
-// Rows whose sum of squares overflows FP32 (|r| beyond about 2^58: bf16
+// Largest finite FP32 value: a warp's sum of squares above it has overflowed.
+constexpr float FP32_MAX = 3.40282347e38f;
+
+// Rows whose sum of squares overflows FP32 (|r| beyond about 2^58; bf16
 // reaches 2^128). Such a row is first scaled by an exact power of two
 // pre = 2^-e (e from its largest magnitude), so that
 //   1 / sqrt(mean(r^2) + eps) = pre / sqrt(mean((pre r)^2) + pre^2 eps)
-// is computed from a finite sum, and each value becomes bf16(((r pre) inv) w).
+// comes from a finite sum; each value becomes bf16(((r pre) inv) w). This path
+// is out of line, so the common one carries none of its code.
 __device__ __forceinline__ float absmax8(const uint4 u, float m) {
   const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -383,25 +389,13 @@ __device__ __forceinline__ float absmax8(const uint4 u, float m) {
   return m;
 }
 
-__device__ __forceinline__ float sumsq8_scaled(const uint4 u, float pre, float acc) {
-  const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float a = bf16lo(w4[q]) * pre, b = bf16hi(w4[q]) * pre;
-    acc = fmaf(a, a, acc);
-    acc = fmaf(b, b, acc);
-  }
-  return acc;
-}
-
-// The factor (x) and the scale (y) of a row whose sum of squares overflowed.
-// Lane l re-reads its 16-byte chunks l, l + 32, ... of the row (nch = H / 256),
-// from shared memory or, written by an earlier kernel, through L2; the loops
-// stay rolled so that this rare path adds no registers to the common one.
-__device__ __forceinline__ float2 rms_factor_scaled(const uint8_t* row, bool row_in_smem, int lane, int H, float eps) {
+// The factor inv (x) and the scale pre (y) of such a row: lane l re-reads its
+// 16-byte chunks l, l + 32, ... (H / 256 of them) from shared memory or,
+// written by an earlier kernel, through L2.
+static __device__ __noinline__ float2 rms_factor_huge(const uint8_t* row, int row_in_smem, int lane, int H,
+                                                      float eps) {
   const int nch = H / 256;
   float m = 0.f;
-#pragma unroll 1
   for (int c = 0; c < nch; ++c) {
     const uint8_t* p = row + (lane + 32 * c) * 16;
     m = absmax8(row_in_smem ? lds128(p) : ld_cg_v4(p), m);
@@ -411,44 +405,30 @@ __device__ __forceinline__ float2 rms_factor_scaled(const uint8_t* row, bool row
   e = e < 0 ? 0 : (e > 120 ? 120 : e);
   const float pre = exp2i(-e);
   float acc = 0.f;
-#pragma unroll 1
   for (int c = 0; c < nch; ++c) {
     const uint8_t* p = row + (lane + 32 * c) * 16;
-    acc = sumsq8_scaled(row_in_smem ? lds128(p) : ld_cg_v4(p), pre, acc);
+    const uint4 u = row_in_smem ? lds128(p) : ld_cg_v4(p);
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+    for (int q = 0; q < 4; ++q) {
+      const float a = bf16lo(w4[q]) * pre, b = bf16hi(w4[q]) * pre;
+      acc = fmaf(a, a, acc);
+      acc = fmaf(b, b, acc);
+    }
   }
   const float ss = warp_sum(acc);
   return make_float2(1.0f / sqrtf(ss / (float)H + (eps * pre) * pre), pre);
 }
 
-// The RMSNorm factor of one row held by a warp (lane l owns the row's 16-byte
-// chunks l, l + 32, ...; `part` is its sum of squares over them, sumsq8 in
-// chunk order). Returns inv and sets pre: pre = 1 on the common path, where
-// inv is 1 / sqrt(mean(r^2) + eps) in FP32; otherwise the power-of-two scale
-// above. The branch is uniform across the warp (the sum is a butterfly).
-__device__ __forceinline__ float rms_factor(float part, int H, float eps, const void* row, bool row_in_smem, int lane,
-                                            float& pre) {
-  const float ss = warp_sum(part);
-  if (ss <= 3.40282347e38f) {
-    pre = 1.0f;
-    return 1.0f / sqrtf(ss / (float)H + eps);
+// One chunk of such a row, normalised with f = rms_factor_huge(...).
+static __device__ __noinline__ uint4 norm8_huge(const uint4 x, const uint4 w, const float2 f) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ws[4] = {w.x, w.y, w.z, w.w};
+  uint32_t o[4];
+  for (int q = 0; q < 4; ++q) {
+    const __nv_bfloat162 r = __floats2bfloat162_rn(((bf16lo(xs[q]) * f.y) * f.x) * bf16lo(ws[q]),
+                                                   ((bf16hi(xs[q]) * f.y) * f.x) * bf16hi(ws[q]));
+    o[q] = *reinterpret_cast<const uint32_t*>(&r);
   }
-  const float2 r = rms_factor_scaled(static_cast<const uint8_t*>(row), row_in_smem, lane, H, eps);
-  pre = r.y;
-  return r.x;
-}
-
-__device__ __forceinline__ uint32_t norm2s(uint32_t x, uint32_t w, float pre, float inv) {
-  const __nv_bfloat162 r = __floats2bfloat162_rn(((bf16lo(x) * pre) * inv) * bf16lo(w),
-                                                 ((bf16hi(x) * pre) * inv) * bf16hi(w));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// One normalised chunk: norm8 on the common path (pre == 1), else with the
-// row's power-of-two prescale applied first.
-__device__ __forceinline__ uint4 norm8p(const uint4 x, const uint4 w, float pre, float inv) {
-  if (pre == 1.0f) return norm8(x, w, inv);
-  return make_uint4(norm2s(x.x, w.x, pre, inv), norm2s(x.y, w.y, pre, inv), norm2s(x.z, w.z, pre, inv),
-                    norm2s(x.w, w.w, pre, inv));
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 

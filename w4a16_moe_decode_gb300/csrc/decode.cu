@@ -59,6 +59,7 @@ struct DecodeArgs {
   const uint16_t* gamma;
   float eps;
   int router_epb;  // experts per router block (4, 2 or 1): the block's 4 warps split its tokens
+  int x_host;      // x is pinned host memory: the router reads it with plain loads, not a bulk copy
   int dn_nbuf;     // down tiles in flight per warp
   int dn_hcap;     // h rows the down kernel stages at a time
 };
@@ -475,6 +476,12 @@ __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* 
   }
 }
 
+// n 16-byte words from src (global or pinned host memory) to shared memory,
+// by the threads of the block; out of line, off the device-memory path.
+static __device__ __noinline__ void load_rows_plain(uint8_t* dst, const uint8_t* src, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) reinterpret_cast<uint4*>(dst)[i] = ld_cg_v4(src + (size_t)i * 16);
+}
+
 template <int NCH>
 __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t dsm[];  // router rows [4][H], norm weight [H], x chunk [<= 8][H]
@@ -523,14 +530,19 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
     for (int t0 = 0; t0 < a.B; t0 += 8) {
       const int nt = min(8, a.B - t0);
       if (!dry) {
-        if (threadIdx.x == 0) {
-          const uint32_t bytes = (uint32_t)nt * a.H * 2;
-          mbar_arrive_expect_tx(&bars[1], bytes);
-          bulk_g2s(xsm, a.x + (size_t)t0 * a.H, bytes, &bars[1]);
+        if (a.x_host) {  // x in pinned host memory: 16-byte loads across the host link
+          load_rows_plain(xsm, reinterpret_cast<const uint8_t*>(a.x + (size_t)t0 * a.H), nt * a.H / 8);
+          __syncthreads();
+        } else {
+          if (threadIdx.x == 0) {
+            const uint32_t bytes = (uint32_t)nt * a.H * 2;
+            mbar_arrive_expect_tx(&bars[1], bytes);
+            bulk_g2s(xsm, a.x + (size_t)t0 * a.H, bytes, &bars[1]);
+          }
+          ok = __syncthreads_and(mbar_wait(&bars[1], phase, status));  // block-uniform
+          phase ^= 1;
+          if (!ok) break;
         }
-        ok = __syncthreads_and(mbar_wait(&bars[1], phase, status));  // block-uniform
-        phase ^= 1;
-        if (!ok) break;
         FLINT_TRACE(a, 2);
         if (a.prenorm) {  // RMSNorm of the chunk's rows, in place
           for (int t = warp; t < nt; t += 4) {
@@ -538,12 +550,20 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
             float part = 0.f;
 #pragma unroll
             for (int c = 0; c < NCH; ++c) part = sumsq8(lds128(row + (lane + 32 * c) * 16), part);
-            float pre;
-            const float inv = rms_factor(part, a.H, a.eps, row, true, lane, pre);
+            const float ss = warp_sum(part);
+            if (ss <= FP32_MAX) {
+              const float inv = 1.0f / sqrtf(ss / (float)a.H + a.eps);
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-              const int off = (lane + 32 * c) * 16;
-              *reinterpret_cast<uint4*>(row + off) = norm8p(lds128(row + off), lds128(gsm + off), pre, inv);
+              for (int c = 0; c < NCH; ++c) {
+                const int off = (lane + 32 * c) * 16;
+                *reinterpret_cast<uint4*>(row + off) = norm8(lds128(row + off), lds128(gsm + off), inv);
+              }
+            } else {  // the sum of squares overflowed: the scaled path (the whole row is read first)
+              const float2 f = rms_factor_huge(row, 1, lane, a.H, a.eps);
+              for (int c = 0; c < NCH; ++c) {
+                const int off = (lane + 32 * c) * 16;
+                *reinterpret_cast<uint4*>(row + off) = norm8_huge(lds128(row + off), lds128(gsm + off), f);
+              }
             }
           }
           __syncthreads();
@@ -717,11 +737,18 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const u
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           if (c < nch) part = sumsq8(v[c], part);
-        float pre;
-        const float inv = rms_factor(part, K, eps, src, false, lane, pre);
+        const float ss = warp_sum(part);
+        if (ss <= FP32_MAX) {
+          const float inv = 1.0f / sqrtf(ss / (float)K + eps);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < nch) v[c] = norm8p(v[c], wv[c], pre, inv);
+          for (int c = 0; c < 8; ++c)
+            if (c < nch) v[c] = norm8(v[c], wv[c], inv);
+        } else {  // the sum of squares overflowed: the scaled path
+          const float2 f = rms_factor_huge(src, 0, lane, K, eps);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (c < nch) v[c] = norm8_huge(v[c], wv[c], f);
+        }
       }
       if (FMT == FLINT_MOE_NVFP4) {
 #pragma unroll
@@ -734,15 +761,22 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const u
       for (int c = 0; c < 8; ++c)
         if (c < nch) store(v[c], c, sc);
     } else {
-      float inv = 1.f, pre = 1.f;
+      float inv = 1.f;
+      float2 huge = make_float2(0.f, 0.f);  // the scaled path's factor and scale, if taken (y != 0)
       if (prenorm) {
         float part = 0.f;
         for (int c = 0; c < nch; ++c) part = sumsq8(ld_cg_v4(src + (lane + 32 * c) * 16), part);
-        inv = rms_factor(part, K, eps, src, false, lane, pre);
+        const float ss = warp_sum(part);
+        if (ss <= FP32_MAX)
+          inv = 1.0f / sqrtf(ss / (float)K + eps);
+        else
+          huge = rms_factor_huge(src, 0, lane, K, eps);
       }
       auto chunk = [&](int c) {
         const uint4 u = ld_cg_v4(src + (lane + 32 * c) * 16);
-        return prenorm ? norm8p(u, __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), pre, inv) : u;
+        if (!prenorm) return u;
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16));
+        return huge.y == 0.f ? norm8(u, w, inv) : norm8_huge(u, w, huge);
       };
       if (FMT == FLINT_MOE_NVFP4) {
         for (int c = 0; c < nch; ++c) mx = absmax(chunk(c), mx);
@@ -1833,6 +1867,19 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   a.W = make_ws_layout(a.H, a.E, a.k, a.I, a.S, B);
   a.prenorm = prenorm ? 1 : 0;
   a.router_epb = router_epb(B);
+  // x and out may be device memory or pinned (device-mapped) host memory;
+  // memory the device cannot address is refused before any launch.
+  {
+    cudaPointerAttributes px, po;
+    if (cudaPointerGetAttributes(&px, x) != cudaSuccess || cudaPointerGetAttributes(&po, out) != cudaSuccess)
+      return FLINT_MOE_EINVAL;
+    auto addressable = [](const cudaPointerAttributes& p) {
+      return p.type == cudaMemoryTypeDevice || p.type == cudaMemoryTypeManaged ||
+             (p.type == cudaMemoryTypeHost && p.devicePointer == p.hostPointer);
+    };
+    if (!addressable(px) || !addressable(po)) return FLINT_MOE_EINVAL;
+    a.x_host = px.type == cudaMemoryTypeHost ? 1 : 0;
+  }
   a.gamma = prenorm ? layer->norm_weight : nullptr;
   a.eps = prenorm ? layer->norm_eps : 0.f;
   if (prenorm && !aligned16(a.gamma)) return FLINT_MOE_EALIGN;

@@ -877,10 +877,15 @@ __global__ void __launch_bounds__(256) k_pf_norm(PfArgs a) {
   const int nch = a.H / 256;  // 16-byte chunks per lane
   float part = 0.f;
   for (int c = 0; c < nch; ++c) part = sumsq8(__ldg(r + lane + 32 * c), part);
-  float pre;
-  const float inv = rms_factor(part, a.H, a.eps, r, false, lane, pre);
-  for (int c = 0; c < nch; ++c)
-    xn[lane + 32 * c] = norm8p(__ldg(r + lane + 32 * c), __ldg(w + lane + 32 * c), pre, inv);
+  const float ss = warp_sum(part);
+  if (ss <= FP32_MAX) {
+    const float inv = 1.0f / sqrtf(ss / (float)a.H + a.eps);
+    for (int c = 0; c < nch; ++c) xn[lane + 32 * c] = norm8(__ldg(r + lane + 32 * c), __ldg(w + lane + 32 * c), inv);
+  } else {  // the sum of squares overflowed: the scaled path
+    const float2 f = rms_factor_huge(reinterpret_cast<const uint8_t*>(r), 0, lane, a.H, a.eps);
+    for (int c = 0; c < nch; ++c)
+      xn[lane + 32 * c] = norm8_huge(__ldg(r + lane + 32 * c), __ldg(w + lane + 32 * c), f);
+  }
 }
 
 // out[t][j] = bf16(sum over q of y[t][q][j]), q = shared experts, then top-k ranks;
