@@ -349,10 +349,14 @@ __device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane
 // (one warp per token) from logits [B][E] and ends with a barrier. Without
 // `full` only the selection bitmaps are built; with it also the weights. tb:
 // first trace event id, or -1.
+// NARROW: the kernel was instantiated for E <= 256 (and H <= 2048), so it
+// carries only the narrow top-k (a kernel's cold code still costs instruction
+// fetches on this latency-bound path).
+template <bool NARROW>
 __device__ void route_select(const DecodeArgs& a, RouteSmem& R, bool full, bool write_debug, int tb,
                              const float* logits) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  if (a.E <= 256) {
+  if (NARROW || a.E <= 256) {
     for (int t = warp; t < a.B; t += nw) topk_token_narrow(a, t, warp, lane, R, full, write_debug, tb, logits);
   } else {
     for (int t = warp; t < a.B; t += nw) topk_token_wide(a, t, warp, lane, R, full, write_debug, tb, logits);
@@ -482,8 +486,9 @@ static __device__ __noinline__ void load_rows_plain(uint8_t* dst, const uint8_t*
   for (int i = threadIdx.x; i < n; i += blockDim.x) reinterpret_cast<uint4*>(dst)[i] = ld_cg_v4(src + (size_t)i * 16);
 }
 
-template <int NCH>
+template <int NCH, int PRE>
 __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
+  const int prenorm = PRE < 0 ? a.prenorm : PRE;
   extern __shared__ __align__(128) uint8_t dsm[];  // router rows [4][H], norm weight [H], x chunk [<= 8][H]
   __shared__ __align__(8) uint64_t bars[2];        // 0: router rows, 1: x
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -499,9 +504,9 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
     mbar_init(&bars[1], 1);
     fence_mbar_init();
     const uint32_t bytes = (uint32_t)nrows * a.H * 2;
-    mbar_arrive_expect_tx(&bars[0], bytes + (a.prenorm ? (uint32_t)a.H * 2 : 0u));
+    mbar_arrive_expect_tx(&bars[0], bytes + (prenorm ? (uint32_t)a.H * 2 : 0u));
     bulk_g2s(wsm, a.router + (size_t)e0 * a.H, bytes, &bars[0]);
-    if (a.prenorm) bulk_g2s(gsm, a.gamma, (uint32_t)a.H * 2, &bars[0]);
+    if (prenorm) bulk_g2s(gsm, a.gamma, (uint32_t)a.H * 2, &bars[0]);
   }
   // Two passes at one call site: a dry one on zeroed activations before the
   // dependency wait (no stores), which brings the dot-product code into this
@@ -544,7 +549,7 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
           if (!ok) break;
         }
         FLINT_TRACE(a, 2);
-        if (a.prenorm) {  // RMSNorm of the chunk's rows, in place
+        if (prenorm) {  // RMSNorm of the chunk's rows, in place
           for (int t = warp; t < nt; t += 4) {
             uint8_t* row = xsm + (size_t)t * a.H * 2;
             float part = 0.f;
@@ -573,16 +578,14 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
       if (e < a.E && ntw > 0) {
         float* lgc = lg + (size_t)t0 * a.E;
         uint32_t* kcc = ws_keys(a) + (size_t)t0 * a.E;
-        switch (ntw) {  // one code path per token count: no predicated-off work
-          case 1: router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
-          case 2: router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
-          case 3: router_dots<NCH, 3>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
-          case 4: router_dots<NCH, 4>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
-          case 5: router_dots<NCH, 5>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
-          case 6: router_dots<NCH, 6>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
-          case 7: router_dots<NCH, 7>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
-          default: router_dots<NCH, 8>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry); break;
-        }
+        // One code path per token count, no predicated-off work. A warp has at
+        // most 2 tokens of a chunk: 1 expert per block and 4 token groups from
+        // 3 tokens on (chunks of 8), 2 experts and 2 groups at 2 tokens, 4
+        // experts and 1 group at 1 token.
+        if (ntw == 1)
+          router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry);
+        else
+          router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry);
         if (!dry) FLINT_TRACE(a, 7);
       }
       fence_proxy_async();  // the zeroing stores and these reads come before the copy into the buffer
@@ -694,9 +697,12 @@ __device__ __forceinline__ bool group_sync_and(int gi, bool v) {
 // layers) and stores the row in mma B-fragment order (f16, or bf16 as is).
 // Read straight from global memory (L2): a row of up to 2048 columns stays in
 // registers between the max and the conversion; wider rows are read twice.
-template <int FMT>
-__device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const uint16_t* gamma, float eps,
+// PRE: 0 or 1 when the kernel was instantiated for one case of the pre-norm
+// block, -1 to follow `prenorm` at run time.
+template <int FMT, bool NARROW = false, int PRE = -1>
+__device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm_rt, const uint16_t* gamma, float eps,
                            uint8_t* xs, int xstride, float* s_inv, int warp, int nwarps, int lane) {
+  const int prenorm = PRE < 0 ? prenorm_rt : PRE;
   for (int t = warp; t < B; t += nwarps) {
     const uint8_t* src = reinterpret_cast<const uint8_t*>(x + (size_t)t * K);
     const int nch = K / 256;  // 16-byte chunks per lane
@@ -723,7 +729,7 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const u
     const uint8_t* gw8 = reinterpret_cast<const uint8_t*>(gamma);
     float mx = 0.f;
     int kx = 0;
-    if (nch <= 8) {
+    if (NARROW || nch <= 8) {
       uint4 v[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c)
@@ -789,13 +795,13 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm, const u
   }
 }
 
-template <int FMT>
+template <int FMT, bool NARROW, int PRE>
 __device__ __forceinline__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xstride, float* s_inv, int warp,
                                         int nwarps, int lane) {
-  stage_rows<FMT>(a.x, a.B, a.H, a.prenorm, a.gamma, a.eps, xs, xstride, s_inv, warp, nwarps, lane);
+  stage_rows<FMT, NARROW, PRE>(a.x, a.B, a.H, a.prenorm, a.gamma, a.eps, xs, xstride, s_inv, warp, nwarps, lane);
 }
 
-template <int FMT, int NTMAX>
+template <int FMT, int NTMAX, bool NARROW, int PRE>
 __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 groups leave room for k_down
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
@@ -840,12 +846,12 @@ __global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 gro
     ++pre;
   }
   route_clear(R, a.E);
-  stage_x<FMT>(a, xs, xstride, s_inv, warp, blockDim.x >> 5, lane);
+  stage_x<FMT, NARROW, PRE>(a, xs, xstride, s_inv, warp, blockDim.x >> 5, lane);
   __syncthreads();  // route_clear before the selection's atomics
   pdl_wait();
   pdl_trigger();
   FLINT_TRACE(a, 9);
-  route_select(a, R, false, false, 21, ws_logits(a));  // its barrier also publishes xs and s_inv
+  route_select<NARROW>(a, R, false, false, 21, ws_logits(a));  // its barrier also publishes xs and s_inv
   FLINT_TRACE(a, 10);
   const int n_units = route_slots(a, R) * TILES;
   for (int jj = pre; jj < NB; ++jj) {
@@ -1009,8 +1015,9 @@ __host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, in
   return p;
 }
 
-template <int FMT, int NBUF>
+template <int FMT, int NBUF, bool NARROW, int PRE>
 __global__ void __launch_bounds__(512) k_down_items(DecodeArgs a) {
+  const int prenorm = PRE < 0 ? a.prenorm : PRE;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   __shared__ int s_wsum[MAX_WARPS];
@@ -1049,7 +1056,7 @@ __global__ void __launch_bounds__(512) k_down_items(DecodeArgs a) {
 
   // k_gateup lets this kernel launch only after its own wait, so the router has
   // finished: route now and fetch the routed down tiles while k_gateup runs.
-  route_select(a, R, true, blockIdx.x == 0, -1, ws_logits(a));
+  route_select<NARROW>(a, R, true, blockIdx.x == 0, -1, ws_logits(a));
   FLINT_TRACE(a, 17);
   const int n_slots = route_slots(a, R);
   {
@@ -1117,7 +1124,7 @@ __global__ void __launch_bounds__(512) k_down_items(DecodeArgs a) {
   const int KG = a.I / KG_COLS;
   // The residual rows of this tile (the layer's input, final before the
   // router ran) are read now, while the wait is pending.
-  if (a.prenorm)
+  if (prenorm)
     for (int p = threadIdx.x; p < a.B * 16; p += blockDim.x)
       s_res[p] = __ldcg(a.x + (size_t)(p >> 4) * a.H + tile * 16 + (p & 15));
   pdl_wait();  // h comes from k_gateup
@@ -1189,7 +1196,7 @@ __global__ void __launch_bounds__(512) k_down_items(DecodeArgs a) {
     float v = 0.f;
     for (int w2 = 0; w2 < nw; ++w2) v += acc_s[(w2 * a.B + t) * 16 + r];
     __nv_bfloat16 o = __float2bfloat16_rn(v);
-    if (a.prenorm) {  // residual stream: r + bf16(layer output), rounded to bf16
+    if (prenorm) {  // residual stream: r + bf16(layer output), rounded to bf16
       const uint32_t rb = (uint32_t)s_res[p] << 16;
       o = __float2bfloat16_rn(__uint_as_float(rb) + __bfloat162float(o));
     }
@@ -1235,7 +1242,7 @@ __host__ __device__ inline DownPlan down_plan(int I, int B, int max_slots, int f
   return p;
 }
 
-template <int FMT>
+template <int FMT, bool NARROW>
 __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
@@ -1282,7 +1289,7 @@ __global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
 
   // k_gateup lets this kernel launch only after its own wait, so the router has
   // finished: route now and fetch the routed down tiles while k_gateup runs.
-  route_select(a, R, true, blockIdx.x == 0, -1, ws_logits(a));
+  route_select<NARROW>(a, R, true, blockIdx.x == 0, -1, ws_logits(a));
   FLINT_TRACE(a, 17);
   const int n_slots = route_slots(a, R);
   {  // item list: chunks of up to 8 of a slot's selecting tokens; items and
@@ -1697,8 +1704,11 @@ cudaError_t launch_any(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 // for a k_down block, which launches early and prefetches meanwhile.
 void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) {
   // static shared memory of the gate/up kernels, as laid out by the compiler
-  static const size_t route = std::max({static_smem(k_gateup<FLINT_MOE_NVFP4, 1>), static_smem(k_gateup<FLINT_MOE_NVFP4, 4>),
-                                        static_smem(k_gateup<FLINT_MOE_BF16, 1>), static_smem(k_gateup<FLINT_MOE_BF16, 4>)});
+  static const size_t route =
+      std::max({static_smem(k_gateup<FLINT_MOE_NVFP4, 1, false, -1>), static_smem(k_gateup<FLINT_MOE_NVFP4, 4, false, -1>),
+                static_smem(k_gateup<FLINT_MOE_BF16, 1, false, -1>), static_smem(k_gateup<FLINT_MOE_BF16, 4, false, -1>),
+                static_smem(k_gateup<FLINT_MOE_NVFP4, 1, true, 0>), static_smem(k_gateup<FLINT_MOE_NVFP4, 1, true, 1>),
+                static_smem(k_gateup<FLINT_MOE_NVFP4, 4, true, -1>)});
   const int ntmax = (B + 7) / 8;
   const size_t budget = B <= 2 ? 110 * 1024 : SMEM_LIMIT;
   const int want_nb = units_per_block <= 3 ? 1 : 2;
@@ -1728,24 +1738,39 @@ void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) 
   nb = 0;
 }
 
-template <int FMT>
-cudaError_t launch_gateup(const DecodeArgs& a, cudaStream_t stream, int ng) {
+// The kernels for E <= 256 and H <= 2048 (the Flint shape) are separate
+// instantiations that carry no code for wider shapes.
+bool narrow_shape(const DecodeArgs& a) { return a.E <= 256 && a.H <= 2048; }
+
+template <int FMT, bool NARROW>
+cudaError_t launch_gateup_n(const DecodeArgs& a, cudaStream_t stream, int ng) {
   const int ntmax = (a.B + 7) / 8;
   const size_t smem = gateup_plan(a.H, a.B, FMT, ntmax, ng, a.gu_nb).total;
   const int units = a.W.max_slots * (a.I / 8);
   const int blocks = units < sm_count() ? units : sm_count();
   const dim3 block(128 * ng);
   switch (ntmax) {
-    case 1: return launch_pdl(k_gateup<FMT, 1>, dim3(blocks), block, smem, stream, a);
-    case 2: return launch_pdl(k_gateup<FMT, 2>, dim3(blocks), block, smem, stream, a);
-    case 3: return launch_pdl(k_gateup<FMT, 3>, dim3(blocks), block, smem, stream, a);
-    default: return launch_pdl(k_gateup<FMT, 4>, dim3(blocks), block, smem, stream, a);
+    case 1:  // up to 8 tokens, the low-latency path: one instantiation per pre-norm case
+      if constexpr (NARROW)
+        return a.prenorm ? launch_pdl(k_gateup<FMT, 1, NARROW, 1>, dim3(blocks), block, smem, stream, a)
+                         : launch_pdl(k_gateup<FMT, 1, NARROW, 0>, dim3(blocks), block, smem, stream, a);
+      else
+        return launch_pdl(k_gateup<FMT, 1, NARROW, -1>, dim3(blocks), block, smem, stream, a);
+    case 2: return launch_pdl(k_gateup<FMT, 2, NARROW, -1>, dim3(blocks), block, smem, stream, a);
+    case 3: return launch_pdl(k_gateup<FMT, 3, NARROW, -1>, dim3(blocks), block, smem, stream, a);
+    default: return launch_pdl(k_gateup<FMT, 4, NARROW, -1>, dim3(blocks), block, smem, stream, a);
   }
 }
 
 template <int FMT>
+cudaError_t launch_gateup(const DecodeArgs& a, cudaStream_t stream, int ng) {
+  return narrow_shape(a) ? launch_gateup_n<FMT, true>(a, stream, ng) : launch_gateup_n<FMT, false>(a, stream, ng);
+}
+
+template <int FMT>
 cudaError_t launch_down(const DecodeArgs& a, cudaStream_t stream, const DownPlan& P) {
-  return launch_pdl(k_down<FMT>, dim3(a.H / 16), dim3(32 * P.nw), P.total, stream, a);
+  return narrow_shape(a) ? launch_pdl(k_down<FMT, true>, dim3(a.H / 16), dim3(32 * P.nw), P.total, stream, a)
+                         : launch_pdl(k_down<FMT, false>, dim3(a.H / 16), dim3(32 * P.nw), P.total, stream, a);
 }
 
 // Up to 2 tokens the block shares its SM with a gate/up block: 8 warps, two
@@ -1762,17 +1787,19 @@ cudaError_t launch_router(const DecodeArgs& a, cudaStream_t stream) {
   const dim3 grid((a.E + a.router_epb - 1) / a.router_epb);
   const size_t smem = router_smem(a.H, a.B);
   switch (a.H / 256) {
-    case 1: return launch_pdl(k_router<1>, grid, dim3(128), smem, stream, a);
-    case 2: return launch_pdl(k_router<2>, grid, dim3(128), smem, stream, a);
-    case 3: return launch_pdl(k_router<3>, grid, dim3(128), smem, stream, a);
-    case 4: return launch_pdl(k_router<4>, grid, dim3(128), smem, stream, a);
-    case 5: return launch_pdl(k_router<5>, grid, dim3(128), smem, stream, a);
-    case 6: return launch_pdl(k_router<6>, grid, dim3(128), smem, stream, a);
-    case 7: return launch_pdl(k_router<7>, grid, dim3(128), smem, stream, a);
-    case 8: return launch_pdl(k_router<8>, grid, dim3(128), smem, stream, a);
-    case 16: return launch_pdl(k_router<16>, grid, dim3(128), smem, stream, a);
-    case 24: return launch_pdl(k_router<24>, grid, dim3(128), smem, stream, a);
-    case 32: return launch_pdl(k_router<32>, grid, dim3(128), smem, stream, a);
+    case 1: return launch_pdl(k_router<1, -1>, grid, dim3(128), smem, stream, a);
+    case 2: return launch_pdl(k_router<2, -1>, grid, dim3(128), smem, stream, a);
+    case 3: return launch_pdl(k_router<3, -1>, grid, dim3(128), smem, stream, a);
+    case 4: return launch_pdl(k_router<4, -1>, grid, dim3(128), smem, stream, a);
+    case 5: return launch_pdl(k_router<5, -1>, grid, dim3(128), smem, stream, a);
+    case 6: return launch_pdl(k_router<6, -1>, grid, dim3(128), smem, stream, a);
+    case 7: return launch_pdl(k_router<7, -1>, grid, dim3(128), smem, stream, a);
+    case 8:  // the Flint shape: one instantiation per pre-norm case
+      return a.prenorm ? launch_pdl(k_router<8, 1>, grid, dim3(128), smem, stream, a)
+                       : launch_pdl(k_router<8, 0>, grid, dim3(128), smem, stream, a);
+    case 16: return launch_pdl(k_router<16, -1>, grid, dim3(128), smem, stream, a);
+    case 24: return launch_pdl(k_router<24, -1>, grid, dim3(128), smem, stream, a);
+    case 32: return launch_pdl(k_router<32, -1>, grid, dim3(128), smem, stream, a);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1892,9 +1919,15 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   // Static shared memory of the down kernels (the routing, the warp sums, the
   // residual values), as the compiler laid it out: static plus dynamic must
   // stay within the per-block limit.
-  static const size_t route_smem = std::max({static_smem(k_down<FLINT_MOE_NVFP4>), static_smem(k_down<FLINT_MOE_BF16>),
-                                             static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF>),
-                                             static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF>)});
+  static const size_t route_smem =
+      std::max({static_smem(k_down<FLINT_MOE_NVFP4, false>), static_smem(k_down<FLINT_MOE_BF16, false>),
+                static_smem(k_down<FLINT_MOE_NVFP4, true>),
+                static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF, false, -1>),
+                static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF, false, -1>),
+                static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF, true, 0>),
+                static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF, true, 1>),
+                static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF, true, 0>),
+                static_smem(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF, true, 1>)});
   int gu_ng = 0;
   {
     const int units = a.W.max_slots * (a.I / 8), sms = sm_count();
@@ -1912,12 +1945,20 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_gateup<FLINT_MOE_NVFP4>(a, stream, gu_ng)
                                                        : launch_gateup<FLINT_MOE_BF16>(a, stream, gu_ng);
   if (e == cudaSuccess) {
+    const bool nar = narrow_shape(a);
+    const size_t dsm = down_items_smem(a);
+    const dim3 grid(a.H / 16), wide_blk(32 * DOWN_ITEMS_WIDE_NW), blk(32 * DOWN_ITEMS_NW);
     if (small_down && B >= 3)
-      e = launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF>, dim3(a.H / 16),
-                     dim3(32 * DOWN_ITEMS_WIDE_NW), down_items_smem(a), stream, a);
+      e = !nar     ? launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF, false, -1>, grid, wide_blk, dsm,
+                                stream, a)
+          : prenorm ? launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF, true, 1>, grid, wide_blk, dsm,
+                                 stream, a)
+                    : launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_WIDE_NBUF, true, 0>, grid, wide_blk, dsm,
+                                 stream, a);
     else if (small_down)
-      e = launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF>, dim3(a.H / 16), dim3(32 * DOWN_ITEMS_NW),
-                     down_items_smem(a), stream, a);
+      e = !nar     ? launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF, false, -1>, grid, blk, dsm, stream, a)
+          : prenorm ? launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF, true, 1>, grid, blk, dsm, stream, a)
+                    : launch_pdl(k_down_items<FLINT_MOE_NVFP4, DOWN_ITEMS_NBUF, true, 0>, grid, blk, dsm, stream, a);
     else
       e = a.fmt == FLINT_MOE_NVFP4 ? launch_down<FLINT_MOE_NVFP4>(a, stream, dp)
                                    : launch_down<FLINT_MOE_BF16>(a, stream, dp);
