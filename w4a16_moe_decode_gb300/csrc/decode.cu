@@ -349,9 +349,20 @@ __device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane
 // (one warp per token) from logits [B][E] and ends with a barrier. Without
 // `full` only the selection bitmaps are built; with it also the weights. tb:
 // first trace event id, or -1.
-// NARROW: the kernel was instantiated for E <= 256 (and H <= 2048), so it
-// carries only the narrow top-k (a kernel's cold code still costs instruction
-// fetches on this latency-bound path).
+// NARROW: the kernel was instantiated for the Flint shape (E = 256 experts,
+// hidden H = 2048), so it carries only the narrow top-k and the short-row
+// staging, with the two sizes known at compile time (a kernel's cold code
+// still costs instruction fetches on this latency-bound path).
+template <bool NARROW>
+__device__ __forceinline__ DecodeArgs flint_shape(const DecodeArgs& a_in) {
+  DecodeArgs a = a_in;
+  if (NARROW) {
+    a.H = 2048;
+    a.E = 256;
+  }
+  return a;
+}
+
 template <bool NARROW>
 __device__ void route_select(const DecodeArgs& a, RouteSmem& R, bool full, bool write_debug, int tb,
                              const float* logits) {
@@ -734,11 +745,8 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm_rt, cons
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         if (c < nch) v[c] = ld_cg_v4(src + (lane + 32 * c) * 16);
-      if (prenorm) {  // RMSNorm, as the router computes it; weights loaded beside x
-        uint4 wv[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < nch) wv[c] = __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16));
+      if (prenorm) {  // RMSNorm, as the router computes it
+        auto wv = [&](int c) { return __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)); };
         float part = 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -748,12 +756,12 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm_rt, cons
           const float inv = 1.0f / sqrtf(ss / (float)K + eps);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            if (c < nch) v[c] = norm8(v[c], wv[c], inv);
+            if (c < nch) v[c] = norm8(v[c], wv(c), inv);
         } else {  // the sum of squares overflowed: the scaled path
           const float2 f = rms_factor_huge(src, 0, lane, K, eps);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            if (c < nch) v[c] = norm8_huge(v[c], wv[c], f);
+            if (c < nch) v[c] = norm8_huge(v[c], wv(c), f);
         }
       }
       if (FMT == FLINT_MOE_NVFP4) {
@@ -802,7 +810,8 @@ __device__ __forceinline__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xs
 }
 
 template <int FMT, int NTMAX, bool NARROW, int PRE>
-__global__ void __maxnreg__(96) k_gateup(DecodeArgs a) {  // 96 registers: 3 groups leave room for k_down
+__global__ void __maxnreg__(96) k_gateup(const DecodeArgs a_in) {  // 96 registers: 3 groups leave room for k_down
+  const DecodeArgs a = flint_shape<NARROW>(a_in);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
@@ -1016,7 +1025,8 @@ __host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, in
 }
 
 template <int FMT, int NBUF, bool NARROW, int PRE>
-__global__ void __launch_bounds__(512) k_down_items(DecodeArgs a) {
+__global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
+  const DecodeArgs a = flint_shape<NARROW>(a_in);
   const int prenorm = PRE < 0 ? a.prenorm : PRE;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
@@ -1243,7 +1253,8 @@ __host__ __device__ inline DownPlan down_plan(int I, int B, int max_slots, int f
 }
 
 template <int FMT, bool NARROW>
-__global__ void __launch_bounds__(512) k_down(DecodeArgs a) {
+__global__ void __launch_bounds__(512) k_down(const DecodeArgs a_in) {
+  const DecodeArgs a = flint_shape<NARROW>(a_in);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
   __shared__ int s_wsum[MAX_WARPS];
@@ -1738,9 +1749,9 @@ void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) 
   nb = 0;
 }
 
-// The kernels for E <= 256 and H <= 2048 (the Flint shape) are separate
-// instantiations that carry no code for wider shapes.
-bool narrow_shape(const DecodeArgs& a) { return a.E <= 256 && a.H <= 2048; }
+// The kernels for the Flint shape (E = 256, H = 2048) are separate
+// instantiations that carry no code for other shapes.
+bool narrow_shape(const DecodeArgs& a) { return a.E == 256 && a.H == 2048; }
 
 template <int FMT, bool NARROW>
 cudaError_t launch_gateup_n(const DecodeArgs& a, cudaStream_t stream, int ng) {
