@@ -13,9 +13,10 @@
  * Conventions as in flint_moe.h: device pointers, caller-owned memory,
  * asynchronous on `stream`, status codes, 16-byte alignment (FLINT_MOE_EALIGN).
  * Shapes: N a multiple of 16, K a multiple of 256 up to 8192 (and of 2048
- * above 2048), 1 <= B <= 32 (B = 0 is a no-op); the activations of all B rows
- * must fit in shared memory (B * (2K + 16) bytes <= 160 KiB), else
- * FLINT_MOE_EUNSUPPORTED.
+ * above 2048), 0 <= B <= 32 (B = 0 is a no-op), else FLINT_MOE_EUNSUPPORTED
+ * (shape) or FLINT_MOE_EINVAL (B). For K > 2048 the K / 2048 column slices of
+ * a 16-row tile go to the CTAs of one thread-block cluster, whose partial sums
+ * are added in distributed shared memory in a fixed order.
  */
 #ifndef FLINT_GEMV_H
 #define FLINT_GEMV_H

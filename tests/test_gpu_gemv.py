@@ -79,3 +79,31 @@ def test_gemv_bf16_weights_and_norm_prologue():
     run_gemv(128, 1024, 4, 49, fmt=fb.BF16)
     run_gemv(128, 1024, 4, 50, norm=True)
     run_gemv(96, 768, 17, 51, fmt=fb.BF16, norm=True)
+
+
+@pytest.mark.parametrize("K,B,fmt,norm", [(8192, 1, fb.NVFP4, False), (8192, 9, fb.NVFP4, True),
+                                          (4096, 32, fb.NVFP4, True), (8192, 3, fb.BF16, True),
+                                          (4096, 17, fb.BF16, False)])
+def test_gemv_split_over_a_cluster(K, B, fmt, norm):
+    """K > 2048: the column slices of a tile are taken by the CTAs of a
+    cluster and added in distributed shared memory (and, with a norm weight,
+    the rows' sums of squares are shared the same way)."""
+    run_gemv(64, K, B, 52 + B, fmt=fmt, norm=norm)
+
+
+def test_gemv_split_norm_of_rows_beyond_the_fp32_square_range():
+    """Rows whose sum of squares overflows FP32 (times 2^100), normalised on the
+    split path: the scaled sum over the whole row."""
+    N, K, B, seed = 32, 4096, 3, 60
+    packed, _ = layers.synth_dense(N, K, seed, 0, fb.NVFP4, DEV)
+    xo = moe.bf16_bits_to_f64(synth.x_bf16(seed, 0, B, K)) * np.array([2.0 ** 100, 1.0, 2.0 ** -100])[:, None]
+    x = torch.from_numpy(moe.f64_to_bf16_bits(xo).view(np.int16)).to(DEV)
+    y = torch.full((B, N), 0x7FC0, dtype=torch.int16, device=DEV)
+    g = layers.synth_norm(K, seed, 0, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fb.flint_gemv(packed, N, K, fb.NVFP4, x, B, y, g, 1e-6, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    go = moe.bf16_bits_to_f64(synth.norm_bf16(seed, 0, K))
+    ref = dense.gemv(moe.bf16_bits_to_f64(moe.f64_to_bf16_bits(xo)), oracle_matrix(N, K, seed, fb.NVFP4), go, 1e-6)
+    check_out(ref, bits_to_f64(y), "gemv split, rows beyond the FP32 square range")

@@ -153,7 +153,6 @@ def test_gemv_host_validation(lib):
     assert L.flint_gemv(*args(2048, 2048, 1, x=0x30008)) == fb.EALIGN
     assert L.flint_gemv(*args(2048, 2048, 1, w=0x50004)) == fb.EALIGN
     assert L.flint_gemv(*args(2048, 2048, 1, eps=float("nan"))) == fb.EINVAL
-    assert L.flint_gemv(*args(64, 8192, 32)) == fb.EUNSUPPORTED          # activations exceed shared memory
 
 
 def test_layer_init_and_pack_validate(lib):

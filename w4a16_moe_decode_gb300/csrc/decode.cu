@@ -779,6 +779,7 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm_rt, cons
       float2 huge = make_float2(0.f, 0.f);  // the scaled path's factor and scale, if taken (y != 0)
       if (prenorm) {
         float part = 0.f;
+#pragma unroll 8
         for (int c = 0; c < nch; ++c) part = sumsq8(ld_cg_v4(src + (lane + 32 * c) * 16), part);
         const float ss = warp_sum(part);
         if (ss <= FP32_MAX)
@@ -792,11 +793,14 @@ __device__ void stage_rows(const uint16_t* x, int B, int K, int prenorm_rt, cons
         const uint4 w = __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16));
         return huge.y == 0.f ? norm8(u, w, inv) : norm8_huge(u, w, huge);
       };
+      // unrolled by 8, so that 8 chunks' loads are in flight together
       if (FMT == FLINT_MOE_NVFP4) {
+#pragma unroll 8
         for (int c = 0; c < nch; ++c) mx = absmax(chunk(c), mx);
         kx = prescale_exp(warp_max(mx));
       }
       const float sc = exp2i(kx);
+#pragma unroll 8
       for (int c = 0; c < nch; ++c) store(chunk(c), c, sc);
     }
     if (lane == 0) s_inv[t] = exp2i(-kx);
@@ -1614,6 +1618,197 @@ __global__ void __launch_bounds__(256) k_gemv(GemvArgs a) {
   }
 }
 
+// ===========================================================================
+// The same GEMV split along K over a thread-block cluster, for K > 2048: the
+// S = K / 2048 CTAs of a cluster share one tile of 16 output rows, each taking
+// 2048 columns (its weights, its slice of x). Their partial sums meet in
+// distributed shared memory and CTA 0 adds them in rank order (a fixed order,
+// so the result does not depend on timing) and writes y. With a norm weight
+// the rows' sums of squares are shared the same way before normalising.
+// Each slice of x is staged from registers (8 16-byte chunks per lane): no
+// serial passes over long rows.
+// ===========================================================================
+constexpr int GEMV_SLICE = 2048;
+
+struct GemvSplitPlan {
+  size_t wbuf_off, xs_off, red_off, part_off, ss_off, inv_off, bar_off, total;
+};
+
+__host__ __device__ inline GemvSplitPlan gemv_split_plan(int B, int fmt, int nw, int ntmax) {
+  const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  GemvSplitPlan p;
+  size_t o = 0;
+  p.wbuf_off = o;  o += (size_t)(GEMV_SLICE / KG_COLS) * kgb;
+  p.xs_off = o;    o += (size_t)B * (GEMV_SLICE * 2 + 16);
+  p.red_off = o;   o += sizeof(float) * nw * ntmax * 128;
+  p.part_off = o;  o += sizeof(float) * MAX_BATCH * 16;
+  p.ss_off = o;    o += sizeof(float) * MAX_BATCH;
+  p.inv_off = o;   o += sizeof(float) * MAX_BATCH;
+  o = (o + 15) & ~(size_t)15;
+  p.bar_off = o;   o += sizeof(uint64_t) * nw;
+  p.total = o;
+  return p;
+}
+
+template <int FMT, int NTMAX>
+__global__ void __launch_bounds__(256) k_gemv_split(GemvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
+  constexpr int NCH = GEMV_SLICE / 256;  // 16-byte chunks per lane of a slice row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const int nw = blockDim.x >> 5;
+  const uint32_t rank = cluster_rank(), S = gridDim.y;
+  const int KGW = (GEMV_SLICE / KG_COLS) / nw;  // k-groups per warp
+  const GemvSplitPlan P = gemv_split_plan(a.B, FMT, nw, NTMAX);
+  uint8_t* wb = smem + P.wbuf_off + (size_t)warp * KGW * KGB;
+  uint8_t* xs = smem + P.xs_off;
+  float* red = reinterpret_cast<float*>(smem + P.red_off);
+  float* part = reinterpret_cast<float*>(smem + P.part_off);  // [B][16] this CTA's partial y
+  float* s_ss = reinterpret_cast<float*>(smem + P.ss_off);    // [B] this slice's sums of squares
+  float* s_inv = reinterpret_cast<float*>(smem + P.inv_off);  // [B] inverse prescale
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + P.bar_off) + warp;
+  const int xstride = GEMV_SLICE * 2 + 16;
+  const size_t col0 = (size_t)rank * GEMV_SLICE;
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = (uint32_t)KGW * KGB;
+    const int64_t off = (int64_t)blockIdx.x * a.L.dn_tile + (int64_t)rank * (GEMV_SLICE / KG_COLS) * KGB +
+                        (int64_t)warp * bytes;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s_stream(wb, a.packed + off, bytes, bar);
+  }
+  pdl_wait();  // x may be the previous kernel's output
+  pdl_trigger();
+  // Stage this CTA's slice of every token row: warp w takes tokens w, w + nw, ...
+  const int ntw = (a.B - warp + nw - 1) / nw;  // tokens of this warp: at most NTMAX with 8 warps
+  uint4 v[NTMAX][NCH];
+  float sq[NTMAX];
+#pragma unroll
+  for (int i = 0; i < NTMAX; ++i) {
+    const int t = warp + i * nw;
+    sq[i] = 0.f;
+    if (i < ntw) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x + (size_t)t * a.K + col0);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) v[i][c] = ld_cg_v4(src + (lane + 32 * c) * 16);
+      if (a.prenorm) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) sq[i] = sumsq8(v[i][c], sq[i]);
+        sq[i] = warp_sum(sq[i]);
+        if (lane == 0) s_ss[t] = sq[i];
+      }
+    }
+  }
+  if (a.prenorm) cluster_sync();  // every slice's sums of squares are published
+#pragma unroll
+  for (int i = 0; i < NTMAX; ++i) {
+    const int t = warp + i * nw;
+    if (i < ntw) {
+      if (a.prenorm) {
+        float ss = 0.f;
+        for (uint32_t r = 0; r < S; ++r) ss += ld_dsmem_f32(s_ss + t, r);  // rank order
+        const uint8_t* gw8 = reinterpret_cast<const uint8_t*>(a.gamma) + col0 * 2;
+        if (ss <= FP32_MAX) {
+          const float inv = 1.0f / sqrtf(ss / (float)a.K + a.eps);
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+            v[i][c] = norm8(v[i][c], __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), inv);
+        } else {  // the sum of squares overflowed: the scaled path over the whole row
+          const float2 f = rms_factor_huge(reinterpret_cast<const uint8_t*>(a.x + (size_t)t * a.K), 0, lane, a.K,
+                                           a.eps);
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+            v[i][c] = norm8_huge(v[i][c], __ldg(reinterpret_cast<const uint4*>(gw8 + (lane + 32 * c) * 16)), f);
+        }
+      }
+      int kx = 0;
+      if (FMT == FLINT_MOE_NVFP4) {
+        float mx = 0.f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) mx = absmax8(v[i][c], mx);
+        kx = prescale_exp(warp_max(mx));
+      }
+      const float sc = exp2i(kx);
+      uint8_t* dst = xs + (size_t)t * xstride;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const uint32_t w4[4] = {v[i][c].x, v[i][c].y, v[i][c].z, v[i][c].w};
+        const int col = 8 * (lane + 32 * c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t bits = w4[q];
+          if (FMT == FLINT_MOE_NVFP4) {
+            const __half2 hv = __floats2half2_rn(bf16lo(w4[q]) * sc, bf16hi(w4[q]) * sc);
+            bits = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          *reinterpret_cast<uint32_t*>(dst + 2 * frag_offset_elems(col + 2 * q)) = bits;
+        }
+      }
+      if (lane == 0) s_inv[t] = exp2i(-kx);
+    }
+  }
+  __syncthreads();
+  const int nt_used = (a.B + 7) >> 3;
+  float acc[2][NTMAX][4];
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int nt = 0; nt < NTMAX; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
+  const bool ok = mbar_wait(bar, 0, a.status);
+  if (ok) {
+    int tok[NTMAX];
+#pragma unroll
+    for (int nt = 0; nt < NTMAX; ++nt) tok[nt] = min(nt * 8 + g, a.B - 1);
+#pragma unroll 4
+    for (int kl = 0; kl < KGW; ++kl) {
+      const int kg = warp * KGW + kl;
+      uint4 bx[NTMAX][2];
+#pragma unroll
+      for (int nt = 0; nt < NTMAX; ++nt) {
+        if (nt < nt_used) {
+          const uint8_t* rp = xs + (size_t)tok[nt] * xstride + kg * 128 + t4 * 32;
+          bx[nt][0] = lds128(rp);
+          bx[nt][1] = lds128(rp + 16);
+        }
+      }
+      if (kl & 1)
+        tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[1]);
+      else
+        tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[0]);
+    }
+  } else {
+    mbar_drain(bar, 0);
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTMAX; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[((warp * NTMAX + nt) * 32 + lane) * 4 + i] = acc[0][nt][i] + acc[1][nt][i];
+  __syncthreads();
+  // This CTA's partial sums (prescale undone), output (row r, token t) at [t][r].
+  for (int p = threadIdx.x; p < 16 * a.B; p += blockDim.x) {
+    const int r = p & 15, t = p >> 4, nt = t >> 3, c = t & 7;
+    const int ln = 4 * (r & 7) + (c >> 1), i = 2 * (r >> 3) + (c & 1);
+    float v2 = 0.f;
+    for (int w2 = 0; w2 < nw; ++w2) v2 += red[((w2 * NTMAX + nt) * 32 + ln) * 4 + i];
+    part[t * 16 + r] = v2 * s_inv[t];
+  }
+  cluster_sync();  // every CTA's partial sums are published
+  if (rank == 0) {
+    const float G = FMT == FLINT_MOE_NVFP4 ? a.G[0] : 1.0f;
+    for (int p = threadIdx.x; p < 16 * a.B; p += blockDim.x) {
+      float v2 = 0.f;
+      for (uint32_t r = 0; r < S; ++r) v2 += ld_dsmem_f32(part + p, r);  // rank order
+      const int rr = p & 15, t = p >> 4;
+      const __nv_bfloat16 o = __float2bfloat16_rn(v2 * G);
+      a.y[(size_t)t * a.N + blockIdx.x * 16 + rr] = *reinterpret_cast<const uint16_t*>(&o);
+    }
+  }
+  cluster_sync();  // the other CTAs' shared memory stays until CTA 0 has read it
+}
+
 }  // namespace flint
 
 using namespace flint;
@@ -1673,6 +1868,30 @@ int sm_count() {
 
 template <typename K, typename Args>
 cudaError_t launch_any(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const Args& a);
+
+// The same launch with a cluster of (1, cy, 1) CTAs.
+template <typename K, typename Args>
+cudaError_t launch_cluster(K kernel, dim3 grid, dim3 block, size_t smem, int cy, cudaStream_t stream, const Args& a) {
+  if (smem > 32 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = cy;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
 template <typename K>
 cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const DecodeArgs& a) {
@@ -2093,6 +2312,29 @@ extern "C" flint_moe_status flint_gemv(const void* packed, int32_t N, int32_t K,
   a.eps = eps;
   a.status = dev_status;
   const int kg = K / KG_COLS, nw = kg % 8 == 0 ? 8 : 4, ntmax = (B + 7) / 8;
+  if (K > GEMV_SLICE) {  // split along K over a cluster of K / 2048 CTAs
+    const int S = K / GEMV_SLICE;
+    const size_t smem = gemv_split_plan(B, fmt, 8, ntmax).total;
+    if (smem > SMEM_LIMIT) return FLINT_MOE_EUNSUPPORTED;
+    const dim3 grid(N / 16, S), block(256);
+    cudaError_t e;
+    if (fmt == FLINT_MOE_NVFP4) {
+      switch (ntmax) {
+        case 1: e = launch_cluster(k_gemv_split<FLINT_MOE_NVFP4, 1>, grid, block, smem, S, stream, a); break;
+        case 2: e = launch_cluster(k_gemv_split<FLINT_MOE_NVFP4, 2>, grid, block, smem, S, stream, a); break;
+        case 3: e = launch_cluster(k_gemv_split<FLINT_MOE_NVFP4, 3>, grid, block, smem, S, stream, a); break;
+        default: e = launch_cluster(k_gemv_split<FLINT_MOE_NVFP4, 4>, grid, block, smem, S, stream, a); break;
+      }
+    } else {
+      switch (ntmax) {
+        case 1: e = launch_cluster(k_gemv_split<FLINT_MOE_BF16, 1>, grid, block, smem, S, stream, a); break;
+        case 2: e = launch_cluster(k_gemv_split<FLINT_MOE_BF16, 2>, grid, block, smem, S, stream, a); break;
+        case 3: e = launch_cluster(k_gemv_split<FLINT_MOE_BF16, 3>, grid, block, smem, S, stream, a); break;
+        default: e = launch_cluster(k_gemv_split<FLINT_MOE_BF16, 4>, grid, block, smem, S, stream, a); break;
+      }
+    }
+    return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ECUDA;
+  }
   size_t o1, o2, o3, o4, o5;
   const size_t smem = gemv_smem(K, B, fmt, nw, ntmax, &o1, &o2, &o3, &o4, &o5);
   if ((size_t)B * (K * 2 + 16) > 160 * 1024 || smem > SMEM_LIMIT) return FLINT_MOE_EUNSUPPORTED;
