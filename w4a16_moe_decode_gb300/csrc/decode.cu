@@ -165,12 +165,13 @@ constexpr float RCP_NR_MAX = 0x1p125f;
 // The IEEE quotient 1 / y, out of line, for values outside rcp_nr's range:
 // the common path then carries none of the division's code.
 __device__ __noinline__ float rcp_ieee(float y) { return 1.0f / y; }
+__device__ __noinline__ float div_ieee(float x, float y) { return x / y; }
 
 // Routing score 1 / (1 + e^-l) in FP32: the IEEE quotient, computed through
 // rcp_nr except for l below about -86.6 (y >= 2^125) or NaN.
 __device__ __forceinline__ float sigmoid_f32(float l) {
   const float y = 1.0f + expf(-l);
-  return y < RCP_NR_MAX ? rcp_nr(y) : 1.0f / y;
+  return y < RCP_NR_MAX ? rcp_nr(y) : rcp_ieee(y);
 }
 
 // Key of expert e: sigmoid of its logit plus its selection bias, in FP32.
@@ -961,7 +962,7 @@ __global__ void __maxnreg__(96) k_gateup(const DecodeArgs a_in) {  // 96 registe
         const float gv = (gs * inv) * Gg;
         const float uv = (us * inv) * Gu;
         const float ey = 1.0f + expf(-gv);
-        const float sv = ey < RCP_NR_MAX ? gv * rcp_nr(ey) : gv / ey;  // SiLU
+        const float sv = ey < RCP_NR_MAX ? gv * rcp_nr(ey) : div_ieee(gv, ey);  // SiLU
         const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
         h[row * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hb);
         hv = fabsf(__bfloat162float(hb));
