@@ -267,7 +267,7 @@ flint_moe_status flint_moe_read_status(const void* workspace, int32_t* host_stat
  * other threads) race on the array: serialise them. Returns
  * FLINT_MOE_EUNSUPPORTED when the workspace this shape and batch need
  * (flint_moe_workspace_bytes) exceeds FLINT_MOE_NOALLOC_SCRATCH_BYTES (the
- * Flint-shape layer needs 6.1 MiB at B = 32, 0.40 MiB at B = 8), checked before
+ * Flint-shape layer needs 6.1 MiB at B = 32, 0.78 MiB at B = 8), checked before
  * anything else touches the device. dev_status (device int32, 4-byte aligned,
  * may be NULL): the device status bits of this call (FLINT_MOE_DEV_ERR_*) are
  * ORed into it by one more small kernel after the decode. */

@@ -81,22 +81,32 @@ __host__ __device__ inline Layout make_dense_layout(int N, int K, int fmt) {
 // ---------------------------------------------------------------------------
 // Workspace layout. Header words, then 256-byte aligned regions.
 // ---------------------------------------------------------------------------
-enum : int { HDR_COUNTER = 0, HDR_STATUS = 1, HDR_NSLOTS = 2, HDR_NROWS = 3, HDR_BATCH = 4 };
+// HDR_HBIG: nonzero when some |h| of the call is 2^15 or more (its f16 copy
+// is then not exact); set by the gate/up kernel, cleared by the router.
+enum : int { HDR_STATUS = 1, HDR_HBIG = 2 };
 
 // Regions: router logits [B][E] and the selection keys the router derives
 // from them ([B][E], order-preserving unsigned form); the routing of the last decode ([B][k]
 // indices and weights, for read-back); the largest |h| per (slot, token) row;
-// h in bf16 [rows][I] in fragment order. Slot s (shared experts first, then
+// h in bf16 [rows][I] in fragment order, and the same values in f16 (exact
+// for 2^-14 <= |h| < 2^15, on the f16 grid of 2^-24 below) for the
+// small-batch down kernel's f16 products. Slot s (shared experts first, then
 // the distinct selected experts in ascending id) owns rows s * B .. s * B + B - 1.
 struct WsLayout {
-  size_t logits, keys, topk_idx, topk_w, hmax, h, total;
+  size_t logits, keys, topk_idx, topk_w, hmax, h, h16, total;
   int max_slots, max_rows;
+  int has_h16;  // the f16 copy of h exists (calls of up to 8 tokens, NVFP4 weights)
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~(size_t)255; }
 
-__host__ __device__ inline WsLayout make_ws_layout(int H, int E, int k, int I, int S, int maxB) {
+// The f16 copy of h serves the small-batch down kernel only: calls of up to
+// 8 tokens with NVFP4 weights.
+__host__ __device__ inline bool ws_wants_h16(int B, int fmt) { return B <= 8 && fmt == FLINT_MOE_NVFP4; }
+
+__host__ __device__ inline WsLayout make_ws_layout(int H, int E, int k, int I, int S, int maxB, bool with_h16) {
   WsLayout W;
+  W.has_h16 = with_h16 ? 1 : 0;
   W.max_slots = S + (E < maxB * k ? E : maxB * k);
   W.max_rows = W.max_slots * maxB;
   size_t o = 256;
@@ -106,6 +116,7 @@ __host__ __device__ inline WsLayout make_ws_layout(int H, int E, int k, int I, i
   W.topk_w = o;   o = ws_align(o + sizeof(float) * maxB * k);
   W.hmax = o;     o = ws_align(o + sizeof(unsigned) * W.max_rows);
   W.h = o;        o = ws_align(o + (size_t)2 * W.max_rows * I);
+  W.h16 = o;      o = ws_align(o + (with_h16 ? (size_t)2 * W.max_rows * I : 0));
   W.total = o;
   return W;
 }

@@ -71,6 +71,7 @@ __device__ __forceinline__ int* ws_topk_idx(const DecodeArgs& a) { return reinte
 __device__ __forceinline__ float* ws_topk_w(const DecodeArgs& a) { return reinterpret_cast<float*>(a.ws + a.W.topk_w); }
 __device__ __forceinline__ unsigned* ws_hmax(const DecodeArgs& a) { return reinterpret_cast<unsigned*>(a.ws + a.W.hmax); }
 __device__ __forceinline__ uint16_t* ws_h(const DecodeArgs& a) { return reinterpret_cast<uint16_t*>(a.ws + a.W.h); }
+__device__ __forceinline__ uint16_t* ws_h16(const DecodeArgs& a) { return reinterpret_cast<uint16_t*>(a.ws + a.W.h16); }
 
 // ---------------------------------------------------------------------------
 // Optional phase trace (built with -DFLINT_MOE_TRACE): per decode call, the
@@ -541,8 +542,10 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
       pdl_wait();  // x is the previous kernel's output
       pdl_trigger();
       FLINT_TRACE(a, 1);
-      if (blockIdx.x == 0)
+      if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i < a.W.max_slots * a.B; i += blockDim.x) ws_hmax(a)[i] = 0u;
+        if (threadIdx.x == 0) ws_hdr(a)[HDR_HBIG] = 0;
+      }
     }
     for (int t0 = 0; t0 < a.B; t0 += 8) {
       const int nt = min(8, a.B - t0);
@@ -943,6 +946,7 @@ __global__ void __maxnreg__(96) k_gateup(const DecodeArgs a_in) {  // 96 registe
     const float Gu = glob[expert * 4 + 1];
     const int hoff = frag_offset_elems(tile * 8 + g);
     uint16_t* h = ws_h(a);
+    uint16_t* h16 = ws_h16(a);
     unsigned* hmax = ws_hmax(a);
     for (int pr = gw; pr < 2 * nt_used; pr += 4) {
       const int nt = pr >> 1, hh = pr & 1;
@@ -966,11 +970,18 @@ __global__ void __maxnreg__(96) k_gateup(const DecodeArgs a_in) {  // 96 registe
         const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
         h[row * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hb);
         hv = fabsf(__bfloat162float(hb));
+        if (a.W.has_h16) {
+          const __half hh = __float2half_rn(__bfloat162float(hb));
+          h16[row * a.I + hoff] = *reinterpret_cast<const uint16_t*>(&hh);
+        }
       }
       hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 4));
       hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 8));
       hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, 16));
-      if (g == 0 && sel && hv > 0.f) atomicMax(hmax + row, __float_as_uint(hv));
+      if (g == 0 && sel && hv > 0.f) {
+        atomicMax(hmax + row, __float_as_uint(hv));
+        if (!(hv < 32768.f)) atomicOr(ws_hdr(a) + HDR_HBIG, 1);  // its f16 copy is not exact
+      }
     }
   }
   FLINT_TRACE(a, 13);
@@ -1008,6 +1019,34 @@ __device__ __forceinline__ void row_to_f16(uint8_t* row, int I, int kh, int lane
 // kernel. Measured faster than the staged kernel below at batch 1 (fewer
 // instructions on the cold path after the wait).
 // ===========================================================================
+// The rare path of the small-batch down kernel, when some |h| of the call
+// reached 2^15 (its f16 copy is not exact): the item's selected token rows
+// (h rows r0 + n, n < 8, bit n of bits) are rebuilt in the buffer from the
+// bf16 h, each times a power of two that puts its largest |h| in
+// [2^14, 2^15) (exact down to 2^-29 of it). Whole warp; returns, in lane
+// n < 8, the inverse of column n's scale (1 elsewhere). Out of line: the
+// common path carries none of it.
+static __device__ __noinline__ float h_rows_prescaled(const unsigned* hmax, const uint16_t* h, int I, uint8_t* hb,
+                                                      int hstride, int r0, uint32_t bits, int lane) {
+  float inv = 1.0f;
+  for (int n = 0; n < 8; ++n) {
+    if (!((bits >> n) & 1u)) continue;
+    const int kh = prescale_exp(__uint_as_float(__ldcg(hmax + r0 + n)));
+    const float sc = exp2i(kh);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(h + (size_t)(r0 + n) * I);
+    uint8_t* dst = hb + n * hstride;
+    for (int q = lane; q < I / 8; q += 32) {
+      const uint4 u = ld_cg_v4(src + q * 16);
+      *reinterpret_cast<uint4*>(dst + q * 16) =
+          make_uint4(bf16x2_to_f16x2_scaled(u.x, sc), bf16x2_to_f16x2_scaled(u.y, sc),
+                     bf16x2_to_f16x2_scaled(u.z, sc), bf16x2_to_f16x2_scaled(u.w, sc));
+    }
+    if (lane == n) inv = exp2i(-kh);
+  }
+  __syncwarp();
+  return inv;
+}
+
 struct DownItemsPlan {
   int buf_bytes, hrows, hstride;
   size_t acc_off, items_off, bar_off, total;
@@ -1133,7 +1172,7 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
     if (lane == 0) mbar_arrive_expect_tx(&bars[b], (uint32_t)(__popc(bits) * a.I * 2));
     __syncwarp();
     if (lane < 8 && ((bits >> lane) & 1u))
-      bulk_g2s(buf(b) + dn_bytes + lane * P.hstride, ws_h(a) + (size_t)(r0 + lane) * a.I, (uint32_t)(a.I * 2),
+      bulk_g2s(buf(b) + dn_bytes + lane * P.hstride, ws_h16(a) + (size_t)(r0 + lane) * a.I, (uint32_t)(a.I * 2),
                &bars[b]);
   };
   const int KG = a.I / KG_COLS;
@@ -1146,9 +1185,13 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
   pdl_trigger();
   FLINT_TRACE(a, 18);
   for (int j = 0; j < NBUF && warp + nw * j < n_items; ++j) issue_h(j);
-  // h is consumed as stored (bf16 products with the weights converted to bf16):
-  // no per-row prescale, so no max |h| to read, no conversion pass and no
-  // block barrier between the wait and the products.
+  // h is consumed in its f16 copy, exact for |h| < 2^15, so the products run
+  // in f16 with the dequantised weights as they are (exact in f16): no
+  // conversion, no per-row prescale, no block barrier between the wait and
+  // the products. Only if some |h| of the call reached 2^15 (the flag is read
+  // while the copies are on their way) does each item rebuild its rows from
+  // the bf16 h with a per-row power-of-two prescale.
+  const bool hbig = __ldcg(ws_hdr(a) + HDR_HBIG) != 0;
   for (int j = 0; warp + nw * j < n_items; ++j) {
     int s, nt, expert;
     uint32_t bits;
@@ -1164,6 +1207,8 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
     if (j == 0) FLINT_TRACE(a, 19);
     uint8_t* wb = buf(b);
     uint8_t* hb = wb + dn_bytes;
+    float hinv = 1.0f;  // this lane's column's inverse prescale (fallback only)
+    if (hbig) hinv = h_rows_prescaled(ws_hmax(a), ws_h(a), a.I, hb, P.hstride, s * a.B + 8 * nt, bits, lane);
     float acc[2][1][4];
 #pragma unroll
     for (int c = 0; c < 2; ++c)
@@ -1177,11 +1222,13 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
       bx[0][0] = lds128(rp);
       bx[0][1] = lds128(rp + 16);
       if (kg & 1)
-        tile_kgroup<FMT, 1, true>(wb + kg * KGB, bx, 1, lane, acc[1]);
+        tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[1]);
       else
-        tile_kgroup<FMT, 1, true>(wb + kg * KGB, bx, 1, lane, acc[0]);
+        tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
     }
     const float Gd = a.globals[expert * 4 + 2];
+    // columns 2 t4 and 2 t4 + 1: their inverse prescales, from lanes n
+    const float inv0 = __shfl_sync(0xffffffffu, hinv, 2 * t4), inv1 = __shfl_sync(0xffffffffu, hinv, 2 * t4 + 1);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int n = 2 * t4 + hh;
@@ -1191,13 +1238,15 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
         if (s >= a.S)
           for (int r = 0; r < a.k; ++r)
             if (R.idx[tok * a.k + r] == expert) wt = R.w[tok * a.k + r];
+        const float inv = hh ? inv1 : inv0;
         float* dst = acc_s + (warp * a.B + tok) * 16;
-        dst[g] += wt * ((acc[0][0][hh] + acc[1][0][hh]) * Gd);
-        dst[g + 8] += wt * ((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * Gd);
+        dst[g] += wt * (((acc[0][0][hh] + acc[1][0][hh]) * inv) * Gd);
+        dst[g + 8] += wt * (((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * inv) * Gd);
       }
     }
     __syncwarp();
     if (warp + nw * (j + NBUF) < n_items) {
+      fence_proxy_async();  // this warp's accesses to the buffer come before the copies into it
       int s2, nt2, e2;
       uint32_t bits2;
       item_of(j + NBUF, s2, nt2, bits2, e2);
@@ -2039,7 +2088,15 @@ cudaError_t launch_router(const DecodeArgs& a, cudaStream_t stream) {
 
 extern "C" size_t flint_moe_workspace_bytes(const flint_moe_config* c, int32_t max_batch) {
   if (flint_moe_check_config(c) != FLINT_MOE_OK || max_batch < 1 || max_batch > MAX_BATCH) return 0;
-  return make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, max_batch).total;
+  // A call of B <= max_batch tokens lays the workspace out for its own B: the
+  // largest layout is that of max_batch, or of 8 tokens where those carry the
+  // f16 copy of h and max_batch does not.
+  const int b8 = max_batch < 8 ? max_batch : 8;
+  const size_t t1 = make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, max_batch,
+                                   ws_wants_h16(max_batch, c->weight_fmt)).total;
+  const size_t t2 = make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, b8,
+                                   ws_wants_h16(b8, c->weight_fmt)).total;
+  return t1 > t2 ? t1 : t2;
 }
 
 extern "C" flint_moe_status flint_moe_workspace_init(const flint_moe_config* c, int32_t max_batch, void* ws,
@@ -2122,7 +2179,7 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   a.ws = static_cast<uint8_t*>(ws);
   // The workspace is laid out for the batch of this call; callers size it for
   // their largest batch, which is at least as large.
-  a.W = make_ws_layout(a.H, a.E, a.k, a.I, a.S, B);
+  a.W = make_ws_layout(a.H, a.E, a.k, a.I, a.S, B, ws_wants_h16(B, a.fmt));
   a.prenorm = prenorm ? 1 : 0;
   a.router_epb = router_epb(B);
   // x and out may be device memory or pinned (device-mapped) host memory;
@@ -2231,7 +2288,8 @@ extern "C" flint_moe_status flint_moe_debug_routing(const flint_moe_config* c, c
                                                     int32_t* idx, float* w, cudaStream_t stream) {
   if (flint_moe_check_config(c) != FLINT_MOE_OK || !ws || !idx || !w || B < 1 || B > MAX_BATCH)
     return FLINT_MOE_EINVAL;
-  const WsLayout W = make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, B);
+  const WsLayout W = make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, B,
+                                    ws_wants_h16(B, c->weight_fmt));
   const uint8_t* base = static_cast<const uint8_t*>(ws);
   const size_t n = (size_t)B * c->top_k;
   if (cudaMemcpyAsync(idx, base + W.topk_idx, n * sizeof(int), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
@@ -2429,7 +2487,8 @@ extern "C" flint_moe_status flint_moe_decode_noalloc(const flint_moe_layer* laye
   if (st != FLINT_MOE_OK) return st;
   if (B < 0 || B > MAX_BATCH) return FLINT_MOE_EINVAL;
   if (B == 0) return FLINT_MOE_OK;
-  if (make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, B).total >
+  if (make_ws_layout(c->hidden, c->num_experts, c->top_k, c->inter, c->n_shared, B, ws_wants_h16(B, c->weight_fmt))
+          .total >
       FLINT_MOE_NOALLOC_SCRATCH_BYTES)
     return FLINT_MOE_EUNSUPPORTED;
   if (!x || !out) return FLINT_MOE_EINVAL;
