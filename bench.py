@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--prefill-batches", default="", help=argparse.SUPPRESS)
     p.add_argument("--prefill-layers", type=int, default=8, help=argparse.SUPPRESS)
     p.add_argument("--oracle-leg", type=int, default=0, help=argparse.SUPPRESS)
+    p.add_argument("--ncu-case", default="", help="small case for ncu captures: a batch size (2 Flint-shape layers, "
+                   "4 decodes, L2 flushed between them) or 'gemv' (one 2048 x 8192 NVFP4 GEMV, 4 calls)")
     return p.parse_args()
 
 
@@ -820,8 +822,48 @@ def gpu_arm(args) -> None:
         dist.destroy_process_group()
 
 
+def ncu_case(args) -> None:
+    """A few launches on a small device footprint (about 1 GB), for --set full
+    ncu captures of one kernel: 2 Flint-shape layers decoded alternately at
+    batch B, or one 2048 x 8192 NVFP4 GEMV at batch 1; a 256 MB write flushes
+    L2 before every call."""
+    import torch
+    from w4a16_moe_decode_gb300 import binding as fb
+    from w4a16_moe_decode_gb300 import layers
+    from w4a16_moe_decode_gb300.build import build
+    build()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    if args.ncu_case == "gemv":
+        N, K = 2048, 8192
+        packed, _ = layers.synth_dense(N, K, 2000, 0, fb.NVFP4, dev)
+        x = layers.synth_x(1, K, 2000, 0, dev)
+        y = torch.empty(1, N, dtype=torch.int16, device=dev)
+        for i in range(4):
+            flush.fill_(float(i))
+            fb.flint_gemv(packed, N, K, fb.NVFP4, x, 1, y)
+        torch.cuda.synchronize()
+        return
+    B = int(args.ncu_case)
+    cfg = fb.make_config(**FLINT)
+    pool = [layers.synth_layer(cfg, args.seed, L, dev) for L in range(2)]
+    xs = [layers.synth_x(B, cfg.hidden, args.seed, L, dev) for L in range(2)]
+    outs = [torch.empty_like(x) for x in xs]
+    ws = layers.workspace(cfg, B, dev)
+    for i in range(4):
+        flush.fill_(float(i))
+        fb.flint_moe_decode(pool[i % 2].handle, xs[i % 2], B, outs[i % 2], ws)
+    torch.cuda.synchronize()
+    st, bits = fb.flint_moe_read_status(ws)
+    if st != fb.OK or bits:
+        raise RuntimeError(f"device status {bits}")
+
+
 def main():
     args = parse_args()
+    if args.ncu_case:
+        ncu_case(args)
+        return
     if args.impl == "reference":
         reference_arm(args)
     else:
