@@ -447,8 +447,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
     int g = 0;
     TileInfo nxt = my_tiles > 0 ? tile_info<MODE>(a, tile_of(0)) : TileInfo{};
     uint32_t idesc = 0, acc = tmem;
-    const uint64_t ad0 = sw128_desc(a_op), ad1 = sw128_desc(a_op + A_STAGE);
-    const uint64_t bd0 = sw128_desc(b_op), bd1 = sw128_desc(b_op + B_STAGE);
+
     int s = 0, phase = 0, i = 0, kb = 0;  // stage, its phase parity, tile, k-block
     for (; g < total; ++g) {
       bool ok = true;
@@ -462,7 +461,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
       ok = ok && wait_ab(&G.full[p][s], (uint32_t)phase, abort, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const uint64_t ad = s ? ad1 : ad0, bd = s ? bd1 : bd0;
+      const uint64_t ad = sw128_desc(a_op + s * A_STAGE), bd = sw128_desc(b_op + s * B_STAGE);
       if (elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks)
