@@ -118,9 +118,9 @@ constexpr int USED_WORDS = MAX_EXPERTS / 32;
 // Routing result in shared memory. Slots are the S shared experts, then the
 // distinct selected experts in ascending id; slot s holds all B token rows
 // s * B .. s * B + B - 1 of h (a token that did not select the expert has a
-// row that is computed and never combined). So a consumer needs no prefix
-// sums: the r-th selected expert is the r-th set bit of `used`, and the tokens
-// of expert e are the bits of mask[e].
+// row that is computed and never combined). The r-th selected expert is the
+// r-th set bit of `used`, which the selection also lists in slot_e, and the
+// tokens of expert e are the bits of mask[e].
 struct __align__(16) RouteSmem {
   uint32_t mask[MAX_EXPERTS];       // bit t: token t selected expert e
   uint32_t used[USED_WORDS];        // bit e % 32 of word e / 32: some token selected e
@@ -128,10 +128,8 @@ struct __align__(16) RouteSmem {
   float w[MAX_BATCH * MAX_TOPK];
   int sel_e[MAX_WARPS][MAX_TOPK];   // per warp scratch for the token being routed
   float sel_l[MAX_WARPS][MAX_TOPK];
-  float sel_s[MAX_WARPS][MAX_TOPK];
-  float sel_k[MAX_WARPS][MAX_TOPK];
+  uint16_t slot_e[MAX_EXPERTS];     // expert of routed slot S + r (built by route_select)
 };
-static_assert(offsetof(RouteSmem, used) % 16 == 0, "slot_info reads `used` 16 bytes at a time");
 
 // Clears the selection bitmaps; the caller synchronises the block afterwards.
 // Needs nothing from the previous kernel, so it runs before the dependency wait.
@@ -352,15 +350,20 @@ __device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane
 // `full` only the selection bitmaps are built; with it also the weights. tb:
 // first trace event id, or -1.
 // NARROW: the kernel was instantiated for the Flint shape (E = 256 experts,
-// hidden H = 2048), so it carries only the narrow top-k and the short-row
-// staging, with the two sizes known at compile time (a kernel's cold code
-// still costs instruction fetches on this latency-bound path).
+// hidden H = 2048, intermediate I = 512, top-6, one shared expert), so it
+// carries only the narrow top-k and the short-row staging, with the sizes
+// known at compile time (a kernel's cold code still costs instruction
+// fetches on this latency-bound path, and its index arithmetic becomes
+// shifts and unrolled loops).
 template <bool NARROW>
 __device__ __forceinline__ DecodeArgs flint_shape(const DecodeArgs& a_in) {
   DecodeArgs a = a_in;
   if (NARROW) {
     a.H = 2048;
     a.E = 256;
+    a.I = 512;
+    a.k = 6;
+    a.S = 1;
   }
   return a;
 }
@@ -373,6 +376,16 @@ __device__ void route_select(const DecodeArgs& a, RouteSmem& R, bool full, bool 
     for (int t = warp; t < a.B; t += nw) topk_token_narrow(a, t, warp, lane, R, full, write_debug, tb, logits);
   } else {
     for (int t = warp; t < a.B; t += nw) topk_token_wide(a, t, warp, lane, R, full, write_debug, tb, logits);
+  }
+  __syncthreads();
+  // The slot table: routed slot S + r is the r-th set bit of `used`.
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+    const uint32_t wd = R.used[e >> 5];
+    if ((wd >> (e & 31)) & 1u) {
+      int r = __popc(wd & ((1u << (e & 31)) - 1u));
+      for (int q = 0; q < (e >> 5); ++q) r += __popc(R.used[q]);
+      R.slot_e[r] = (uint16_t)e;
+    }
   }
   __syncthreads();
   FLINT_TRACE(a, tb < 0 ? -1 : 14);
@@ -415,35 +428,7 @@ __device__ __forceinline__ SlotInfo slot_info(const DecodeArgs& a, const RouteSm
     si.tmask = a.B >= 32 ? 0xFFFFFFFFu : (1u << a.B) - 1u;
     return si;
   }
-  // The r-th set bit of `used`, four words per 16-byte load (words past E / 32
-  // are zero).
-  int r = slot - a.S, w = -1;
-  uint32_t u = 0u;
-  for (int q = 0; q < USED_WORDS && q < (((a.E + 127) >> 7) << 2); q += 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(&R.used[q]);
-    const int c0 = __popc(v.x), c1 = c0 + __popc(v.y), c2 = c1 + __popc(v.z), c3 = c2 + __popc(v.w);
-    if (r < c3) {
-      if (r < c0) {
-        w = q;
-        u = v.x;
-      } else if (r < c1) {
-        w = q + 1;
-        u = v.y;
-        r -= c0;
-      } else if (r < c2) {
-        w = q + 2;
-        u = v.z;
-        r -= c1;
-      } else {
-        w = q + 3;
-        u = v.w;
-        r -= c2;
-      }
-      break;
-    }
-    r -= c3;
-  }
-  si.expert = w >= 0 ? 32 * w + nth_set_bit(u, r) : 0;  // w < 0 only for slot >= route_slots
+  si.expert = R.slot_e[slot - a.S];  // slot < route_slots
   si.tmask = R.mask[si.expert];
   return si;
 }
@@ -876,14 +861,16 @@ __global__ void __maxnreg__(96) k_gateup(const DecodeArgs a_in) {  // 96 registe
     if (u < n_units) issue_w(jj, slot_info(a, R, u / TILES).expert, u % TILES);
   }
   const float* glob = a.globals;
+  int b = 0;          // jj % NB
+  uint32_t par = 0u;  // (jj / NB) & 1
   for (int jj = 0;; ++jj) {
     const int u = unit_of(jj);
     if (u >= n_units) break;  // the same for the 4 warps of the group
-    const int b = jj % NB;
-    const uint32_t par = (uint32_t)((jj / NB) & 1);
     const int slot = u / TILES, tile = u % TILES;
     const SlotInfo si = slot_info(a, R, slot);
     const int expert = si.expert;
+    const float Gg = glob[expert * 4 + 0];  // loaded while the weights are on their way
+    const float Gu = glob[expert * 4 + 1];
     // One token tile (B <= 8): column c is token c. More: column c is the
     // slot's c-th selecting token, so a slot chosen by few tokens needs one tile.
     const int T = NTMAX == 1 ? a.B : __popc(si.tmask);
@@ -942,13 +929,13 @@ __global__ void __maxnreg__(96) k_gateup(const DecodeArgs a_in) {  // 96 registe
       const int u2 = unit_of(jj + NB);
       if (u2 < n_units) issue_w(b, slot_info(a, R, u2 / TILES).expert, u2 % TILES);
     }
-    const float Gg = glob[expert * 4 + 0];
-    const float Gu = glob[expert * 4 + 1];
     const int hoff = frag_offset_elems(tile * 8 + g);
     uint16_t* h = ws_h(a);
     uint16_t* h16 = ws_h16(a);
     unsigned* hmax = ws_hmax(a);
-    for (int pr = gw; pr < 2 * nt_used; pr += 4) {
+    // (token tile, column parity) pairs; one token has no odd column
+    const int npairs = NTMAX == 1 && T == 1 ? 1 : 2 * nt_used;
+    for (int pr = gw; pr < npairs; pr += 4) {
       const int nt = pr >> 1, hh = pr & 1;
       float gs = 0.f, us = 0.f;
 #pragma unroll
@@ -982,6 +969,10 @@ __global__ void __maxnreg__(96) k_gateup(const DecodeArgs a_in) {  // 96 registe
         atomicMax(hmax + row, __float_as_uint(hv));
         if (!(hv < 32768.f)) atomicOr(ws_hdr(a) + HDR_HBIG, 1);  // its f16 copy is not exact
       }
+    }
+    if (++b == NB) {
+      b = 0;
+      par ^= 1u;
     }
   }
   FLINT_TRACE(a, 13);
@@ -2018,9 +2009,9 @@ void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) 
   nb = 0;
 }
 
-// The kernels for the Flint shape (E = 256, H = 2048) are separate
-// instantiations that carry no code for other shapes.
-bool narrow_shape(const DecodeArgs& a) { return a.E == 256 && a.H == 2048; }
+// The kernels for the Flint shape (E = 256, H = 2048, I = 512, top-6, one
+// shared expert) are separate instantiations that carry no code for other shapes.
+bool narrow_shape(const DecodeArgs& a) { return a.E == 256 && a.H == 2048 && a.I == 512 && a.k == 6 && a.S == 1; }
 
 template <int FMT, bool NARROW>
 cudaError_t launch_gateup_n(const DecodeArgs& a, cudaStream_t stream, int ng) {
