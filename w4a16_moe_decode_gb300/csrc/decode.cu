@@ -448,8 +448,7 @@ __device__ __forceinline__ SlotInfo slot_info(const DecodeArgs& a, const RouteSm
 // Tokens t0, t0 + ts, ... (NT of them) of the x chunk.
 template <int NCH, int NT>
 __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* xsm, int H, int lane, float* lg,
-                                            uint32_t* kc, const float* bias, int E, int e, int t0, int ts,
-                                            bool dry) {
+                                            uint32_t* kc, float bias_e, int E, int e, int t0, int ts, bool dry) {
   float acc[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t] = 0.f;
@@ -469,7 +468,7 @@ __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* 
   for (int t = 0; t < NT; ++t) {
     const float v = warp_sum(acc[t]);
     if (lane == t) {
-      const uint32_t key = ordered_key(route_key(v, bias, e));
+      const uint32_t key = ordered_key(sigmoid_f32(v) + bias_e);  // bias_e: 0 without a selection bias
       if (!dry) {
         lg[(t0 + t * ts) * E + e] = v;
         kc[(t0 + t * ts) * E + e] = key;
@@ -512,6 +511,8 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
   int* status = ws_hdr(a) + HDR_STATUS;
   float* lg = ws_logits(a);
   const uint8_t* wrow = wsm + (size_t)(warp % epb) * a.H * 2;
+  // the selection bias of this warp's expert, read before the dependency wait
+  const float bias_e = a.bias && e < a.E ? __ldg(a.bias + e) : 0.f;
   {
     const int n = (a.B < 8 ? a.B : 8) * a.H / 8;  // 16-byte words of the first x chunk
     for (int i = threadIdx.x; i < n; i += blockDim.x) reinterpret_cast<uint4*>(xsm)[i] = make_uint4(0, 0, 0, 0);
@@ -583,9 +584,9 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
         // 3 tokens on (chunks of 8), 2 experts and 2 groups at 2 tokens, 4
         // experts and 1 group at 1 token.
         if (ntw == 1)
-          router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry);
+          router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, kcc, bias_e, a.E, e, tg, G, dry);
         else
-          router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, kcc, a.bias, a.E, e, tg, G, dry);
+          router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, kcc, bias_e, a.E, e, tg, G, dry);
         if (!dry) FLINT_TRACE(a, 7);
       }
       fence_proxy_async();  // the zeroing stores and these reads come before the copy into the buffer
@@ -1190,6 +1191,7 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
     const int Tc = min(8, a.B - 8 * nt);
     const int b = j % NBUF;
     const uint32_t parity = (uint32_t)((j / NBUF) & 1);
+    const float Gd = a.globals[expert * 4 + 2];  // loaded while the copies are on their way
     if (!mbar_wait(&bars[b], parity, status)) {
       for (int jj = j; jj < j + NBUF && warp + nw * jj < n_items; ++jj)
         mbar_drain(&bars[jj % NBUF], (uint32_t)((jj / NBUF) & 1));
@@ -1217,7 +1219,6 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
       else
         tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
     }
-    const float Gd = a.globals[expert * 4 + 2];
     // columns 2 t4 and 2 t4 + 1: their inverse prescales, from lanes n
     const float inv0 = __shfl_sync(0xffffffffu, hinv, 2 * t4), inv1 = __shfl_sync(0xffffffffu, hinv, 2 * t4 + 1);
 #pragma unroll
@@ -1475,6 +1476,7 @@ __global__ void __launch_bounds__(512) k_down(const DecodeArgs a_in) {
       const uint32_t tm = (uint32_t)s_items[4 * it + 3];
       const int expert = s_items[4 * it + 1], rb = rowbase(it) - rb0;
       const int b = j % NBUF;
+      const float Gd = a.globals[expert * 4 + 2];  // loaded while the copies are on their way
       if (!mbar_wait(&wbars[b], (uint32_t)((j / NBUF) & 1), status)) {
         for (int jj = j; jj < j + NBUF && warp + nw * jj < n_items; ++jj)
           mbar_drain(&wbars[jj % NBUF], (uint32_t)((jj / NBUF) & 1));
@@ -1502,7 +1504,6 @@ __global__ void __launch_bounds__(512) k_down(const DecodeArgs a_in) {
         else
           tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
       }
-      const float Gd = a.globals[expert * 4 + 2];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int n = 2 * t4 + hh;
