@@ -58,7 +58,7 @@ struct DecodeArgs {
   int prenorm;
   const uint16_t* gamma;
   float eps;
-  int router_epb;  // experts per router block (4, 2 or 1): the block's 4 warps split its tokens
+  int router_epb;  // experts per router block; the block's warps split its tokens into nw / epb groups
   int x_host;      // x is pinned host memory: the router reads it with plain loads, not a bulk copy
   int dn_nbuf;     // down tiles in flight per warp
   int dn_hcap;     // h rows the down kernel stages at a time
@@ -345,6 +345,22 @@ __device__ void topk_token_narrow(const DecodeArgs& a, int t, int warp, int lane
   if (t == 0) FLINT_TRACE(a, tb < 0 ? -1 : tb + 2);
 }
 
+// Rank of selected expert e among the selected experts (its routed slot is
+// S + rank): the set bits of `used` below e.
+template <bool NARROW>
+__device__ __forceinline__ int used_rank(const DecodeArgs& a, const RouteSmem& R, int e) {
+  const int w = e >> 5;
+  int r = __popc(R.used[w] & ((1u << (e & 31)) - 1u));
+  if (NARROW) {  // 8 words, loaded at once
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < w) r += __popc(R.used[q]);
+  } else {
+    for (int q = 0; q < w; ++q) r += __popc(R.used[q]);
+  }
+  return r;
+}
+
 // Whole block, after route_clear and a barrier: selects every token's experts
 // (one warp per token) from logits [B][E] and ends with a barrier. Without
 // `full` only the selection bitmaps are built; with it also the weights. tb:
@@ -379,14 +395,8 @@ __device__ void route_select(const DecodeArgs& a, RouteSmem& R, bool full, bool 
   }
   __syncthreads();
   // The slot table: routed slot S + r is the r-th set bit of `used`.
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-    const uint32_t wd = R.used[e >> 5];
-    if ((wd >> (e & 31)) & 1u) {
-      int r = __popc(wd & ((1u << (e & 31)) - 1u));
-      for (int q = 0; q < (e >> 5); ++q) r += __popc(R.used[q]);
-      R.slot_e[r] = (uint16_t)e;
-    }
-  }
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x)
+    if ((R.used[e >> 5] >> (e & 31)) & 1u) R.slot_e[used_rank<NARROW>(a, R, e)] = (uint16_t)e;
   __syncthreads();
   FLINT_TRACE(a, tb < 0 ? -1 : 14);
 }
@@ -484,12 +494,13 @@ static __device__ __noinline__ void load_rows_plain(uint8_t* dst, const uint8_t*
 }
 
 template <int NCH, int PRE>
-__global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
+__global__ void __launch_bounds__(512) k_router(DecodeArgs a) {
   const int prenorm = PRE < 0 ? a.prenorm : PRE;
   extern __shared__ __align__(128) uint8_t dsm[];  // router rows [4][H], norm weight [H], x chunk [<= 8][H]
   __shared__ __align__(8) uint64_t bars[2];        // 0: router rows, 1: x
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int epb = a.router_epb, G = 4 / epb;  // experts per block, token groups
+  const int nw = blockDim.x >> 5;
+  const int epb = a.router_epb, G = nw / epb;  // experts per block, token groups
   const int e0 = blockIdx.x * epb, e = e0 + warp % epb, tg = warp / epb;
   const int nrows = min(epb, a.E - e0);
   uint8_t* wsm = dsm;
@@ -551,7 +562,7 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
         }
         FLINT_TRACE(a, 2);
         if (prenorm) {  // RMSNorm of the chunk's rows, in place
-          for (int t = warp; t < nt; t += 4) {
+          for (int t = warp; t < nt; t += nw) {
             uint8_t* row = xsm + (size_t)t * a.H * 2;
             float part = 0.f;
 #pragma unroll
@@ -580,9 +591,7 @@ __global__ void __launch_bounds__(128) k_router(DecodeArgs a) {
         float* lgc = lg + (size_t)t0 * a.E;
         uint32_t* kcc = ws_keys(a) + (size_t)t0 * a.E;
         // One code path per token count, no predicated-off work. A warp has at
-        // most 2 tokens of a chunk: 1 expert per block and 4 token groups from
-        // 3 tokens on (chunks of 8), 2 experts and 2 groups at 2 tokens, 4
-        // experts and 1 group at 1 token.
+        // most 2 tokens of a chunk (at least 4 token groups from 3 tokens on).
         if (ntw == 1)
           router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, kcc, bias_e, a.E, e, tg, G, dry);
         else
@@ -1039,6 +1048,17 @@ static __device__ __noinline__ float h_rows_prescaled(const unsigned* hmax, cons
   return inv;
 }
 
+// The small-batch down kernel's two shapes: 8 warps with 2 tiles in flight
+// each (1 and 2 tokens, beside a gate/up block), or 16 warps with 1.
+constexpr int DOWN_ITEMS_NW = 8, DOWN_ITEMS_NBUF = 2, DOWN_ITEMS_WIDE_NW = 16, DOWN_ITEMS_WIDE_NBUF = 1;
+__host__ __device__ constexpr int down_items_warps(int nbuf) { return nbuf == DOWN_ITEMS_NBUF ? DOWN_ITEMS_NW : DOWN_ITEMS_WIDE_NW; }
+
+// A compile-time flag as a value (selects a copy of a generic lambda's body).
+template <bool V>
+struct BoolTag {
+  static constexpr bool value = V;
+};
+
 struct DownItemsPlan {
   int buf_bytes, hrows, hstride;
   size_t acc_off, items_off, bar_off, total;
@@ -1047,13 +1067,12 @@ struct DownItemsPlan {
 __host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, int max_slots, int fmt, int nbuf, int nw) {
   DownItemsPlan p;
   const int kgb = fmt == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
-  const int nt = (B + 7) / 8;
   p.hrows = B < 8 ? B : 8;
   p.hstride = I * 2 + 16;
   p.buf_bytes = (I / KG_COLS) * kgb + p.hrows * p.hstride;
   size_t o = (size_t)nw * nbuf * p.buf_bytes;
   p.acc_off = o;    o += sizeof(float) * nw * B * 16;
-  p.items_off = o;  o += sizeof(int) * 2 * max_slots * nt;
+  p.items_off = o;  o += sizeof(float) * 8 * max_slots;  // routing weights [slot][token]
   o = (o + 15) & ~(size_t)15;
   p.bar_off = o;    o += sizeof(uint64_t) * nw * nbuf;
   p.total = o;
@@ -1064,19 +1083,17 @@ template <int FMT, int NBUF, bool NARROW, int PRE>
 __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
   const DecodeArgs a = flint_shape<NARROW>(a_in);
   const int prenorm = PRE < 0 ? a.prenorm : PRE;
+  constexpr int NW = down_items_warps(NBUF);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
-  __shared__ int s_wsum[MAX_WARPS];
-  __shared__ uint16_t s_res[MAX_BATCH * 16];  // residual values (pre-norm block)
+  __shared__ uint16_t s_res[8 * 16];  // residual values (pre-norm block)
   constexpr int KGB = FMT == FLINT_MOE_NVFP4 ? KG_NVFP4 : KG_BF16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-  const int nw = blockDim.x >> 5;
   const int tile = blockIdx.x;
-  const int NT = (a.B + 7) / 8;  // token tiles
-  const DownItemsPlan P = down_items_plan(a.H, a.I, a.B, a.W.max_slots, FMT, NBUF, nw);
+  const DownItemsPlan P = down_items_plan(a.H, a.I, a.B, a.W.max_slots, FMT, NBUF, NW);
   const int dn_bytes = (int)a.L.dn_tile;
   float* acc_s = reinterpret_cast<float*>(smem + P.acc_off);
-  int* s_items = reinterpret_cast<int*>(smem + P.items_off);  // per item: slot << 16 | tile << 8 | tokens, expert
+  float* s_sw = reinterpret_cast<float*>(smem + P.items_off);  // [slot][8]: routing weight of token n
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off) + warp * NBUF;
   auto buf = [&](int b) { return smem + (size_t)(warp * NBUF + b) * P.buf_bytes; };
   int* status = ws_hdr(a) + HDR_STATUS;
@@ -1084,7 +1101,7 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
   FLINT_TRACE(a, 16);
   if (lane < NBUF) mbar_init(&bars[lane], 2);  // one arrival for the weights, one for the h rows
   fence_mbar_init();
-  for (int i = threadIdx.x; i < nw * a.B * 16; i += blockDim.x) acc_s[i] = 0.f;
+  for (int i = threadIdx.x; i < NW * a.B * 16; i += blockDim.x) acc_s[i] = 0.f;
   route_clear(R, a.E);
   __syncthreads();
 
@@ -1095,71 +1112,43 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
       bulk_g2s_stream(buf(j % NBUF), src, (uint32_t)dn_bytes, &bars[j % NBUF]);
     }
   };
-  // Items are (slot, token tile) pairs, slot-major. The shared experts' items
-  // come first and cover every token tile, so they are known before routing.
+  // Up to 8 tokens (one token tile) a slot is one work item: warp w takes
+  // slots w, w + NW, .... The shared experts' slots come first and are known
+  // before routing.
   int w_issued = 0;
-  for (int i = warp; i < a.S * NT && w_issued < NBUF; i += nw, ++w_issued) issue_weights(w_issued, a.E + i / NT);
+  for (int i = warp; i < a.S && w_issued < NBUF; i += NW, ++w_issued) issue_weights(w_issued, a.E + i);
 
   // k_gateup lets this kernel launch only after its own wait, so the router has
   // finished: route now and fetch the routed down tiles while k_gateup runs.
   route_select<NARROW>(a, R, true, blockIdx.x == 0, -1, ws_logits(a));
   FLINT_TRACE(a, 17);
-  const int n_slots = route_slots(a, R);
-  {
-    const int spt = (n_slots + blockDim.x - 1) / blockDim.x;
-    const int s0 = threadIdx.x * spt;
-    int local = 0;
-    for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
-      const uint32_t tm = slot_info(a, R, s).tmask;
-      for (int nt = 0; nt < NT; ++nt) local += ((tm >> (8 * nt)) & 0xFFu) != 0u;
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
-    int run = incl - local;
-    for (int w2 = 0; w2 < warp; ++w2) run += s_wsum[w2];
-    for (int s = s0; s < s0 + spt && s < n_slots; ++s) {
-      const SlotInfo si = slot_info(a, R, s);
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t bits = (si.tmask >> (8 * nt)) & 0xFFu;
-        if (bits) {
-          s_items[2 * run] = (s << 16) | (nt << 8) | (int)bits;
-          s_items[2 * run + 1] = si.expert;
-          ++run;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  int n_items = 0;
-  for (int w2 = 0; w2 < nw; ++w2) n_items += s_wsum[w2];
-  auto item_of = [&](int j, int& s, int& nt, uint32_t& bits, int& expert) {
-    const int it = s_items[2 * (warp + nw * j)];
-    s = it >> 16;
-    nt = (it >> 8) & 0xFF;
-    bits = (uint32_t)it & 0xFFu;
-    expert = s_items[2 * (warp + nw * j) + 1];
+  const int n_items = route_slots(a, R);
+  auto item_of = [&](int j, int& s, uint32_t& bits, int& expert) {
+    s = warp + NW * j;
+    const SlotInfo si = slot_info(a, R, s);
+    expert = si.expert;
+    bits = si.tmask & 0xFFu;
   };
-  for (int j = w_issued; j < NBUF && warp + nw * j < n_items; ++j) {
-    int s, nt, e;
+  for (int j = w_issued; j < NBUF && warp + NW * j < n_items; ++j) {
+    int s, e;
     uint32_t bits;
-    item_of(j, s, nt, bits, e);
+    item_of(j, s, bits, e);
     issue_weights(j, e);
   }
+  // The combine's routing weights, by slot and token: entry (slot of the
+  // r-th pick of token t, t) = the pick's weight (entries of tokens that did
+  // not select the slot's expert are never read; shared slots weigh 1).
+  for (int i = threadIdx.x; i < a.B * a.k; i += blockDim.x)
+    s_sw[(a.S + used_rank<NARROW>(a, R, R.idx[i])) * 8 + i / a.k] = R.w[i];
 
-  // Token tile nt of slot s is h rows s * B + 8 nt + n, n < 8; only the rows
-  // of tokens that selected the expert are copied (column n of the product is
-  // token n, and the other columns are never combined).
+  // Slot s is h rows s * B + n, n < B; only the rows of tokens that selected
+  // the expert are copied (column n of the product is token n, and the other
+  // columns are never combined).
   auto issue_h = [&](int j) {
-    int s, nt, e;
+    int s, e;
     uint32_t bits;
-    item_of(j, s, nt, bits, e);
-    const int r0 = s * a.B + 8 * nt;
+    item_of(j, s, bits, e);
+    const int r0 = s * a.B;
     const int b = j % NBUF;
     if (lane == 0) mbar_arrive_expect_tx(&bars[b], (uint32_t)(__popc(bits) * a.I * 2));
     __syncwarp();
@@ -1173,84 +1162,92 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
   if (prenorm)
     for (int p = threadIdx.x; p < a.B * 16; p += blockDim.x)
       s_res[p] = __ldcg(a.x + (size_t)(p >> 4) * a.H + tile * 16 + (p & 15));
-  pdl_wait();  // h comes from k_gateup
+  __syncthreads();  // the weight table is complete
+  pdl_wait();       // h comes from k_gateup
   pdl_trigger();
   FLINT_TRACE(a, 18);
-  for (int j = 0; j < NBUF && warp + nw * j < n_items; ++j) issue_h(j);
+  for (int j = 0; j < NBUF && warp + NW * j < n_items; ++j) issue_h(j);
   // h is consumed in its f16 copy, exact for |h| < 2^15, so the products run
   // in f16 with the dequantised weights as they are (exact in f16): no
   // conversion, no per-row prescale, no block barrier between the wait and
   // the products. Only if some |h| of the call reached 2^15 (the flag is read
   // while the copies are on their way) does each item rebuild its rows from
-  // the bf16 h with a per-row power-of-two prescale.
+  // the bf16 h with a per-row power-of-two prescale: a second copy of the
+  // item loop, so that the common one carries no call.
   const bool hbig = __ldcg(ws_hdr(a) + HDR_HBIG) != 0;
-  for (int j = 0; warp + nw * j < n_items; ++j) {
-    int s, nt, expert;
-    uint32_t bits;
-    item_of(j, s, nt, bits, expert);
-    const int Tc = min(8, a.B - 8 * nt);
-    const int b = j % NBUF;
-    const uint32_t parity = (uint32_t)((j / NBUF) & 1);
-    const float Gd = a.globals[expert * 4 + 2];  // loaded while the copies are on their way
-    if (!mbar_wait(&bars[b], parity, status)) {
-      for (int jj = j; jj < j + NBUF && warp + nw * jj < n_items; ++jj)
-        mbar_drain(&bars[jj % NBUF], (uint32_t)((jj / NBUF) & 1));
-      break;
-    }
-    if (j == 0) FLINT_TRACE(a, 19);
-    uint8_t* wb = buf(b);
-    uint8_t* hb = wb + dn_bytes;
-    float hinv = 1.0f;  // this lane's column's inverse prescale (fallback only)
-    if (hbig) hinv = h_rows_prescaled(ws_hmax(a), ws_h(a), a.I, hb, P.hstride, s * a.B + 8 * nt, bits, lane);
-    float acc[2][1][4];
+  auto run_items = [&](auto hbig_tag) {
+    constexpr bool HBIG = decltype(hbig_tag)::value;
+    for (int j = 0; warp + NW * j < n_items; ++j) {
+      int s, expert;
+      uint32_t bits;
+      item_of(j, s, bits, expert);
+      const int b = j % NBUF;
+      const uint32_t parity = (uint32_t)((j / NBUF) & 1);
+      const float Gd = a.globals[expert * 4 + 2];  // loaded while the copies are on their way
+      if (!mbar_wait(&bars[b], parity, status)) {
+        for (int jj = j; jj < j + NBUF && warp + NW * jj < n_items; ++jj)
+          mbar_drain(&bars[jj % NBUF], (uint32_t)((jj / NBUF) & 1));
+        break;
+      }
+      if (j == 0) FLINT_TRACE(a, 19);
+      uint8_t* wb = buf(b);
+      uint8_t* hb = wb + dn_bytes;
+      float hinv = 1.0f;  // this lane's column's inverse prescale (fallback only)
+      if constexpr (HBIG) hinv = h_rows_prescaled(ws_hmax(a), ws_h(a), a.I, hb, P.hstride, s * a.B, bits, lane);
+      float acc[2][1][4];
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[c][0][i] = 0.f;
-    const int nrow = g < Tc ? g : Tc - 1;
+        for (int i = 0; i < 4; ++i) acc[c][0][i] = 0.f;
+      const int nrow = g < a.B ? g : a.B - 1;
 #pragma unroll 4
-    for (int kg = 0; kg < KG; ++kg) {
-      const uint8_t* rp = hb + nrow * P.hstride + kg * 128 + t4 * 32;
-      uint4 bx[1][2];
-      bx[0][0] = lds128(rp);
-      bx[0][1] = lds128(rp + 16);
-      if (kg & 1)
-        tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[1]);
-      else
-        tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
-    }
-    // columns 2 t4 and 2 t4 + 1: their inverse prescales, from lanes n
-    const float inv0 = __shfl_sync(0xffffffffu, hinv, 2 * t4), inv1 = __shfl_sync(0xffffffffu, hinv, 2 * t4 + 1);
+      for (int kg = 0; kg < KG; ++kg) {
+        const uint8_t* rp = hb + nrow * P.hstride + kg * 128 + t4 * 32;
+        uint4 bx[1][2];
+        bx[0][0] = lds128(rp);
+        bx[0][1] = lds128(rp + 16);
+        if (kg & 1)
+          tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[1]);
+        else
+          tile_kgroup<FMT, 1>(wb + kg * KGB, bx, 1, lane, acc[0]);
+      }
+      float inv0 = 1.0f, inv1 = 1.0f;
+      if constexpr (HBIG) {  // columns 2 t4 and 2 t4 + 1: their inverse prescales, from lanes n
+        inv0 = __shfl_sync(0xffffffffu, hinv, 2 * t4);
+        inv1 = __shfl_sync(0xffffffffu, hinv, 2 * t4 + 1);
+      }
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int n = 2 * t4 + hh;
-      if (n < Tc && ((bits >> n) & 1u)) {
-        const int tok = 8 * nt + n;
-        float wt = 1.0f;  // the shared experts are unweighted
-        if (s >= a.S)
-          for (int r = 0; r < a.k; ++r)
-            if (R.idx[tok * a.k + r] == expert) wt = R.w[tok * a.k + r];
-        const float inv = hh ? inv1 : inv0;
-        float* dst = acc_s + (warp * a.B + tok) * 16;
-        dst[g] += wt * (((acc[0][0][hh] + acc[1][0][hh]) * inv) * Gd);
-        dst[g + 8] += wt * (((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * inv) * Gd);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int n = 2 * t4 + hh;  // the column's token
+        if (n < a.B && ((bits >> n) & 1u)) {
+          const float wt = s < a.S ? 1.0f : s_sw[s * 8 + n];  // the shared experts are unweighted
+          const float inv = hh ? inv1 : inv0;
+          float* dst = acc_s + (warp * a.B + n) * 16;
+          dst[g] += wt * (((acc[0][0][hh] + acc[1][0][hh]) * inv) * Gd);
+          dst[g + 8] += wt * (((acc[0][0][2 + hh] + acc[1][0][2 + hh]) * inv) * Gd);
+        }
+      }
+      __syncwarp();
+      if (warp + NW * (j + NBUF) < n_items) {
+        fence_proxy_async();  // this warp's accesses to the buffer come before the copies into it
+        int s2, e2;
+        uint32_t bits2;
+        item_of(j + NBUF, s2, bits2, e2);
+        issue_weights(j + NBUF, e2);
+        issue_h(j + NBUF);
       }
     }
-    __syncwarp();
-    if (warp + nw * (j + NBUF) < n_items) {
-      fence_proxy_async();  // this warp's accesses to the buffer come before the copies into it
-      int s2, nt2, e2;
-      uint32_t bits2;
-      item_of(j + NBUF, s2, nt2, bits2, e2);
-      issue_weights(j + NBUF, e2);
-      issue_h(j + NBUF);
-    }
-  }
+  };
+  if (hbig)
+    run_items(BoolTag<true>{});
+  else
+    run_items(BoolTag<false>{});
   __syncthreads();
   for (int p = threadIdx.x; p < a.B * 16; p += blockDim.x) {
     const int t = p >> 4, r = p & 15;
     float v = 0.f;
-    for (int w2 = 0; w2 < nw; ++w2) v += acc_s[(w2 * a.B + t) * 16 + r];
+#pragma unroll
+    for (int w2 = 0; w2 < NW; ++w2) v += acc_s[(w2 * a.B + t) * 16 + r];
     __nv_bfloat16 o = __float2bfloat16_rn(v);
     if (prenorm) {  // residual stream: r + bf16(layer output), rounded to bf16
       const uint32_t rb = (uint32_t)s_res[p] << 16;
@@ -1866,6 +1863,9 @@ constexpr size_t SMEM_LIMIT = 227 * 1024;
 
 // Experts per router block: the four warps of a block split its tokens.
 int router_epb(int B) { return B <= 1 ? 4 : (B == 2 ? 2 : 1); }
+// Warps per router block: 4, so that a warp has at most 2 tokens of a chunk
+// of 8 (nw / epb >= 4 token groups from 3 tokens on).
+int router_warps(int B) { return 4; }
 
 // Router rows of one block, the norm weight and one x chunk of up to 8 tokens.
 size_t router_smem(int H, int B) { return (size_t)(router_epb(B) + 1 + (B < 8 ? B : 8)) * H * 2; }
@@ -2047,7 +2047,6 @@ cudaError_t launch_down(const DecodeArgs& a, cudaStream_t stream, const DownPlan
 
 // Up to 2 tokens the block shares its SM with a gate/up block: 8 warps, two
 // buffers each. From 3 tokens on it runs alone: 16 warps, one buffer each.
-constexpr int DOWN_ITEMS_NW = 8, DOWN_ITEMS_NBUF = 2, DOWN_ITEMS_WIDE_NW = 16, DOWN_ITEMS_WIDE_NBUF = 1;
 size_t down_items_smem(const DecodeArgs& a) {
   const bool wide = a.B >= 3;
   return down_items_plan(a.H, a.I, a.B, a.W.max_slots, a.fmt, wide ? DOWN_ITEMS_WIDE_NBUF : DOWN_ITEMS_NBUF,
@@ -2056,22 +2055,22 @@ size_t down_items_smem(const DecodeArgs& a) {
 }
 
 cudaError_t launch_router(const DecodeArgs& a, cudaStream_t stream) {
-  const dim3 grid((a.E + a.router_epb - 1) / a.router_epb);
+  const dim3 grid((a.E + a.router_epb - 1) / a.router_epb), block(32 * router_warps(a.B));
   const size_t smem = router_smem(a.H, a.B);
   switch (a.H / 256) {
-    case 1: return launch_pdl(k_router<1, -1>, grid, dim3(128), smem, stream, a);
-    case 2: return launch_pdl(k_router<2, -1>, grid, dim3(128), smem, stream, a);
-    case 3: return launch_pdl(k_router<3, -1>, grid, dim3(128), smem, stream, a);
-    case 4: return launch_pdl(k_router<4, -1>, grid, dim3(128), smem, stream, a);
-    case 5: return launch_pdl(k_router<5, -1>, grid, dim3(128), smem, stream, a);
-    case 6: return launch_pdl(k_router<6, -1>, grid, dim3(128), smem, stream, a);
-    case 7: return launch_pdl(k_router<7, -1>, grid, dim3(128), smem, stream, a);
+    case 1: return launch_pdl(k_router<1, -1>, grid, block, smem, stream, a);
+    case 2: return launch_pdl(k_router<2, -1>, grid, block, smem, stream, a);
+    case 3: return launch_pdl(k_router<3, -1>, grid, block, smem, stream, a);
+    case 4: return launch_pdl(k_router<4, -1>, grid, block, smem, stream, a);
+    case 5: return launch_pdl(k_router<5, -1>, grid, block, smem, stream, a);
+    case 6: return launch_pdl(k_router<6, -1>, grid, block, smem, stream, a);
+    case 7: return launch_pdl(k_router<7, -1>, grid, block, smem, stream, a);
     case 8:  // the Flint shape: one instantiation per pre-norm case
-      return a.prenorm ? launch_pdl(k_router<8, 1>, grid, dim3(128), smem, stream, a)
-                       : launch_pdl(k_router<8, 0>, grid, dim3(128), smem, stream, a);
-    case 16: return launch_pdl(k_router<16, -1>, grid, dim3(128), smem, stream, a);
-    case 24: return launch_pdl(k_router<24, -1>, grid, dim3(128), smem, stream, a);
-    case 32: return launch_pdl(k_router<32, -1>, grid, dim3(128), smem, stream, a);
+      return a.prenorm ? launch_pdl(k_router<8, 1>, grid, block, smem, stream, a)
+                       : launch_pdl(k_router<8, 0>, grid, block, smem, stream, a);
+    case 16: return launch_pdl(k_router<16, -1>, grid, block, smem, stream, a);
+    case 24: return launch_pdl(k_router<24, -1>, grid, block, smem, stream, a);
+    case 32: return launch_pdl(k_router<32, -1>, grid, block, smem, stream, a);
     default: return cudaErrorInvalidValue;
   }
 }
