@@ -812,8 +812,14 @@ __device__ __forceinline__ void stage_x(const DecodeArgs& a, uint8_t* xs, int xs
   stage_rows<FMT, NARROW, PRE>(a.x, a.B, a.H, a.prenorm, a.gamma, a.eps, xs, xstride, s_inv, warp, nwarps, lane);
 }
 
-template <int FMT, int NTMAX, bool NARROW, int PRE>
-__global__ void __maxnreg__(96) k_gateup(const DecodeArgs a_in) {  // 96 registers: 3 groups leave room for k_down
+// Registers per thread of the gate/up kernel in its three-group shape (1 and 2
+// tokens), which shares each SM with a down block of 8 warps at 64.
+constexpr int GATEUP_SMALL_REGS = 112;
+
+// REGS: registers per thread; 96 lets five groups fill the register file,
+// GATEUP_SMALL_REGS is for three groups beside a down block (1 and 2 tokens).
+template <int FMT, int NTMAX, bool NARROW, int PRE, int REGS = 96>
+__global__ void __maxnreg__(REGS) k_gateup(const DecodeArgs a_in) {
   const DecodeArgs a = flint_shape<NARROW>(a_in);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ RouteSmem R;
@@ -1980,6 +1986,8 @@ void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) 
       std::max({static_smem(k_gateup<FLINT_MOE_NVFP4, 1, false, -1>), static_smem(k_gateup<FLINT_MOE_NVFP4, 4, false, -1>),
                 static_smem(k_gateup<FLINT_MOE_BF16, 1, false, -1>), static_smem(k_gateup<FLINT_MOE_BF16, 4, false, -1>),
                 static_smem(k_gateup<FLINT_MOE_NVFP4, 1, true, 0>), static_smem(k_gateup<FLINT_MOE_NVFP4, 1, true, 1>),
+                static_smem(k_gateup<FLINT_MOE_NVFP4, 1, true, 0, GATEUP_SMALL_REGS>),
+                static_smem(k_gateup<FLINT_MOE_NVFP4, 1, true, 1, GATEUP_SMALL_REGS>),
                 static_smem(k_gateup<FLINT_MOE_NVFP4, 4, true, -1>)});
   const int ntmax = (B + 7) / 8;
   const size_t budget = B <= 2 ? 110 * 1024 : SMEM_LIMIT;
@@ -2023,11 +2031,16 @@ cudaError_t launch_gateup_n(const DecodeArgs& a, cudaStream_t stream, int ng) {
   const dim3 block(128 * ng);
   switch (ntmax) {
     case 1:  // up to 8 tokens, the low-latency path: one instantiation per pre-norm case
-      if constexpr (NARROW)
+      if constexpr (NARROW) {
+        if (ng <= 3)
+          return a.prenorm
+                     ? launch_pdl(k_gateup<FMT, 1, NARROW, 1, GATEUP_SMALL_REGS>, dim3(blocks), block, smem, stream, a)
+                     : launch_pdl(k_gateup<FMT, 1, NARROW, 0, GATEUP_SMALL_REGS>, dim3(blocks), block, smem, stream, a);
         return a.prenorm ? launch_pdl(k_gateup<FMT, 1, NARROW, 1>, dim3(blocks), block, smem, stream, a)
                          : launch_pdl(k_gateup<FMT, 1, NARROW, 0>, dim3(blocks), block, smem, stream, a);
-      else
+      } else {
         return launch_pdl(k_gateup<FMT, 1, NARROW, -1>, dim3(blocks), block, smem, stream, a);
+      }
     case 2: return launch_pdl(k_gateup<FMT, 2, NARROW, -1>, dim3(blocks), block, smem, stream, a);
     case 3: return launch_pdl(k_gateup<FMT, 3, NARROW, -1>, dim3(blocks), block, smem, stream, a);
     default: return launch_pdl(k_gateup<FMT, 4, NARROW, -1>, dim3(blocks), block, smem, stream, a);
