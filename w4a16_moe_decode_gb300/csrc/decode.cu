@@ -631,7 +631,7 @@ __device__ __forceinline__ void tile_kgroup(const uint8_t* kp, const uint4 (&bx)
       }
 #pragma unroll
       for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < nt_used) {
+        if (NTMAX == 1 || nt < nt_used) {
           const uint4& q = bx[nt][ks >> 1];
           if (BF16B)
             mma_bf16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
@@ -647,7 +647,7 @@ __device__ __forceinline__ void tile_kgroup(const uint8_t* kp, const uint4 (&bx)
       const uint32_t af[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < nt_used) {
+        if (NTMAX == 1 || nt < nt_used) {
           const uint4& q = bx[nt][ks >> 1];
           mma_bf16(acc[nt], af, (ks & 1) ? q.z : q.x, (ks & 1) ? q.w : q.y);
         }
@@ -900,7 +900,11 @@ __global__ void __maxnreg__(REGS) k_gateup(const DecodeArgs a_in) {
         for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
     const bool ok = mbar_wait(wbar(b), par, status);
     if (jj == 0) FLINT_TRACE(a, 11);
-    if (ok) {
+    // After a failed wait the buffer's copy is let land and the products run on
+    // it all the same (the group stops after them): the loop is not under a
+    // branch, so its mma.sync need no reconvergence of the warp first.
+    if (!ok) mbar_drain(wbar(b), par);
+    {
       int tok[NTMAX];  // column 8 nt + g (past T: a repeat of the last selecting token)
 #pragma unroll
       for (int nt = 0; nt < NTMAX; ++nt)
@@ -912,7 +916,7 @@ __global__ void __maxnreg__(REGS) k_gateup(const DecodeArgs a_in) {
         uint4 bx[NTMAX][2];
 #pragma unroll
         for (int nt = 0; nt < NTMAX; ++nt) {
-          if (nt < nt_used) {  // columns past the slot's tokens repeat a valid row
+          if (NTMAX == 1 || nt < nt_used) {  // columns past the slot's tokens repeat a valid row
             const uint8_t* rp = xs + (size_t)tok[nt] * xstride + kg * 128 + t4 * 32;
             bx[nt][0] = lds128(rp);
             bx[nt][1] = lds128(rp + 16);
@@ -923,8 +927,6 @@ __global__ void __maxnreg__(REGS) k_gateup(const DecodeArgs a_in) {
         else
           tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[0]);
       }
-    } else {
-      mbar_drain(wbar(b), par);
     }
     // Every warp's partial sums go to the group's reduction buffer
     // (double-buffered by unit parity); after the barrier the 2 * nt_used
@@ -1621,7 +1623,10 @@ __global__ void __launch_bounds__(256) k_gemv(GemvArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
   const bool ok = mbar_wait(bar, 0, a.status);
-  if (ok) {
+  // after a failed wait the copy is let land and the products run on it (the
+  // block stops after them): no branch around the loop's mma.sync
+  if (!ok) mbar_drain(bar, 0);
+  {
     int tok[NTMAX];  // column g of token tile nt is token 8 nt + g (past B: a repeat of token B - 1)
 #pragma unroll
     for (int nt = 0; nt < NTMAX; ++nt) tok[nt] = min(nt * 8 + g, a.B - 1);
@@ -1631,7 +1636,7 @@ __global__ void __launch_bounds__(256) k_gemv(GemvArgs a) {
       uint4 bx[NTMAX][2];
 #pragma unroll
       for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < nt_used) {
+        if (NTMAX == 1 || nt < nt_used) {
           const uint8_t* rp = xs + (size_t)tok[nt] * xstride + kg * 128 + t4 * 32;
           bx[nt][0] = lds128(rp);
           bx[nt][1] = lds128(rp + 16);
@@ -1642,8 +1647,6 @@ __global__ void __launch_bounds__(256) k_gemv(GemvArgs a) {
       else
         tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[0]);
     }
-  } else {
-    mbar_drain(bar, 0);
   }
 #pragma unroll
   for (int nt = 0; nt < NTMAX; ++nt)
@@ -1803,7 +1806,10 @@ __global__ void __launch_bounds__(256) k_gemv_split(GemvArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[c][nt][i] = 0.f;
   const bool ok = mbar_wait(bar, 0, a.status);
-  if (ok) {
+  // after a failed wait the copy is let land and the products run on it (the
+  // block stops after them): no branch around the loop's mma.sync
+  if (!ok) mbar_drain(bar, 0);
+  {
     int tok[NTMAX];
 #pragma unroll
     for (int nt = 0; nt < NTMAX; ++nt) tok[nt] = min(nt * 8 + g, a.B - 1);
@@ -1813,7 +1819,7 @@ __global__ void __launch_bounds__(256) k_gemv_split(GemvArgs a) {
       uint4 bx[NTMAX][2];
 #pragma unroll
       for (int nt = 0; nt < NTMAX; ++nt) {
-        if (nt < nt_used) {
+        if (NTMAX == 1 || nt < nt_used) {
           const uint8_t* rp = xs + (size_t)tok[nt] * xstride + kg * 128 + t4 * 32;
           bx[nt][0] = lds128(rp);
           bx[nt][1] = lds128(rp + 16);
@@ -1824,8 +1830,6 @@ __global__ void __launch_bounds__(256) k_gemv_split(GemvArgs a) {
       else
         tile_kgroup<FMT, NTMAX>(wb + kl * KGB, bx, nt_used, lane, acc[0]);
     }
-  } else {
-    mbar_drain(bar, 0);
   }
 #pragma unroll
   for (int nt = 0; nt < NTMAX; ++nt)
