@@ -407,10 +407,11 @@ def gpu_arm(args) -> None:
     def e2e(pool, B, steps, mapped, min_ms=100.0):
         """Through the C ABI with host buffers: every step's x comes from pinned
         host memory and its out goes back to pinned host memory. With mapped,
-        flint_moe_decode is given the pinned host buffers themselves and its
-        kernels read x and write out across NVLink-C2C (the same bytes cross
-        the link, with no copy-engine operation and no break in the
-        programmatic-launch chain between steps); otherwise each step is a
+        flint_moe_decode is given the pinned host buffers themselves: a staging
+        kernel reads x across NVLink-C2C into the workspace and the down kernel
+        writes out across it (the same bytes cross the link, with no
+        copy-engine operation and no break in the programmatic-launch chain
+        between steps); otherwise each step is a
         cudaMemcpyAsync of x, the decode on device buffers and a cudaMemcpyAsync
         of out. The steps of one rotation are captured once into a CUDA graph
         and replayed, as a serving loop would, so the number is not the Python
@@ -809,9 +810,10 @@ def gpu_arm(args) -> None:
         "e2e": None if e2e_us is None else {"value": e2e_us, "unit": "us/layer",
                                             "h2d_bytes_per_step": B * cfg.hidden * 2,
                                             "d2h_bytes_per_step": B * cfg.hidden * 2,
-                                            "transfer": "x read and out written in pinned host memory by the "
-                                                        "decode kernels over NVLink-C2C (no copy-engine operation); "
-                                                        "the copy-engine variant is e2e_copy_engine_us"},
+                                            "transfer": "x and out in pinned host memory: x read once over "
+                                                        "NVLink-C2C into the workspace by a staging kernel, out "
+                                                        "written over the link by the down kernel (no copy-engine "
+                                                        "operation); the copy-engine variant is e2e_copy_engine_us"},
         "gpu_launches": 3 * K * n_regions,
         "cpu_baseline": cpu,
     }

@@ -170,9 +170,11 @@ flint_moe_status flint_moe_layer_set_norm(flint_moe_layer* layer, const uint16_t
 /* One decode step of the MoE layer for B tokens (0 <= B <= 32; B = 0 is a
  * no-op). x: bf16 [B][H]; out: bf16 [B][H]. x and out may be device memory or
  * pinned host memory (cudaHostAlloc / cudaMallocHost, addressable by the
- * device under unified addressing): the kernels then read x and write out
- * across the host link themselves, with no copy before or after; any other
- * host memory is refused with FLINT_MOE_EINVAL. workspace: flint_moe_workspace_bytes
+ * device under unified addressing): with x in host memory a first kernel
+ * copies it across the host link into the workspace, once, and the layer's
+ * kernels read that copy; out in host memory is written by the down kernel
+ * across the link; there is no copy-engine operation before or after. Any
+ * other host memory is refused with FLINT_MOE_EINVAL. workspace: flint_moe_workspace_bytes
  * (cfg, >= B) bytes, initialised once with flint_moe_workspace_init, not shared
  * by decodes in flight at the same time. Three kernels: the router GEMV
  * (logits); gate/up GEMV with SiLU*up over the selected and shared experts;

@@ -59,7 +59,6 @@ struct DecodeArgs {
   const uint16_t* gamma;
   float eps;
   int router_epb;  // experts per router block; the block's warps split its tokens into nw / epb groups
-  int x_host;      // x is pinned host memory: the router reads it with plain loads, not a bulk copy
   int dn_nbuf;     // down tiles in flight per warp
   int dn_hcap;     // h rows the down kernel stages at a time
 };
@@ -487,10 +486,16 @@ __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* 
   }
 }
 
-// n 16-byte words from src (global or pinned host memory) to shared memory,
-// by the threads of the block; out of line, off the device-memory path.
-static __device__ __noinline__ void load_rows_plain(uint8_t* dst, const uint8_t* src, int n) {
-  for (int i = threadIdx.x; i < n; i += blockDim.x) reinterpret_cast<uint4*>(dst)[i] = ld_cg_v4(src + (size_t)i * 16);
+// Calls whose x is pinned host memory: its rows are copied once, by this
+// kernel, into the workspace, and the layer's kernels read that copy (the
+// 16-byte loads cross the host link once, not once per block that needs x).
+__global__ void __launch_bounds__(256) k_stage_x(const DecodeArgs a) {
+  pdl_wait();  // x may be written by earlier work in the stream
+  pdl_trigger();
+  const int n = a.B * a.H / 8;  // 16-byte words
+  uint4* dst = reinterpret_cast<uint4*>(a.ws + a.W.xs);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    dst[i] = ld_cg_v4(reinterpret_cast<const uint8_t*>(a.x) + (size_t)i * 16);
 }
 
 template <int NCH, int PRE>
@@ -547,19 +552,14 @@ __global__ void __launch_bounds__(512) k_router(DecodeArgs a) {
     for (int t0 = 0; t0 < a.B; t0 += 8) {
       const int nt = min(8, a.B - t0);
       if (!dry) {
-        if (a.x_host) {  // x in pinned host memory: 16-byte loads across the host link
-          load_rows_plain(xsm, reinterpret_cast<const uint8_t*>(a.x + (size_t)t0 * a.H), nt * a.H / 8);
-          __syncthreads();
-        } else {
-          if (threadIdx.x == 0) {
-            const uint32_t bytes = (uint32_t)nt * a.H * 2;
-            mbar_arrive_expect_tx(&bars[1], bytes);
-            bulk_g2s(xsm, a.x + (size_t)t0 * a.H, bytes, &bars[1]);
-          }
-          ok = __syncthreads_and(mbar_wait(&bars[1], phase, status));  // block-uniform
-          phase ^= 1;
-          if (!ok) break;
+        if (threadIdx.x == 0) {
+          const uint32_t bytes = (uint32_t)nt * a.H * 2;
+          mbar_arrive_expect_tx(&bars[1], bytes);
+          bulk_g2s(xsm, a.x + (size_t)t0 * a.H, bytes, &bars[1]);
         }
+        ok = __syncthreads_and(mbar_wait(&bars[1], phase, status));  // block-uniform
+        phase ^= 1;
+        if (!ok) break;
         FLINT_TRACE(a, 2);
         if (prenorm) {  // RMSNorm of the chunk's rows, in place
           for (int t = warp; t < nt; t += nw) {
@@ -2192,6 +2192,7 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   a.router_epb = router_epb(B);
   // x and out may be device memory or pinned (device-mapped) host memory;
   // memory the device cannot address is refused before any launch.
+  bool x_host = false;
   {
     cudaPointerAttributes px, po;
     if (cudaPointerGetAttributes(&px, x) != cudaSuccess || cudaPointerGetAttributes(&po, out) != cudaSuccess)
@@ -2201,7 +2202,7 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
              (p.type == cudaMemoryTypeHost && p.devicePointer == p.hostPointer);
     };
     if (!addressable(px) || !addressable(po)) return FLINT_MOE_EINVAL;
-    a.x_host = px.type == cudaMemoryTypeHost ? 1 : 0;
+    x_host = px.type == cudaMemoryTypeHost;
   }
   a.gamma = prenorm ? layer->norm_weight : nullptr;
   a.eps = prenorm ? layer->norm_eps : 0.f;
@@ -2237,7 +2238,13 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
   a.dn_nbuf = dp.nbuf;
   a.dn_hcap = dp.hcap;
   const bool small_down = B <= 8 && a.fmt == FLINT_MOE_NVFP4 && down_items_smem(a) <= down_budget;
-  cudaError_t e = launch_router(a, stream);
+  cudaError_t e = cudaSuccess;
+  if (x_host) {  // one copy of x into the workspace, which the layer's kernels read
+    const int words = B * a.H / 8;
+    e = launch_pdl(k_stage_x, dim3((words + 255) / 256), dim3(256), 0, stream, a);
+    a.x = reinterpret_cast<const uint16_t*>(a.ws + a.W.xs);
+  }
+  if (e == cudaSuccess) e = launch_router(a, stream);
   if (e == cudaSuccess) e = a.fmt == FLINT_MOE_NVFP4 ? launch_gateup<FLINT_MOE_NVFP4>(a, stream, gu_ng)
                                                        : launch_gateup<FLINT_MOE_BF16>(a, stream, gu_ng);
   if (e == cudaSuccess) {
