@@ -185,6 +185,7 @@ def test_decode_flint_batch32_routing_of_every_token():
 
 def test_decode_bf16_weights():
     run_parity(FLINT, 1, seed=0, fmt=fb.BF16)
+    run_parity(FLINT, 2, seed=3, fmt=fb.BF16)
     run_parity(FLINT, 8, seed=0, fmt=fb.BF16)
     run_parity(TINY, 5, seed=1, fmt=fb.BF16)
 

@@ -1982,8 +1982,10 @@ cudaError_t launch_any(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 }
 
 // Warp groups (ng) and buffers per group (nb) of k_gateup: as many units in
-// flight as fit, and for small batches a footprint that leaves room on each SM
-// for a k_down block, which launches early and prefetches meanwhile.
+// flight as fit, and for 1 and 2 tokens of NVFP4 weights a footprint that
+// leaves room on each SM for a down block, which launches early and prefetches
+// meanwhile (a BF16 unit is 3.6 times larger: there the gate/up block takes
+// the SM's shared memory, as more units in flight measured faster).
 void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) {
   // static shared memory of the gate/up kernels, as laid out by the compiler
   static const size_t route =
@@ -1994,12 +1996,12 @@ void gateup_shape(int H, int B, int fmt, int units_per_block, int& ng, int& nb) 
                 static_smem(k_gateup<FLINT_MOE_NVFP4, 1, true, 1, GATEUP_SMALL_REGS>),
                 static_smem(k_gateup<FLINT_MOE_NVFP4, 4, true, -1>)});
   const int ntmax = (B + 7) / 8;
-  const size_t budget = B <= 2 ? 110 * 1024 : SMEM_LIMIT;
+  const size_t budget = B <= 2 && fmt == FLINT_MOE_NVFP4 ? 110 * 1024 : SMEM_LIMIT;
   const int want_nb = units_per_block <= 3 ? 1 : 2;
   // Up to 2 tokens a gate/up block stays small (3 groups) so that a down block
   // runs beside it; larger batches take a fourth and fifth group of warps
   // (five groups of 4 warps at 96 registers fill the register file).
-  const int first = B <= 2 ? 4 : 0;
+  const int first = B <= 2 && fmt == FLINT_MOE_NVFP4 ? 4 : 0;
   const int cand[][2] = {{5, want_nb}, {5, 1}, {4, want_nb}, {4, 1}, {3, want_nb}, {3, 1}, {2, 2}, {2, 1},
                          {1, 3},       {1, 2}, {1, 1}};
   for (int i = first; i < (int)(sizeof(cand) / sizeof(cand[0])); ++i) {
@@ -2231,7 +2233,7 @@ flint_moe_status decode_impl(const flint_moe_layer* layer, const uint16_t* x, in
     gateup_shape(a.H, B, a.fmt, (units + sms - 1) / sms, gu_ng, a.gu_nb);
   }
   DownPlan dp;
-  const size_t down_budget = (B <= 2 ? 110 * 1024 : SMEM_LIMIT) - route_smem;
+  const size_t down_budget = (B <= 2 && a.fmt == FLINT_MOE_NVFP4 ? 110 * 1024 : SMEM_LIMIT) - route_smem;
   if (gu_ng == 0 || !down_shape(a.I, B, a.k, a.S, a.W.max_slots, a.fmt, down_budget, dp) ||
       router_smem(a.H, B) > SMEM_LIMIT)
     return FLINT_MOE_EUNSUPPORTED;

@@ -489,17 +489,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
     // 64 (lw / 4) .. of each tile's accumulator.
     const int lw = warp - p * PCW;
     TileInfo nxt = my_tiles > 0 ? tile_info<MODE>(a, tile_of(0)) : TileInfo{}, t = nxt;
-    const int dq_p = lw, dq_g = lane >> 2, dq_t = lane & 3;
+    const int dq_p = lw, dq_g = lane >> 2;
     const int q4 = lw & 3, cg = lw >> 2;
-    uint32_t doff[4][4];  // this lane's swizzled 4-byte destinations in a stage
+    // The k-step's 16 x 16 fragment goes to shared memory with one
+    // stmatrix.x4: lanes 8 i .. 8 i + 7 address the rows of 8 x 8 matrix i
+    // (rows 8 (i & 1) .., columns 8 (i >> 1) .. of the fragment, the order of
+    // the mma A registers), each a 16-byte swizzled chunk.
+    uint32_t soff[4];
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const int r0 = dq_p * 16 + dq_g, c0 = ks * 16 + 2 * dq_t;
-      doff[ks][0] = sw128_off(r0, c0);
-      doff[ks][1] = sw128_off(r0 + 8, c0);
-      doff[ks][2] = sw128_off(r0, c0 + 8);
-      doff[ks][3] = sw128_off(r0 + 8, c0 + 8);
-    }
+    for (int ks = 0; ks < 4; ++ks)
+      soff[ks] = sw128_off(dq_p * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, ks * 16 + (lane >> 4) * 8);
     const uint32_t tile_off = (uint32_t)(dq_p * RAW_KB * KG_NVFP4);
     int ctok[2] = {0, 0}, cq[2] = {0, 0};  // this lane's two epilogue columns: 64 cg + lane, + 32
     float cw[2] = {0.f, 0.f}, cinv[2] = {1.f, 1.f};
@@ -544,11 +543,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
           for (int ks = 0; ks < 4; ++ks) {
             uint32_t af[4];
             nvfp4_afrag(cw4[ks], sg, sg8, ks, af);
+            if (MODE != GATEUP) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              asm volatile("st.shared.u32 [%0], %1;" ::"r"(ap + doff[ks][q]),
-                           "r"(MODE == GATEUP ? af[q] : f16x2_to_bf16x2(af[q]))
-                           : "memory");
+              for (int q = 0; q < 4; ++q) af[q] = f16x2_to_bf16x2(af[q]);
+            }
+            asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(ap + soff[ks]),
+                         "r"(af[0]), "r"(af[1]), "r"(af[2]), "r"(af[3])
+                         : "memory");
           }
           fence_proxy_async();  // these st.shared -> visible to the tensor core
           __syncwarp();
