@@ -1,6 +1,8 @@
 // Decode step of the Flint-style W4A16 MoE layer on sm_103a: three kernels
 // chained with programmatic dependent launch (PDL), plus the dense GEMV.
 //
+//   k_stage_x     (x in pinned host memory only) copies x once into the
+//                 workspace, where the other kernels read it.
 //   k_router      logits = x Wr^T (FP32 accumulation), optionally on the
 //                 RMS-normalised x; a block's router rows arrive by one bulk
 //                 copy before the wait, its warps split the tokens.
@@ -11,7 +13,7 @@
 //                 the 1 KB-per-token logits, streams its units' packed gate/up
 //                 tiles into shared memory, dequantises into mma fragments and
 //                 writes h = bf16(silu(g) * u).
-//   k_down_items  (up to 4 tokens) / k_down (more): one block per 16 output
+//   k_down_items  (up to 8 tokens) / k_down (more): one block per 16 output
 //                 rows; routes and prefetches its down tiles *before* waiting
 //                 for k_gateup, then, once h exists, multiplies and accumulates
 //                 w * y per warp, adds the warps in a fixed order and writes
