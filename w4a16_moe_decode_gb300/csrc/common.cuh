@@ -93,7 +93,7 @@ enum : int { HDR_STATUS = 1, HDR_HBIG = 2 };
 // small-batch down kernel's f16 products. Slot s (shared experts first, then
 // the distinct selected experts in ascending id) owns rows s * B .. s * B + B - 1.
 struct WsLayout {
-  size_t logits, keys, topk_idx, topk_w, hmax, h, h16, xs, total;
+  size_t logits, keys, topk_idx, topk_w, hmax, h, h16, xs, xn, total;
   int max_slots, max_rows;
   int has_h16;  // the f16 copy of h exists (calls of up to 8 tokens, NVFP4 weights)
 };
@@ -118,6 +118,7 @@ __host__ __device__ inline WsLayout make_ws_layout(int H, int E, int k, int I, i
   W.h = o;        o = ws_align(o + (size_t)2 * W.max_rows * I);
   W.h16 = o;      o = ws_align(o + (with_h16 ? (size_t)2 * W.max_rows * I : 0));
   W.xs = o;       o = ws_align(o + (size_t)2 * maxB * H);  // x staged from host memory
+  W.xn = o;       o = ws_align(o + (size_t)2 * maxB * H);  // the pre-norm block's normalised x
   W.total = o;
   return W;
 }
