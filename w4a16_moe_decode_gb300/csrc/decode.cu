@@ -488,6 +488,49 @@ __device__ __forceinline__ void router_dots(const uint8_t* wrow, const uint8_t* 
   }
 }
 
+// One token's logit of expert e for the pre-norm block of 2 tokens: the
+// warp normalises the token's row (in shared memory, as loaded) itself, the
+// same steps in the same order as every kernel that normalises a row, and
+// feeds each normalised chunk to the dot product as it goes; no warp writes
+// the row back, so no barrier separates the norm from the dot products (the
+// block's warps each do this for their own expert).
+template <int NCH>
+__device__ __forceinline__ void router_dot_normed(const uint8_t* wrow, const uint8_t* xrow, const uint8_t* gsm, int H,
+                                                  float eps, int lane, float* lg, uint32_t* kc, float bias_e, int E,
+                                                  int e, int t, bool dry) {
+  uint4 xv[NCH];
+  float part = 0.f;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    xv[c] = lds128(xrow + (lane + 32 * c) * 16);
+    part = sumsq8(xv[c], part);
+  }
+  const float ss = warp_sum(part);
+  float acc = 0.f;
+  if (ss <= FP32_MAX) {
+    const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int off = (lane + 32 * c) * 16;
+      acc = dot8_bf16(lds128(wrow + off), norm8(xv[c], lds128(gsm + off), inv), acc);
+    }
+  } else {  // the sum of squares overflowed: the scaled path
+    const float2 f = rms_factor_huge(xrow, 1, lane, H, eps);
+    for (int c = 0; c < NCH; ++c) {
+      const int off = (lane + 32 * c) * 16;
+      acc = dot8_bf16(lds128(wrow + off), norm8_huge(xv[c], lds128(gsm + off), f), acc);
+    }
+  }
+  const float v = warp_sum(acc);
+  if (lane == 0) {
+    const uint32_t key = ordered_key(sigmoid_f32(v) + bias_e);  // bias_e: 0 without a selection bias
+    if (!dry) {
+      lg[t * E + e] = v;
+      kc[t * E + e] = key;
+    }
+  }
+}
+
 // Pre-norm calls of NORM_KERNEL_MIN_B tokens or more: one warp per row
 // computes the RMSNorm once (the same steps, in the same order, as every
 // kernel that normalises a row: bit-identical results) and writes the
@@ -606,7 +649,11 @@ __global__ void __launch_bounds__(512) k_router(DecodeArgs a) {
         phase ^= 1;
         if (!ok) break;
         FLINT_TRACE(a, 2);
-        if (prenorm) {  // RMSNorm of the chunk's rows, in place
+        // RMSNorm of the chunk's rows, in place (8 and more tokens arrive
+        // normalised by k_norm_x); 2 tokens: inside the dot products, which
+        // measured faster there (pre-norm stack 16.8 -> 16.2 us per layer) but
+        // not at 1 token (10.8 -> 11.3)
+        if (prenorm && nt != 2) {
           for (int t = warp; t < nt; t += nw) {
             uint8_t* row = xsm + (size_t)t * a.H * 2;
             float part = 0.f;
@@ -637,7 +684,10 @@ __global__ void __launch_bounds__(512) k_router(DecodeArgs a) {
         uint32_t* kcc = ws_keys(a) + (size_t)t0 * a.E;
         // One code path per token count, no predicated-off work. A warp has at
         // most 2 tokens of a chunk (at least 4 token groups from 3 tokens on).
-        if (ntw == 1)
+        if (prenorm && nt == 2)  // one token per warp
+          router_dot_normed<NCH>(wrow, xsm + (size_t)tg * a.H * 2, gsm, a.H, a.eps, lane, lgc, kcc, bias_e, a.E, e,
+                                 tg, dry);
+        else if (ntw == 1)
           router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, kcc, bias_e, a.E, e, tg, G, dry);
         else
           router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, kcc, bias_e, a.E, e, tg, G, dry);
