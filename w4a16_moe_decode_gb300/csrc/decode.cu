@@ -1164,7 +1164,7 @@ struct BoolTag {
 
 struct DownItemsPlan {
   int buf_bytes, hrows, hstride;
-  size_t acc_off, items_off, bar_off, total;
+  size_t acc_off, sw_off, bar_off, total;
 };
 
 __host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, int max_slots, int fmt, int nbuf, int nw) {
@@ -1175,13 +1175,22 @@ __host__ __device__ inline DownItemsPlan down_items_plan(int H, int I, int B, in
   p.buf_bytes = (I / KG_COLS) * kgb + p.hrows * p.hstride;
   size_t o = (size_t)nw * nbuf * p.buf_bytes;
   p.acc_off = o;    o += sizeof(float) * nw * B * 16;
-  p.items_off = o;  o += sizeof(float) * 8 * max_slots;  // routing weights [slot][token]
+  p.sw_off = o;     o += sizeof(float) * 8 * max_slots;  // routing weights [slot][token]
   o = (o + 15) & ~(size_t)15;
   p.bar_off = o;    o += sizeof(uint64_t) * nw * nbuf;
   p.total = o;
   return p;
 }
 
+// ===========================================================================
+// Small-batch down kernel (up to 8 tokens, NVFP4 weights): one block per 16
+// output rows. Up to 8 tokens a slot is one work item; warp w takes slots
+// w, w + NW, ... with NBUF buffers, each holding the slot's 4.6 KB down tile
+// and the f16 rows of h of the tokens that selected its expert. Before its
+// dependency wait the block fetches the down tiles (the shared experts' at
+// once, the routed ones after routing) while k_gateup runs; after it, the h
+// rows. Per-warp partial sums are added in warp order at the end.
+// ===========================================================================
 template <int FMT, int NBUF, bool NARROW, int PRE>
 __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
   const DecodeArgs a = flint_shape<NARROW>(a_in);
@@ -1196,7 +1205,7 @@ __global__ void __launch_bounds__(512) k_down_items(const DecodeArgs a_in) {
   const DownItemsPlan P = down_items_plan(a.H, a.I, a.B, a.W.max_slots, FMT, NBUF, NW);
   const int dn_bytes = (int)a.L.dn_tile;
   float* acc_s = reinterpret_cast<float*>(smem + P.acc_off);
-  float* s_sw = reinterpret_cast<float*>(smem + P.items_off);  // [slot][8]: routing weight of token n
+  float* s_sw = reinterpret_cast<float*>(smem + P.sw_off);  // [slot][8]: routing weight of token n
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bar_off) + warp * NBUF;
   auto buf = [&](int b) { return smem + (size_t)(warp * NBUF + b) * P.buf_bytes; };
   int* status = ws_hdr(a) + HDR_STATUS;
