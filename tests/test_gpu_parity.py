@@ -331,8 +331,13 @@ def test_decode_prenorm_tiny(B, seed, inplace):
 
 
 def test_decode_prenorm_flint():
+    """Pre-norm block at the Flint shape: 1 token (the router normalises in
+    shared memory), 2 (each router warp normalises inside its dot product),
+    8 and 16 (the rows arrive normalised by the normalisation kernel)."""
     run_parity_prenorm(FLINT, 1, seed=23)
+    run_parity_prenorm(FLINT, 2, seed=24)
     run_parity_prenorm(FLINT, 8, seed=1004, layer=4, bias=_stack_bias_vector(), inplace=True)
+    run_parity_prenorm(FLINT, 16, seed=25, layer=2, tokens=[0, 9, 15])
 
 
 def test_decode_batch0_is_a_noop():
@@ -398,7 +403,8 @@ def test_bounded_wait_gives_up_and_reports():
     worst, excluded, _ = run_parity(TINY, 3, seed=5)  # the GPU still decodes correctly
 
 
-@pytest.mark.parametrize("d,B,prenorm", [(TINY, 3, False), (FLINT, 1, False), (FLINT, 8, False), (FLINT, 4, True)])
+@pytest.mark.parametrize("d,B,prenorm", [(TINY, 3, False), (FLINT, 1, False), (FLINT, 8, False), (FLINT, 2, True),
+                                           (FLINT, 4, True), (FLINT, 8, True)])
 def test_decode_with_x_and_out_in_pinned_host_memory(d, B, prenorm):
     """x and out in pinned host memory (the kernels read and write them across
     the host link): bit-identical to the same decode on device buffers, with
