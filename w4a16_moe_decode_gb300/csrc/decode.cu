@@ -589,6 +589,9 @@ __global__ void __launch_bounds__(256) k_stage_x(const DecodeArgs a) {
 template <int NCH, int PRE>
 __global__ void __launch_bounds__(512) k_router(DecodeArgs a) {
   const int prenorm = PRE < 0 ? a.prenorm : PRE;
+  // 2 pre-norm tokens normalised inside the dot products (rows of up to 2048:
+  // a lane keeps its NCH chunks in registers)
+  constexpr bool FUSED_NORM2 = NCH <= 8;
   extern __shared__ __align__(128) uint8_t dsm[];  // router rows [4][H], norm weight [H], x chunk [<= 8][H]
   __shared__ __align__(8) uint64_t bars[2];        // 0: router rows, 1: x
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -653,7 +656,7 @@ __global__ void __launch_bounds__(512) k_router(DecodeArgs a) {
         // normalised by k_norm_x); 2 tokens: inside the dot products, which
         // measured faster there (pre-norm stack 16.8 -> 16.2 us per layer) but
         // not at 1 token (10.8 -> 11.3)
-        if (prenorm && nt != 2) {
+        if (prenorm && (nt != 2 || !FUSED_NORM2)) {
           for (int t = warp; t < nt; t += nw) {
             uint8_t* row = xsm + (size_t)t * a.H * 2;
             float part = 0.f;
@@ -684,10 +687,16 @@ __global__ void __launch_bounds__(512) k_router(DecodeArgs a) {
         uint32_t* kcc = ws_keys(a) + (size_t)t0 * a.E;
         // One code path per token count, no predicated-off work. A warp has at
         // most 2 tokens of a chunk (at least 4 token groups from 3 tokens on).
-        if (prenorm && nt == 2)  // one token per warp
-          router_dot_normed<NCH>(wrow, xsm + (size_t)tg * a.H * 2, gsm, a.H, a.eps, lane, lgc, kcc, bias_e, a.E, e,
-                                 tg, dry);
-        else if (ntw == 1)
+        bool done = false;
+        if constexpr (FUSED_NORM2) {
+          if (prenorm && nt == 2) {  // one token per warp
+            router_dot_normed<NCH>(wrow, xsm + (size_t)tg * a.H * 2, gsm, a.H, a.eps, lane, lgc, kcc, bias_e, a.E,
+                                   e, tg, dry);
+            done = true;
+          }
+        }
+        if (done) {
+        } else if (ntw == 1)
           router_dots<NCH, 1>(wrow, xsm, a.H, lane, lgc, kcc, bias_e, a.E, e, tg, G, dry);
         else
           router_dots<NCH, 2>(wrow, xsm, a.H, lane, lgc, kcc, bias_e, a.E, e, tg, G, dry);
