@@ -636,58 +636,49 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   }
 }
 
-// One block per token, after the plan: the token's entries of the grouped
-// row lists (token, slot rank, routing weight), and its gate/up activations in
+// One warp per token, after the plan: the token's entries of the grouped row
+// lists (token, slot rank, routing weight), and its gate/up activations in
 // f16 for the tensor cores: a power of two 2^kx maps the row's largest |x|
 // into [2^14, 2^15), so every bf16 value is exact in f16 (down to 2^-24 of
 // that bound, below which the tail flushes; the epilogue multiplies by
 // 2^-kx). The row goes to x16 and to the grouped rows of its k routed pairs.
 __global__ void __launch_bounds__(256) k_pf_token_rows(PfArgs a) {
-  __shared__ float red[8];
-  const int t = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= a.B) return;
   const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H);
   const int nw = a.H / 8;
+  // Lane q < S + k: list row q of the token (its S shared rows s B + t, then
+  // its k routed rows rowbase[e_j] + pos_j, the token's place in e_j's list).
+  int row = 0;
+  if (lane < a.S + a.k) {
+    float w = 1.0f;
+    if (lane < a.S) {
+      row = lane * a.B + t;
+    } else {
+      const size_t p = (size_t)t * a.k + (lane - a.S);
+      const int e = __ldcg(ws_at<const int>(a, a.W.idx) + p);
+      row = __ldcg(ws_at<const int>(a, a.W.rowbase) + e) + __ldcg(ws_at<const int>(a, a.W.pos) + p);
+      w = __ldcg(ws_at<const float>(a, a.W.w) + p);
+    }
+    ws_at<int>(a, a.W.list_tok)[row] = t;
+    ws_at<int>(a, a.W.list_q)[row] = lane;
+    ws_at<float>(a, a.W.list_w)[row] = w;
+  }
   float m = 0.f;
-  for (int i = threadIdx.x; i < nw; i += blockDim.x) {
+#pragma unroll 4
+  for (int i = lane; i < nw; i += 32) {
     const uint4 v = __ldg(src + i);
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(w4[j])), fabsf(bf16hi(w4[j]))));
   }
-  m = warp_max(m);
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  m = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
-  const int kx = prescale_exp(m);
+  const int kx = prescale_exp(warp_max(m));
   const float sc = exp2i(kx);
-  if (threadIdx.x == 0) ws_at<int>(a, a.W.kx)[t] = kx;
-  // This token's entries of the grouped lists: its S shared rows s B + t and
-  // its k routed rows rowbase[e_j] + pos_j (the token's place in expert e_j's list).
-  int rows[MAX_TOPK];
-  for (int j = 0; j < a.k; ++j) {
-    const size_t p = (size_t)t * a.k + j;
-    const int e = __ldcg(ws_at<const int>(a, a.W.idx) + p);
-    rows[j] = __ldcg(ws_at<const int>(a, a.W.rowbase) + e) + __ldcg(ws_at<const int>(a, a.W.pos) + p);
-  }
-  if (threadIdx.x < a.S + a.k) {
-    const int q = threadIdx.x;
-    int row;
-    float w = 1.0f;
-    if (q < a.S) {
-      row = q * a.B + t;
-    } else {
-      row = rows[q - a.S];
-      w = __ldcg(ws_at<const float>(a, a.W.w) + (size_t)t * a.k + (q - a.S));
-    }
-    ws_at<int>(a, a.W.list_tok)[row] = t;
-    ws_at<int>(a, a.W.list_q)[row] = q;
-    ws_at<float>(a, a.W.list_w)[row] = w;
-  }
-  for (int j = 0; j < a.k; ++j) rows[j] -= a.S * a.B;  // grouped routed row (activation copy)
+  if (lane == 0) ws_at<int>(a, a.W.kx)[t] = kx;
   uint4* x16 = ws_at<uint4>(a, a.W.x16) + (size_t)t * nw;
   uint4* xg = ws_at<uint4>(a, a.W.xg);
-  for (int i = threadIdx.x; i < nw; i += blockDim.x) {
+  for (int i = lane; i < nw; i += 32) {
     const uint4 v = __ldg(src + i);
     uint4 o;
     o.x = bf16x2_to_f16x2_scaled(v.x, sc);
@@ -695,7 +686,10 @@ __global__ void __launch_bounds__(256) k_pf_token_rows(PfArgs a) {
     o.z = bf16x2_to_f16x2_scaled(v.z, sc);
     o.w = bf16x2_to_f16x2_scaled(v.w, sc);
     x16[i] = o;
-    for (int j = 0; j < a.k; ++j) xg[(size_t)rows[j] * nw + i] = o;
+    for (int j = 0; j < a.k; ++j) {  // grouped routed row (activation copy)
+      const int r = __shfl_sync(0xffffffffu, row, a.S + j) - a.S * a.B;
+      xg[(size_t)r * nw + i] = o;
+    }
   }
 }
 
@@ -708,13 +702,14 @@ __device__ __forceinline__ uint32_t order_f32(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+template <int PER>
 __global__ void __launch_bounds__(256) k_pf_topk(PfArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= a.B) return;
-  constexpr int PER = MAX_E / 32;
   float* logits = ws_at<float>(a, a.W.logits) + (size_t)t * a.E;
   const float* part = ws_at<const float>(a, a.W.y) + (size_t)t * a.E;  // split partials (rsplit > 1)
+  const size_t plane = (size_t)a.B * a.E;
   float s[PER];
   uint32_t key[PER];
   uint32_t taken = 0;
@@ -725,57 +720,74 @@ __global__ void __launch_bounds__(256) k_pf_topk(PfArgs a) {
     key[i] = 0u;
     if (e < a.E) {
       float l;
-      if (a.rsplit > 1) {  // the splits' partial sums, added in split order
-        l = __ldcg(part + e);
-        for (int q = 1; q < a.rsplit; ++q) l += __ldcg(part + (size_t)q * a.B * a.E + e);
+      if (a.rsplit > 1) {  // the splits' partial sums, all loaded at once, added in split order
+        float pq[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pq[q] = q < a.rsplit ? __ldcg(part + q * plane + e) : 0.f;
+        l = pq[0];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+          if (q < a.rsplit) l += pq[q];
         logits[e] = l;
       } else {
         l = __ldcg(logits + e);
       }
       s[i] = 1.0f / (1.0f + expf(-l));
-      key[i] = order_f32(s[i] + (a.bias ? a.bias[e] : 0.f));
+      key[i] = order_f32(s[i] + (a.bias ? __ldg(a.bias + e) : 0.f));
     } else {
       taken |= 1u << i;
     }
   }
+  // k rounds of a warp arg-max; every lane ends with every rank's expert and sigmoid.
   int sel_e[MAX_TOPK];
   float sel_s[MAX_TOPK];
-  for (int j = 0; j < a.k; ++j) {
-    uint64_t best = 0;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const uint64_t c = ((uint64_t)key[i] << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)(lane + 32 * i));
-      if (!((taken >> i) & 1u) && c > best) best = c;
+  for (int j = 0; j < MAX_TOPK; ++j) {
+    sel_e[j] = 0;
+    sel_s[j] = 0.f;
+    if (j < a.k) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const uint64_t c = ((uint64_t)key[i] << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)(lane + 32 * i));
+        if (!((taken >> i) & 1u) && c > best) best = c;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      const int e = (int)(0xFFFFFFFFu - (uint32_t)best);
+      const int owner = e & 31, slot_i = e >> 5;
+      float se = 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (i == slot_i) se = s[i];
+      se = __shfl_sync(0xffffffffu, se, owner);
+      if (lane == owner) taken |= 1u << slot_i;
+      sel_e[j] = e;
+      sel_s[j] = se;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)best);
-    const int owner = e & 31, slot_i = e >> 5;
-    float se = 0.f;
-#pragma unroll
-    for (int i = 0; i < PER; ++i)
-      if (i == slot_i) se = s[i];
-    se = __shfl_sync(0xffffffffu, se, owner);
-    if (lane == owner) taken |= 1u << slot_i;
-    sel_e[j] = e;
-    sel_s[j] = se;
   }
-  if (lane == 0) {
-    float sum = 0.f;
-    for (int j = 0; j < a.k; ++j) sum += sel_s[j];
-    int* idx = ws_at<int>(a, a.W.idx) + (size_t)t * a.k;
-    float* w = ws_at<float>(a, a.W.w) + (size_t)t * a.k;
-    int* pos = ws_at<int>(a, a.W.pos) + (size_t)t * a.k;
-    int* counts = ws_at<int>(a, a.W.counts);
-    for (int j = 0; j < a.k; ++j) {
-      const float wj = a.renorm ? sel_s[j] / sum : sel_s[j];
-      idx[j] = sel_e[j];
-      w[j] = wj * a.routed_scale;
-      pos[j] = atomicAdd(counts + sel_e[j], 1);
-    }
+  // Lane j finishes rank j: the same sum in rank order on every lane.
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAX_TOPK; ++j)
+    if (j < a.k) sum += sel_s[j];
+  if (lane < a.k) {
+    int ej = 0;
+    float sj = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j == lane) {
+        ej = sel_e[j];
+        sj = sel_s[j];
+      }
+    const size_t p = (size_t)t * a.k + lane;
+    const float wj = a.renorm ? sj / sum : sj;
+    ws_at<int>(a, a.W.idx)[p] = ej;
+    ws_at<float>(a, a.W.w)[p] = wj * a.routed_scale;
+    ws_at<int>(a, a.W.pos)[p] = atomicAdd(ws_at<int>(a, a.W.counts) + ej, 1);
   }
 }
 
@@ -813,7 +825,7 @@ __device__ int block_exclusive_scan(int v, int* sh) {  // sh: 32 ints
 __global__ void __launch_bounds__(PLAN_THREADS) k_pf_plan(PfArgs a) {
   __shared__ int sh[32];
   __shared__ int s_rowbase[MAX_E];
-  __shared__ int s_slot_cnt[PLAN_THREADS], s_slot_row0[PLAN_THREADS];
+  __shared__ int s_slot_cnt[PLAN_THREADS], s_slot_row0[PLAN_THREADS], s_slot_tb[PLAN_THREADS];
   __shared__ int s_nslots, s_ntiles;
   int* counts = ws_at<int>(a, a.W.counts);
   const int e = threadIdx.x;
@@ -843,18 +855,30 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_pf_plan(PfArgs a) {
   if (s == PLAN_THREADS - 1) s_ntiles = tb + ntl;
   const int mgu = 2 * a.I / BM, mdn = a.H / BM;
   if (s < nslots) {
-    const int row0 = s_slot_row0[s];
-    ws_at<int>(a, a.W.slot_row0)[s] = row0;
+    s_slot_tb[s] = tb;
+    ws_at<int>(a, a.W.slot_row0)[s] = s_slot_row0[s];
     ws_at<int>(a, a.W.slot_count)[s] = cnt;
-    int4* gu = ws_at<int4>(a, a.W.gu_tiles);
-    int4* dn = ws_at<int4>(a, a.W.dn_tiles);
-    for (int q = 0; q < ntl; ++q) {
-      const int n = min(NT, cnt - q * NT);
-      for (int m = 0; m < mgu; ++m) gu[(size_t)(tb + q) * mgu + m] = make_int4(s, m, row0 + q * NT, n);
-      for (int m = 0; m < mdn; ++m) dn[(size_t)(tb + q) * mdn + m] = make_int4(s, m, row0 + q * NT, n);
-    }
   }
   __syncthreads();
+  // Tile lists, spread over the block: entry i of the token tiles x (gate/up
+  // m-tiles + down m-tiles); its slot is the last one whose first tile is <= its tile.
+  {
+    int4* gu = ws_at<int4>(a, a.W.gu_tiles);
+    int4* dn = ws_at<int4>(a, a.W.dn_tiles);
+    const int per = mgu + mdn, n_ent = s_ntiles * per;
+    for (int i = threadIdx.x; i < n_ent; i += PLAN_THREADS) {
+      const int tile = i / per, m = i % per;
+      int lo = 0, hi = nslots - 1;  // s_slot_tb is non-decreasing; the answer has ntl > 0
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_slot_tb[mid] <= tile) lo = mid; else hi = mid - 1;
+      }
+      const int q = tile - s_slot_tb[lo], row0 = s_slot_row0[lo] + q * NT;
+      const int n = min(NT, s_slot_cnt[lo] - q * NT);
+      if (m < mgu) gu[(size_t)tile * mgu + m] = make_int4(lo, m, row0, n);
+      else dn[(size_t)tile * mdn + (m - mgu)] = make_int4(lo, m - mgu, row0, n);
+    }
+  }
   if (threadIdx.x == 0) {
     int* hdr = ws_at<int>(a, 0);
     hdr[PF_NSLOTS] = nslots;
@@ -1092,11 +1116,14 @@ static flint_moe_status prefill_impl(const flint_moe_layer* layer, const uint16_
     a.rsplit *= 2;
   if (launch_gemm<ROUTER>(a, m_router, std::min(nsm, router_tiles * a.rsplit), stream) != cudaSuccess)
     return FLINT_MOE_ECUDA;
-  k_pf_topk<<<(B + 7) / 8, 256, 0, stream>>>(a);
+  if (a.E <= 256)  // experts per lane: 8 (up to 256 experts) or 16
+    k_pf_topk<8><<<(B + 7) / 8, 256, 0, stream>>>(a);
+  else
+    k_pf_topk<MAX_E / 32><<<(B + 7) / 8, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   k_pf_plan<<<1, PLAN_THREADS, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
-  k_pf_token_rows<<<B, 256, 0, stream>>>(a);
+  k_pf_token_rows<<<(B + 7) / 8, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   if (launch_gemm<GATEUP>(a, m_gateup, std::min(nsm, a.W.max_gu), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
   if (launch_gemm<DOWN>(a, m_down, std::min(nsm, a.W.max_dn), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
