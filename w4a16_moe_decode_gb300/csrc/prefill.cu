@@ -18,7 +18,10 @@
 //   k_pf_plan          slots, grouped-row bases, tile lists (one block)
 //   k_pf_token_rows    per token: its grouped-list entries, its f16 rows
 //   k_pf_gemm<GATEUP>  h = bf16(silu(G_g g) * G_u u) per (token, expert), f16 MMA
+//   k_pf_small<GATEUP> the same for slots of few rows (up to 512-token calls):
+//                      tiles of up to 16 tokens on mma.sync, dequantised in registers
 //   k_pf_gemm<DOWN>    y[t][q] = w * G_d (c_d h) per (token, expert), bf16 MMA
+//   k_pf_small<DOWN>   the same for the small tiles
 //   k_pf_combine       out = bf16(sum_q y[t][q]) in slot order
 #include <algorithm>
 #include <atomic>
@@ -35,6 +38,10 @@ namespace pf {
 constexpr int BM = 128;       // weight rows per tile (MMA M)
 constexpr int BK = 64;        // k per pipeline stage: one 128-byte swizzle row of bf16
 constexpr int NT = 128;       // tokens per tile at most (MMA N)
+constexpr int SN = 16;                 // tokens per small tile (two 8-column groups of mma.sync)
+constexpr int SMALL_MAX = 16;          // routed slots of up to this many rows take small tiles (when they fit)
+constexpr int SMALL_SHARED_MAX = 256;  // shared-expert slots (B rows) likewise
+constexpr int SMALL_B_MAX = 512;       // calls of more tokens use the tensor-core tiles only
 constexpr int NPIPE = 2;      // independent GEMM pipelines per CTA (one CTA per SM)
 constexpr int KPS = 1;        // k-blocks per operand stage
 constexpr int STAGES = 2;     // operand stages per pipeline
@@ -46,13 +53,13 @@ constexpr int B_STAGE = KPS * B_KBLK;
 constexpr int MAX_E = 512;
 
 enum Mode : int { ROUTER = 0, GATEUP = 1, DOWN = 2 };
-enum : int { PF_STATUS = HDR_STATUS, PF_NSLOTS = 2, PF_NGU = 3, PF_NDN = 4 };
+enum : int { PF_STATUS = HDR_STATUS, PF_NSLOTS = 2, PF_NGU = 3, PF_NDN = 4, PF_NGUS = 5, PF_NDNS = 6 };
 
 // Workspace: header words, then 256-byte aligned regions sized for T tokens.
 struct PfLayout {
   size_t counts, logits, idx, w, pos, slot_expert, slot_row0, slot_count, list_tok, list_q, list_w, gu_tiles,
-      dn_tiles, rowbase, kx, xn, x16, xg, h, y, total;
-  int max_slots, max_rows, max_gu, max_dn;
+      dn_tiles, gus_tiles, dns_tiles, rowbase, kx, xn, x16, xg, h, y, total;
+  int max_slots, max_rows, max_gu, max_dn, max_gus, max_dns;
 };
 
 __host__ __device__ inline PfLayout make_pf_layout(int H, int E, int k, int I, int S, int T) {
@@ -63,6 +70,10 @@ __host__ __device__ inline PfLayout make_pf_layout(int H, int E, int k, int I, i
   const int max_nt = W.max_rows / NT + W.max_slots + 1;
   W.max_gu = max_nt * (2 * I / BM);
   W.max_dn = max_nt * (H / BM);
+  // small token tiles: the shared slots' B <= SMALL_SHARED_MAX rows, the routed slots' <= SMALL_MAX rows
+  const int max_nts = S * (SMALL_SHARED_MAX / SN) + W.max_slots * (SMALL_MAX / SN);
+  W.max_gus = max_nts * (2 * I / BM);
+  W.max_dns = max_nts * (H / BM);
   size_t o = 256;
   W.counts = o;      o = ws_align(o + sizeof(int) * E);
   W.logits = o;      o = ws_align(o + sizeof(float) * (size_t)T * E);
@@ -77,6 +88,8 @@ __host__ __device__ inline PfLayout make_pf_layout(int H, int E, int k, int I, i
   W.list_w = o;      o = ws_align(o + sizeof(float) * (size_t)W.max_rows);
   W.gu_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_gu);
   W.dn_tiles = o;    o = ws_align(o + sizeof(int4) * (size_t)W.max_dn);
+  W.gus_tiles = o;   o = ws_align(o + sizeof(int4) * (size_t)W.max_gus);
+  W.dns_tiles = o;   o = ws_align(o + sizeof(int4) * (size_t)W.max_dns);
   W.rowbase = o;     o = ws_align(o + sizeof(int) * E);                // first grouped row of each routed expert
   W.kx = o;          o = ws_align(o + sizeof(int) * (size_t)T);       // per-token power-of-two prescale
   W.xn = o;          o = ws_align(o + (size_t)2 * T * H);             // RMS-normalised x (pre-norm block)
@@ -111,6 +124,11 @@ struct PfArgs {
   // written only later, by the down GEMM), and k_pf_topk adds the splits in
   // order and stores the logits.
   int rsplit;
+  // Routed slots with at most small_max grouped rows, and shared slots with at
+  // most small_shared (0: none), take small tiles of up to SN tokens, multiplied
+  // on the mma.sync path (k_pf_small); the others take the tensor-core tiles
+  // of up to NT tokens.
+  int small_max, small_shared;
 };
 
 template <typename T>
@@ -636,6 +654,165 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
   }
 }
 
+// ---------------------------------------------------------------------------
+// Small tiles: a slot with few grouped rows (a routed expert that few tokens
+// chose) gives the tensor-core tiles little to multiply per dequantised weight,
+// so its tiles of up to SN tokens go through registers instead: each of the 8
+// warps of a block takes one packed tile (16 weight rows) of the tile's m-tile,
+// streams its k-groups from global memory, dequantises each k-step into the
+// mma.sync A fragment (the layout the packed bytes are stored in) and
+// multiplies it with the tile's token rows, which the block stages in shared
+// memory (row pitch K + 8 elements, so the 8 rows an ldmatrix reads fall in
+// distinct banks; rows n..SN-1 are zero). Same epilogues, arithmetic and
+// rounding points as k_pf_gemm; only the FP32 summation order of the products
+// differs. Persistent over the small tiles blockIdx.x, + gridDim.x, ...
+// ---------------------------------------------------------------------------
+constexpr int SMALL_THREADS = 256;
+constexpr int SMALL_PF = 4;  // k-groups of packed weights loaded ahead per warp
+
+__host__ __device__ constexpr size_t small_smem_bytes(int K) { return (size_t)SN * (K * 2 + 16); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(SMALL_THREADS, 3) k_pf_small(const PfArgs a) {
+  extern __shared__ __align__(16) uint8_t srows[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+  const int K = MODE == DOWN ? a.I : a.H;
+  const int pitch = K * 2 + 16, nkg = K / 64, cpr = K / 8;
+  const int n_tiles = __ldcg(ws_at<int>(a, 0) + (MODE == GATEUP ? PF_NGUS : PF_NDNS));
+  const int4* tiles = ws_at<const int4>(a, MODE == GATEUP ? a.W.gus_tiles : a.W.dns_tiles);
+  const int64_t wtile = MODE == GATEUP ? a.L.gu_tile : a.L.dn_tile;
+  const uint32_t sbase = smem_addr(srows);
+  // ldmatrix.x4 rows of this lane: matrix lane / 8 = (token half, k half) of a k-step
+  const uint32_t bl = sbase + (uint32_t)(((lane >> 4) * 8 + (lane & 7)) * pitch + ((lane >> 3) & 1) * 16);
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int4 tv = __ldcg(tiles + tile);
+    const int slot = tv.x, mt = tv.y, row0 = tv.z, n = tv.w;
+    const int expert = __ldcg(ws_at<const int>(a, a.W.slot_expert) + slot);
+    const uint16_t* src;
+    if (MODE == GATEUP)  // a shared expert's rows are the tokens in order; the routed pairs' are grouped
+      src = slot < a.S ? ws_at<const uint16_t>(a, a.W.x16) + (size_t)(row0 - slot * a.B) * K
+                       : ws_at<const uint16_t>(a, a.W.xg) + (size_t)(row0 - a.S * a.B) * K;
+    else
+      src = ws_at<const uint16_t>(a, a.W.h) + (size_t)row0 * K;
+    __syncthreads();  // the previous tile's rows are no longer read
+    for (int i = threadIdx.x; i < SN * cpr; i += SMALL_THREADS) {
+      const int r = i / cpr, c = i % cpr;
+      cp_async16(sbase + (uint32_t)(r * pitch + c * 16), src + (size_t)(r < n ? r : 0) * K + c * 8, r < n ? 16u : 0u);
+    }
+    cp_async_commit();
+    // Packed tile (8 mt + warp) of the expert's gate/up or down matrix.
+    const uint8_t* wp = a.packed + (int64_t)expert * a.L.expert_bytes + (MODE == GATEUP ? 0 : a.L.gu_bytes) +
+                        (int64_t)(mt * 8 + warp) * wtile;
+    uint4 cw[SMALL_PF];
+    uint32_t sg[SMALL_PF], sg8[SMALL_PF];
+#pragma unroll
+    for (int j = 0; j < SMALL_PF; ++j)
+      if (j < nkg) {
+        const uint8_t* kp = wp + j * KG_NVFP4;
+        cw[j] = ldg_stream_v4(kp + lane * 16);
+        sg[j] = ldg_stream_u32(kp + KG_CODE_BYTES + g * 4);
+        sg8[j] = ldg_stream_u32(kp + KG_CODE_BYTES + (g + 8) * 4);
+      }
+    cp_async_wait<0>();
+    __syncthreads();
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // k-group kg0 + j sits in register set j; once multiplied, the set takes
+    // k-group kg0 + j + SMALL_PF, so SMALL_PF k-groups stay in flight.
+    for (int kg0 = 0; kg0 < nkg; kg0 += SMALL_PF) {
+#pragma unroll
+      for (int j = 0; j < SMALL_PF; ++j) {
+        if (kg0 + j < nkg) {
+          const uint32_t w4[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            uint32_t af[4];
+            nvfp4_afrag(w4[ks], sg[j], sg8[j], ks, af);
+            uint32_t b[4];
+            ldsm_x4(bl + (uint32_t)(((kg0 + j) * 64 + ks * 16) * 2), b);
+            if (MODE == GATEUP) {
+              mma_f16(acc[0], af, b[0], b[1]);
+              mma_f16(acc[1], af, b[2], b[3]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) af[q] = f16x2_to_bf16x2(af[q]);
+              mma_bf16(acc[0], af, b[0], b[1]);
+              mma_bf16(acc[1], af, b[2], b[3]);
+            }
+          }
+        }
+        if (kg0 + SMALL_PF + j < nkg) {
+          const uint8_t* kp = wp + (kg0 + SMALL_PF + j) * KG_NVFP4;
+          cw[j] = ldg_stream_v4(kp + lane * 16);
+          sg[j] = ldg_stream_u32(kp + KG_CODE_BYTES + g * 4);
+          sg8[j] = ldg_stream_u32(kp + KG_CODE_BYTES + (g + 8) * 4);
+        }
+      }
+    }
+    // Epilogue: lane (g, tq) holds rows g, g + 8 of the packed tile for token
+    // columns 8 jn + 2 tq + {0, 1}.
+    if (MODE == GATEUP) {
+      // rows g and g + 8 are the gate and up rows of intermediate index 8 (8 mt + warp) + g
+      const float Gg = a.globals[expert * 4 + 0], Gu = a.globals[expert * 4 + 1];
+      const int ii = (mt * 8 + warp) * 8 + g;
+      uint16_t* hbuf = ws_at<uint16_t>(a, a.W.h);
+#pragma unroll
+      for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = jn * 8 + tq * 2 + e;
+          if (c < n) {
+            const int tok = slot < a.S ? row0 - slot * a.B + c : __ldcg(ws_at<const int>(a, a.W.list_tok) + row0 + c);
+            const float inv = exp2i(-__ldcg(ws_at<const int>(a, a.W.kx) + tok));
+            const float gv = acc[jn][e] * inv * Gg;
+            const float uv = acc[jn][2 + e] * inv * Gu;
+            const float sv = __fdividef(gv, 1.0f + __expf(-gv));
+            const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
+            hbuf[(size_t)(row0 + c) * a.I + ii] = *reinterpret_cast<const uint16_t*>(&hb);
+          }
+        }
+    } else {
+      const float Gd = a.globals[expert * 4 + 2];
+      float* y = ws_at<float>(a, a.W.y);
+      const int jrow = mt * BM + warp * 16 + g;
+      const int q_per_tok = a.S + a.k;
+#pragma unroll
+      for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = jn * 8 + tq * 2 + e;
+          if (c < n) {
+            const int row = row0 + c;
+            const int tok = __ldcg(ws_at<const int>(a, a.W.list_tok) + row);
+            const int qq = __ldcg(ws_at<const int>(a, a.W.list_q) + row);
+            const float wv = __ldcg(ws_at<const float>(a, a.W.list_w) + row);
+            float* yr = y + ((size_t)tok * q_per_tok + qq) * a.H + jrow;
+            yr[0] = wv * (acc[jn][e] * Gd);
+            yr[8] = wv * (acc[jn][2 + e] * Gd);
+          }
+        }
+    }
+  }
+}
+
 // One warp per token, after the plan: the token's entries of the grouped row
 // lists (token, slot rank, routing weight), and its gate/up activations in
 // f16 for the tensor cores: a power of two 2^kx maps the row's largest |x|
@@ -825,8 +1002,9 @@ __device__ int block_exclusive_scan(int v, int* sh) {  // sh: 32 ints
 __global__ void __launch_bounds__(PLAN_THREADS) k_pf_plan(PfArgs a) {
   __shared__ int sh[32];
   __shared__ int s_rowbase[MAX_E];
-  __shared__ int s_slot_cnt[PLAN_THREADS], s_slot_row0[PLAN_THREADS], s_slot_tb[PLAN_THREADS];
-  __shared__ int s_nslots, s_ntiles;
+  __shared__ int s_slot_cnt[PLAN_THREADS], s_slot_row0[PLAN_THREADS], s_slot_tb[PLAN_THREADS],
+      s_slot_tbs[PLAN_THREADS];
+  __shared__ int s_nslots, s_ntiles, s_nstiles;
   int* counts = ws_at<int>(a, a.W.counts);
   const int e = threadIdx.x;
   const int c = e < a.E ? __ldcg(counts + e) : 0;
@@ -847,36 +1025,53 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_pf_plan(PfArgs a) {
   if (e == PLAN_THREADS - 1) s_nslots = a.S + sl + (c > 0 ? 1 : 0);
   __syncthreads();
   const int nslots = s_nslots;
-  // Token tiles per slot (one slot per thread: S + E <= PLAN_THREADS).
+  // Token tiles per slot (one slot per thread: S + E <= PLAN_THREADS): NT-token
+  // tiles for the tensor cores, or SN-token tiles for slots of few rows.
   const int s = threadIdx.x;
   const int cnt = s < nslots ? s_slot_cnt[s] : 0;
-  const int ntl = (cnt + NT - 1) / NT;
+  const bool small = cnt <= (s < a.S ? a.small_shared : a.small_max);
+  const int ntl = small ? 0 : (cnt + NT - 1) / NT;
+  const int nts = small ? (cnt + SN - 1) / SN : 0;
   const int tb = block_exclusive_scan(ntl, sh);
-  if (s == PLAN_THREADS - 1) s_ntiles = tb + ntl;
+  const int tbs = block_exclusive_scan(nts, sh);
+  if (s == PLAN_THREADS - 1) {
+    s_ntiles = tb + ntl;
+    s_nstiles = tbs + nts;
+  }
   const int mgu = 2 * a.I / BM, mdn = a.H / BM;
   if (s < nslots) {
     s_slot_tb[s] = tb;
+    s_slot_tbs[s] = tbs;
     ws_at<int>(a, a.W.slot_row0)[s] = s_slot_row0[s];
     ws_at<int>(a, a.W.slot_count)[s] = cnt;
   }
   __syncthreads();
   // Tile lists, spread over the block: entry i of the token tiles x (gate/up
-  // m-tiles + down m-tiles); its slot is the last one whose first tile is <= its tile.
-  {
-    int4* gu = ws_at<int4>(a, a.W.gu_tiles);
-    int4* dn = ws_at<int4>(a, a.W.dn_tiles);
-    const int per = mgu + mdn, n_ent = s_ntiles * per;
+  // m-tiles + down m-tiles). A token tile's slot is the last one whose first
+  // tile is <= it: the first tiles are non-decreasing in slot order, and a slot
+  // without tiles of the kind shares its first tile with the next slot that has some.
+  auto slot_of = [&](const int* first, int tile) {
+    int lo = 0, hi = nslots - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (first[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+  const int per = mgu + mdn;
+  for (int kind = 0; kind < 2; ++kind) {
+    const int* first = kind ? s_slot_tbs : s_slot_tb;
+    const int tsz = kind ? SN : NT;
+    int4* gu = ws_at<int4>(a, kind ? a.W.gus_tiles : a.W.gu_tiles);
+    int4* dn = ws_at<int4>(a, kind ? a.W.dns_tiles : a.W.dn_tiles);
+    const int n_ent = (kind ? s_nstiles : s_ntiles) * per;
     for (int i = threadIdx.x; i < n_ent; i += PLAN_THREADS) {
       const int tile = i / per, m = i % per;
-      int lo = 0, hi = nslots - 1;  // s_slot_tb is non-decreasing; the answer has ntl > 0
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_slot_tb[mid] <= tile) lo = mid; else hi = mid - 1;
-      }
-      const int q = tile - s_slot_tb[lo], row0 = s_slot_row0[lo] + q * NT;
-      const int n = min(NT, s_slot_cnt[lo] - q * NT);
-      if (m < mgu) gu[(size_t)tile * mgu + m] = make_int4(lo, m, row0, n);
-      else dn[(size_t)tile * mdn + (m - mgu)] = make_int4(lo, m - mgu, row0, n);
+      const int sl = slot_of(first, tile);
+      const int q = tile - first[sl], row0 = s_slot_row0[sl] + q * tsz;
+      const int n = min(tsz, s_slot_cnt[sl] - q * tsz);
+      if (m < mgu) gu[(size_t)tile * mgu + m] = make_int4(sl, m, row0, n);
+      else dn[(size_t)tile * mdn + (m - mgu)] = make_int4(sl, m - mgu, row0, n);
     }
   }
   if (threadIdx.x == 0) {
@@ -884,6 +1079,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) k_pf_plan(PfArgs a) {
     hdr[PF_NSLOTS] = nslots;
     hdr[PF_NGU] = s_ntiles * mgu;
     hdr[PF_NDN] = s_ntiles * mdn;
+    hdr[PF_NGUS] = s_nstiles * mgu;
+    hdr[PF_NDNS] = s_nstiles * mdn;
   }
   if (e < a.E) ws_at<int>(a, a.W.rowbase)[e] = s_rowbase[e];
   if (e < a.E) counts[e] = 0;  // ready for the next call (every read of counts is above)
@@ -955,6 +1152,19 @@ __global__ void k_pf_debug_routing(const int* idx, const float* w, const float* 
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
+template <int MODE>
+static cudaError_t launch_small(const PfArgs& a, int grid, cudaStream_t stream) {
+  static std::atomic<int> attr_set{0};
+  const size_t smem = small_smem_bytes(MODE == DOWN ? a.I : a.H);
+  if (smem > 48 * 1024 && !attr_set.load()) {
+    cudaError_t e = cudaFuncSetAttribute(k_pf_small<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set.store(1);
+  }
+  k_pf_small<MODE><<<grid, SMALL_THREADS, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
 static flint_moe_status cfg_supported(const flint_moe_config* c) {
   const flint_moe_status st = flint_moe_check_config(c);
   if (st != FLINT_MOE_OK) return st;
@@ -1086,6 +1296,13 @@ static flint_moe_status prefill_impl(const flint_moe_layer* layer, const uint16_
   a.res = x;
   a.gamma = layer->norm_weight;
   a.eps = layer->norm_eps;
+  // Small tiles while three blocks' token rows fit one SM's shared memory, for
+  // calls of up to SMALL_B_MAX tokens: beyond, most routed experts have more
+  // than SMALL_MAX tokens, and the few small tiles would only add a launch
+  // after the tensor-core tiles.
+  const bool small_fits = 3 * small_smem_bytes(a.H) <= (size_t)227 * 1024 && B <= SMALL_B_MAX;
+  a.small_max = small_fits ? SMALL_MAX : 0;
+  a.small_shared = small_fits ? SMALL_SHARED_MAX : 0;
   if (ws_bytes < a.W.total) return FLINT_MOE_EINVAL;
   if (prenorm) {  // the layer runs on the normalised rows
     k_pf_norm<<<(B + 7) / 8, 256, 0, stream>>>(a);
@@ -1126,7 +1343,11 @@ static flint_moe_status prefill_impl(const flint_moe_layer* layer, const uint16_
   k_pf_token_rows<<<(B + 7) / 8, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
   if (launch_gemm<GATEUP>(a, m_gateup, std::min(nsm, a.W.max_gu), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
+  if (small_fits && launch_small<GATEUP>(a, std::min(3 * nsm, a.W.max_gus), stream) != cudaSuccess)
+    return FLINT_MOE_ECUDA;
   if (launch_gemm<DOWN>(a, m_down, std::min(nsm, a.W.max_dn), stream) != cudaSuccess) return FLINT_MOE_ECUDA;
+  if (small_fits && launch_small<DOWN>(a, std::min(3 * nsm, a.W.max_dns), stream) != cudaSuccess)
+    return FLINT_MOE_ECUDA;
   const int cgrid = (int)std::min<size_t>((size_t)nsm * 8, ((size_t)B * a.H / 4 + 255) / 256);
   k_pf_combine<<<cgrid, 256, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FLINT_MOE_ECUDA;
