@@ -691,11 +691,13 @@ __device__ __forceinline__ uint32_t ldg_stream_u32(const void* p) {
   return v;
 }
 
-template <int MODE>
+// NKG > 0: the k-groups per packed tile (K / 64) fixed at compile time (the
+// Flint shape: 32 for gate/up, 8 for down); 0: read from the arguments.
+template <int MODE, int NKG>
 __global__ void __launch_bounds__(SMALL_THREADS, 3) k_pf_small(const PfArgs a) {
   extern __shared__ __align__(16) uint8_t srows[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
-  const int K = MODE == DOWN ? a.I : a.H;
+  const int K = NKG ? NKG * 64 : (MODE == DOWN ? a.I : a.H);
   const int pitch = K * 2 + 16, nkg = K / 64, cpr = K / 8;
   const int n_tiles = __ldcg(ws_at<int>(a, 0) + (MODE == GATEUP ? PF_NGUS : PF_NDNS));
   const int4* tiles = ws_at<const int4>(a, MODE == GATEUP ? a.W.gus_tiles : a.W.dns_tiles);
@@ -714,10 +716,10 @@ __global__ void __launch_bounds__(SMALL_THREADS, 3) k_pf_small(const PfArgs a) {
     else
       src = ws_at<const uint16_t>(a, a.W.h) + (size_t)row0 * K;
     __syncthreads();  // the previous tile's rows are no longer read
-    for (int i = threadIdx.x; i < SN * cpr; i += SMALL_THREADS) {
-      const int r = i / cpr, c = i % cpr;
-      cp_async16(sbase + (uint32_t)(r * pitch + c * 16), src + (size_t)(r < n ? r : 0) * K + c * 8, r < n ? 16u : 0u);
-    }
+#pragma unroll 4
+    for (int r = 0; r < SN; ++r)
+      for (int c = threadIdx.x; c < cpr; c += SMALL_THREADS)
+        cp_async16(sbase + (uint32_t)(r * pitch + c * 16), src + (size_t)(r < n ? r : 0) * K + c * 8, r < n ? 16u : 0u);
     cp_async_commit();
     // Packed tile (8 mt + warp) of the expert's gate/up or down matrix.
     const uint8_t* wp = a.packed + (int64_t)expert * a.L.expert_bytes + (MODE == GATEUP ? 0 : a.L.gu_bytes) +
@@ -1152,17 +1154,24 @@ __global__ void k_pf_debug_routing(const int* idx, const float* w, const float* 
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-template <int MODE>
-static cudaError_t launch_small(const PfArgs& a, int grid, cudaStream_t stream) {
+template <int MODE, int NKG>
+static cudaError_t launch_small_k(const PfArgs& a, int grid, cudaStream_t stream) {
   static std::atomic<int> attr_set{0};
   const size_t smem = small_smem_bytes(MODE == DOWN ? a.I : a.H);
   if (smem > 48 * 1024 && !attr_set.load()) {
-    cudaError_t e = cudaFuncSetAttribute(k_pf_small<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_pf_small<MODE, NKG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set.store(1);
   }
-  k_pf_small<MODE><<<grid, SMALL_THREADS, smem, stream>>>(a);
+  k_pf_small<MODE, NKG><<<grid, SMALL_THREADS, smem, stream>>>(a);
   return cudaGetLastError();
+}
+
+template <int MODE>
+static cudaError_t launch_small(const PfArgs& a, int grid, cudaStream_t stream) {
+  const int K = MODE == DOWN ? a.I : a.H;
+  constexpr int FLINT_K = MODE == DOWN ? 512 : 2048;  // the Flint shape's I and H
+  return K == FLINT_K ? launch_small_k<MODE, FLINT_K / 64>(a, grid, stream) : launch_small_k<MODE, 0>(a, grid, stream);
 }
 
 static flint_moe_status cfg_supported(const flint_moe_config* c) {
