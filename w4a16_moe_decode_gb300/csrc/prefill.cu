@@ -520,6 +520,88 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
     const uint32_t tile_off = (uint32_t)(dq_p * RAW_KB * KG_NVFP4);
     int ctok[2] = {0, 0}, cq[2] = {0, 0};  // this lane's two epilogue columns: 64 cg + lane, + 32
     float cw[2] = {0.f, 0.f}, cinv[2] = {1.f, 1.f};
+    // Deferred epilogue: once all k-blocks of a tile are dequantised, its
+    // accumulator is read out one 16-column chunk after each k-block of the
+    // next tile (in time this warp would otherwise spend waiting for a free
+    // stage), and the rest after the last tile. The MMAs of the tile after
+    // next wait for this buffer, so a tile's epilogue always ends before the
+    // dequantisation of the following tile does.
+    bool pend = false;
+    TileInfo pt{};
+    int pi = 0, pc = 0;  // the pending tile's index and next chunk column
+    int pctok[2] = {0, 0}, pcq[2] = {0, 0};
+    float pcw[2] = {0.f, 0.f}, pcinv[2] = {1.f, 1.f};
+    auto epi_chunk = [&]() -> bool {  // false: a wait gave up
+      const int ab = pi & 1;
+      if (pc == cg * 64) {  // before the first chunk: the tile's MMAs are complete
+        const bool ok = wait_ab(&G.acc_full[p][ab], (pi / 2) & 1, abort, status);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        tc_fence_after();
+      }
+      const int r = q4 * 32 + lane;  // weight row within the m-tile
+      const uint32_t tacc = tmem + (uint32_t)(ab * NT) + ((uint32_t)(q4 * 32) << 16);
+      const int c0 = pc;
+      if (c0 < cg * 64 + 64 && c0 < pt.n) {
+        const int hcol = (c0 - cg * 64) >> 5;  // which of the lane's two column registers
+        uint32_t v[16];
+        tc_ld16(tacc + (uint32_t)c0, v);
+        if (MODE == ROUTER) {
+          const int e = pt.mt * BM + r;
+          float* logits = a.rsplit > 1 ? ws_at<float>(a, a.W.y) + (size_t)pt.slot * a.B * a.E : ws_at<float>(a, a.W.logits);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (e < a.E && c0 + j < pt.n) logits[(size_t)(pt.row0 + c0 + j) * a.E + e] = __uint_as_float(v[j]);
+        } else if (MODE == GATEUP) {
+          // Rows 16 u .. 16 u + 7 of packed tile u are gate rows, the next 8 the
+          // up rows of the same intermediate indices 8 (8 mt + u) + r % 8: lane
+          // L and lane L ^ 8 hold (gate, up) of one index. The gate lane
+          // finishes the even columns, the up lane the odd ones.
+          const float Gg = a.globals[pt.expert * 4 + 0], Gu = a.globals[pt.expert * 4 + 1];
+          const bool gate = (lane & 8) == 0;
+          const int ii = (pt.mt * 8 + q4 * 2 + (lane >> 4)) * 8 + (lane & 7);
+          uint16_t* hbuf = ws_at<uint16_t>(a, a.W.h);
+          const float cinv_h = hcol ? pcinv[1] : pcinv[0];
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            const float v0 = __uint_as_float(v[j]), v1 = __uint_as_float(v[j + 1]);
+            const float mine = gate ? v0 : v1;
+            const float other = __shfl_xor_sync(0xffffffffu, gate ? v1 : v0, 8);
+            const int c = c0 + j + (gate ? 0 : 1);
+            const float inv = __shfl_sync(0xffffffffu, cinv_h, c & 31);
+            const float gv = (gate ? mine : other) * inv * Gg;
+            const float uv = (gate ? other : mine) * inv * Gu;
+            const float sv = __fdividef(gv, 1.0f + __expf(-gv));
+            if (c < pt.n) {
+              const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
+              hbuf[(size_t)(pt.row0 + c) * a.I + ii] = *reinterpret_cast<const uint16_t*>(&hb);
+            }
+          }
+        } else {
+          const float Gd = a.globals[pt.expert * 4 + 2];
+          float* y = ws_at<float>(a, a.W.y);
+          const int jrow = pt.mt * BM + r;
+          const int q_per_tok = a.S + a.k;
+          const int ctok_h = hcol ? pctok[1] : pctok[0], cq_h = hcol ? pcq[1] : pcq[0];
+          const float cw_h = hcol ? pcw[1] : pcw[0];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = c0 + j, src = c & 31;
+            const int tok = __shfl_sync(0xffffffffu, ctok_h, src);
+            const int qq = __shfl_sync(0xffffffffu, cq_h, src);
+            const float wv = __shfl_sync(0xffffffffu, cw_h, src);
+            if (c < pt.n) y[((size_t)tok * q_per_tok + qq) * a.H + jrow] = wv * (__uint_as_float(v[j]) * Gd);
+          }
+        }
+        pc = c0 + 16;
+      }
+      if (!(pc < cg * 64 + 64 && pc < pt.n)) {  // the warp's columns are done: the buffer is free for it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&G.acc_empty[p][ab]);
+        pend = false;
+      }
+      return true;
+    };
     bool failed = false;
     for (int u = 0; u < n_slots && !failed; ++u) {
       const int i = u / SPT, kb0 = (u % SPT) * RAW_KB, nk = min(RAW_KB, KB - kb0);
@@ -572,6 +654,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
           fence_proxy_async();  // these st.shared -> visible to the tensor core
           __syncwarp();
           if (lane == 0) mbar_arrive(&G.full[p][s]);
+          if (pend && !epi_chunk()) {
+            failed = true;
+            break;
+          }
         }
         if (failed || !__all_sync(0xffffffffu, ok)) {
           failed = true;
@@ -580,70 +666,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_pf_gemm(const PfArgs a, con
         __syncwarp();
         if (lane == 0) mbar_arrive(&G.raw_empty[p][u % RAW_SL]);  // this warp is done with the slot
       }
-      if (kb0 + nk == KB) {  // the tile's epilogue
-        const int ab = i & 1;
-        const bool ok = wait_ab(&G.acc_full[p][ab], (i / 2) & 1, abort, status);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        tc_fence_after();
-        const int r = q4 * 32 + lane;  // weight row within the m-tile
-        const uint32_t tacc = tmem + (uint32_t)(ab * NT) + ((uint32_t)(q4 * 32) << 16);
-        for (int c0 = cg * 64; c0 < cg * 64 + 64 && c0 < t.n; c0 += 16) {
-          const int hcol = (c0 - cg * 64) >> 5;  // which of the lane's two column registers
-          uint32_t v[16];
-          tc_ld16(tacc + (uint32_t)c0, v);
-          if (MODE == ROUTER) {
-            const int e = t.mt * BM + r;
-            float* logits = a.rsplit > 1 ? ws_at<float>(a, a.W.y) + (size_t)t.slot * a.B * a.E : ws_at<float>(a, a.W.logits);
+      if (kb0 + nk == KB) {  // all k-blocks of the tile are dequantised: its epilogue is next
+        while (pend && !failed) failed = !epi_chunk();
+        if (failed) break;
+        pend = true;
+        pt = t;
+        pi = i;
+        pc = cg * 64;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (e < a.E && c0 + j < t.n) logits[(size_t)(t.row0 + c0 + j) * a.E + e] = __uint_as_float(v[j]);
-          } else if (MODE == GATEUP) {
-            // Rows 16 u .. 16 u + 7 of packed tile u are gate rows, the next 8 the
-            // up rows of the same intermediate indices 8 (8 mt + u) + r % 8: lane
-            // L and lane L ^ 8 hold (gate, up) of one index. The gate lane
-            // finishes the even columns, the up lane the odd ones.
-            const float Gg = a.globals[t.expert * 4 + 0], Gu = a.globals[t.expert * 4 + 1];
-            const bool gate = (lane & 8) == 0;
-            const int ii = (t.mt * 8 + q4 * 2 + (lane >> 4)) * 8 + (lane & 7);
-            uint16_t* hbuf = ws_at<uint16_t>(a, a.W.h);
-            const float cinv_h = hcol ? cinv[1] : cinv[0];
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              const float v0 = __uint_as_float(v[j]), v1 = __uint_as_float(v[j + 1]);
-              const float mine = gate ? v0 : v1;
-              const float other = __shfl_xor_sync(0xffffffffu, gate ? v1 : v0, 8);
-              const int c = c0 + j + (gate ? 0 : 1);
-              const float inv = __shfl_sync(0xffffffffu, cinv_h, c & 31);
-              const float gv = (gate ? mine : other) * inv * Gg;
-              const float uv = (gate ? other : mine) * inv * Gu;
-              const float sv = __fdividef(gv, 1.0f + __expf(-gv));
-              if (c < t.n) {
-                const __nv_bfloat16 hb = __float2bfloat16_rn(sv * uv);
-                hbuf[(size_t)(t.row0 + c) * a.I + ii] = *reinterpret_cast<const uint16_t*>(&hb);
-              }
-            }
-          } else {
-            const float Gd = a.globals[t.expert * 4 + 2];
-            float* y = ws_at<float>(a, a.W.y);
-            const int jrow = t.mt * BM + r;
-            const int q_per_tok = a.S + a.k;
-            const int ctok_h = hcol ? ctok[1] : ctok[0], cq_h = hcol ? cq[1] : cq[0];
-            const float cw_h = hcol ? cw[1] : cw[0];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int c = c0 + j, src = c & 31;
-              const int tok = __shfl_sync(0xffffffffu, ctok_h, src);
-              const int qq = __shfl_sync(0xffffffffu, cq_h, src);
-              const float wv = __shfl_sync(0xffffffffu, cw_h, src);
-              if (c < t.n) y[((size_t)tok * q_per_tok + qq) * a.H + jrow] = wv * (__uint_as_float(v[j]) * Gd);
-            }
-          }
+        for (int h = 0; h < 2; ++h) {
+          pctok[h] = ctok[h];
+          pcq[h] = cq[h];
+          pcw[h] = cw[h];
+          pcinv[h] = cinv[h];
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&G.acc_empty[p][ab]);
+        if (MODE == ROUTER)  // no dequantisation to interleave with: now
+          while (pend && !failed) failed = !epi_chunk();
       }
     }
+    while (pend && !failed) failed = !epi_chunk();
   }
 
   tc_fence_before();
