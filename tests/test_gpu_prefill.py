@@ -86,7 +86,13 @@ def test_prefill_parity_tiny_all_tokens(B):
     assert len(excluded) <= max(1, B // 20)
 
 
-@pytest.mark.parametrize("B,tokens", [(1, [0]), (16, [0, 7, 15]), (64, [0, 1, 33, 63]), (300, [0, 128, 299])])
+# The batch sizes straddle the path's tile choices: up to 256 tokens the shared
+# expert takes 16-token mma.sync tiles, beyond it tensor-core tiles; up to 512
+# tokens routed experts with at most 16 tokens take small tiles, from 513 on
+# every slot takes tensor-core tiles.
+@pytest.mark.parametrize("B,tokens", [(1, [0]), (16, [0, 7, 15]), (64, [0, 1, 33, 63]), (256, [0, 100, 255]),
+                                      (257, [0, 128, 256]), (300, [0, 128, 299]), (512, [0, 255, 511]),
+                                      (513, [0, 256, 512])])
 def test_prefill_parity_flint_sampled(B, tokens):
     worst, excluded, routing = run_parity(FLINT, B, seed=11, tokens=tokens)
     assert not set(excluded) & set(tokens) and len(excluded) <= max(1, B // 50)
