@@ -132,6 +132,65 @@ def check_routing(routing, idx_gpu, w_gpu, tokens=None):
     return excluded
 
 
+# The GPU computes the pre-norm RMSNorm r * w / sqrt(mean(r^2) + eps) in FP32
+# before rounding it to bf16: each lane sums the squares of 64 of a 2048-wide
+# row's elements, a 5-level butterfly adds the lanes, then a division, a square
+# root, a reciprocal and two products. All terms positive, that is at most
+# (64 + 5) rounding errors of 2^-24 relative in the sum, half of it after the
+# root, a few more after: below 2^-18 relative. Where the float64 value lies
+# within that of a bf16 rounding boundary, the GPU may round it to the other
+# neighbour.
+NORM_REL = 2.0 ** -18
+NORM_MAX_UNDECIDED = 12  # at most 2^12 rounding combinations tried per token
+
+
+def prenorm_undecided(r, gamma, eps):
+    """The oracle's normalised rows xn (bf16 values) and, per element, the other
+    bf16 value the GPU's FP32 normalisation may round to (equal to xn where
+    the rounding is decided)."""
+    x = np.asarray(r, np.float64)
+    g = np.asarray(gamma, np.float64)
+    v = x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + np.float64(eps)) * g[None, :]
+    xn = moe.bf16_round(v)
+    lo, hi = moe.bf16_round(v * (1 - NORM_REL)), moe.bf16_round(v * (1 + NORM_REL))
+    alt = np.where(lo != xn, lo, hi)
+    return xn, alt
+
+
+def check_routing_prenorm(r, gamma, eps, router, cfg, bias, idx_gpu, w_gpu, tokens=None):
+    """check_routing for the pre-norm block. The oracle's routing of the
+    normalised rows must match, or, for a token whose normalisation has
+    elements within NORM_REL of a bf16 rounding boundary, the routing of one
+    of the rows those elements' two roundings give (the rounding is the one
+    step where FP32 and float64 may decide differently). Returns (excluded
+    tokens, tokens matched through another rounding)."""
+    xn, alt = prenorm_undecided(r, gamma, eps)
+    routing = moe.route(xn, router, cfg, bias)
+    B = routing.idx.shape[0]
+    tokens = range(B) if tokens is None else tokens
+    excluded, rerounded = [], []
+    for t in tokens:
+        if routing.gap[t] < GAP_MIN:
+            excluded.append(t)
+            continue
+        def same(rt, row=0):
+            return (idx_gpu[t].tolist() == rt.idx[row].tolist() and
+                    np.all(np.abs(w_gpu[t].astype(np.float64) - rt.w[row].astype(np.float64)) <= W_TOL))
+        if same(routing, t):
+            continue
+        und = np.nonzero(alt[t] != xn[t])[0]
+        assert 0 < len(und) <= NORM_MAX_UNDECIDED, (t, len(und), idx_gpu[t], routing.idx[t], w_gpu[t], routing.w[t])
+        rows = np.repeat(xn[t][None, :], 2 ** len(und), axis=0)
+        for m in range(1, 2 ** len(und)):
+            flip = [und[j] for j in range(len(und)) if (m >> j) & 1]
+            rows[m, flip] = alt[t, flip]
+        rt = moe.route(rows, router, cfg, bias)
+        assert any(same(rt, m) for m in range(1, rows.shape[0])), (t, idx_gpu[t], routing.idx[t], w_gpu[t],
+                                                                  routing.w[t])
+        rerounded.append(t)
+    return excluded, rerounded
+
+
 def bf16_ulp(ref):
     """Spacing of bf16 numbers at |ref| (8 significant bits; the subnormal
     spacing 2^-133 below 2^-126)."""

@@ -32,7 +32,8 @@ from w4a16_moe_decode_gb300 import binding as fb
 from w4a16_moe_decode_gb300 import layers
 from w4a16_moe_decode_gb300.build import build
 
-from _common import FLINT, TINY, bits_to_f64, check_out, check_routing, oracle_config, oracle_experts, oracle_inputs
+from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, check_routing_prenorm, oracle_config,
+                     oracle_experts, oracle_inputs)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -276,6 +277,6 @@ def test_prenorm_rows_near_the_ends_of_bf16(prefill, B):
     _, router = oracle_inputs(d, seed, 0, 1)
     gamma = moe.bf16_bits_to_f64(synth.norm_bf16(seed, 0, d["hidden"]))
     ref, routing = moe.moe_block(ro, router, oracle_experts(d, seed, 0), oracle_config(d), gamma, 1e-6)
-    excluded = check_routing(routing, idx, w)
+    excluded, _ = check_routing_prenorm(ro, gamma, 1e-6, router, oracle_config(d), None, idx, w)
     assert not ({0, 1, 3} & set(t for t in excluded))
     check_out(ref, bits_to_f64(out), f"prenorm near the ends of bf16, B={B}, {'prefill' if prefill else 'decode'}")

@@ -15,8 +15,8 @@ from w4a16_moe_decode_gb300 import binding as fb
 from w4a16_moe_decode_gb300 import layers
 from w4a16_moe_decode_gb300.build import build
 
-from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, needed_experts, oracle_config,
-                     oracle_experts, oracle_inputs)
+from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, check_routing_prenorm, needed_experts,
+                     oracle_config, oracle_experts, oracle_inputs)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -316,7 +316,7 @@ def run_parity_prenorm(d, B, seed=0, layer=0, tokens=None, bias=None, inplace=Fa
     tokens = list(range(B)) if tokens is None else tokens
     oc = oracle_config(d)
     routing = moe.route(moe.rmsnorm(ro, gamma, 1e-6), router, oc, bias)
-    excluded = check_routing(routing, idx.cpu().numpy(), w.cpu().numpy())  # every token
+    excluded, _ = check_routing_prenorm(ro, gamma, 1e-6, router, oc, bias, idx.cpu().numpy(), w.cpu().numpy())
     get = oracle_experts(d, seed, layer, prefetch=needed_experts(d, routing, tokens))
     ref, routing2 = moe.moe_block(ro, router, get, oc, gamma, 1e-6, bias, tokens)
     assert np.array_equal(routing2.idx, routing.idx)
@@ -426,3 +426,41 @@ def test_decode_with_x_and_out_in_pinned_host_memory(d, B, prenorm):
     unpinned = torch.zeros(B, cfg.hidden, dtype=torch.int16)  # ordinary host memory: refused before any launch
     with pytest.raises(fb.FlintMoeError):
         call(dl.handle, unpinned, B, ref, ws)
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+def test_prenorm_rounding_decision_at_32_tokens(prefill):
+    """Seed 61, 32 tokens: the FP32 normalisation of token 31 rounds an element
+    to the other bf16 neighbour than the float64 oracle does (it lies within
+    FP32 error of the rounding boundary), which moves that token's routing
+    weights by about 4e-6 with the same experts. The pre-norm check accepts it
+    through that rounding, on the small-batch kernels and on the
+    expert-grouped path alike."""
+    d, seed, B = FLINT, 61, 32
+    cfg = cfg_of(d)
+    dl = layers.synth_layer(cfg, seed, 0, DEV, norm_eps=1e-6)
+    r = layers.synth_x(B, cfg.hidden, seed, 0, DEV)
+    out = torch.full_like(r, 0x7FC0)
+    idx = torch.empty(B, cfg.top_k, dtype=torch.int32, device=DEV)
+    w = torch.empty(B, cfg.top_k, dtype=torch.float32, device=DEV)
+    if prefill:
+        ws = layers.prefill_workspace(cfg, B, DEV)
+        fb.flint_moe_prefill_prenorm(dl.handle, r, B, out, ws)
+        fb.flint_moe_prefill_debug_routing(cfg, ws, B, idx, w)
+    else:
+        ws = layers.workspace(cfg, B, DEV)
+        fb.flint_moe_decode_prenorm(dl.handle, r, B, out, ws)
+        fb.flint_moe_debug_routing(cfg, ws, B, idx, w)
+    st, bits = fb.flint_moe_read_status(ws)
+    assert st == fb.OK and bits == 0
+    ro, router = oracle_inputs(d, seed, 0, B)
+    gamma = moe.bf16_bits_to_f64(synth.norm_bf16(seed, 0, d["hidden"]))
+    oc = oracle_config(d)
+    excluded, rerounded = check_routing_prenorm(ro, gamma, 1e-6, router, oc, None, idx.cpu().numpy(),
+                                                w.cpu().numpy())
+    assert excluded == [] and rerounded == [31]
+    tokens = [0, 16, 31]
+    routing = moe.route(moe.rmsnorm(ro, gamma, 1e-6), router, oc)
+    get = oracle_experts(d, seed, 0, prefetch=needed_experts(d, routing, tokens))
+    ref, _ = moe.moe_block(ro, router, get, oc, gamma, 1e-6, None, tokens)
+    check_out(ref, bits_to_f64(out)[tokens], f"prenorm B=32 seed=61, {'prefill' if prefill else 'decode'}")

@@ -19,8 +19,8 @@ from w4a16_moe_decode_gb300 import binding as fb
 from w4a16_moe_decode_gb300 import layers
 from w4a16_moe_decode_gb300.build import build
 
-from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, needed_experts, oracle_config,
-                     oracle_experts, oracle_inputs)
+from _common import (FLINT, TINY, bits_to_f64, check_out, check_routing, check_routing_prenorm, needed_experts,
+                     oracle_config, oracle_experts, oracle_inputs)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -199,7 +199,8 @@ def run_prefill_prenorm(d, B, seed, tokens=None, bias=None, inplace=False, scale
     gamma = moe.bf16_bits_to_f64(synth.norm_bf16(seed, layer, d["hidden"]))
     tokens = list(range(B)) if tokens is None else tokens
     routing = moe.route(moe.rmsnorm(ro, gamma, 1e-6), router, oracle_config(d), bias)
-    excluded = check_routing(routing, idx.cpu().numpy(), w.cpu().numpy())  # every token
+    excluded, _ = check_routing_prenorm(ro, gamma, 1e-6, router, oracle_config(d), bias, idx.cpu().numpy(),
+                                        w.cpu().numpy())  # every token
     get = oracle_experts(d, seed, layer, prefetch=needed_experts(d, routing, tokens))
     ref, _ = moe.moe_block(ro, router, get, oracle_config(d), gamma, 1e-6, bias, tokens)
     keep = [i for i, t in enumerate(tokens) if t not in excluded]
