@@ -8,7 +8,11 @@
  * With many tokens every expert is selected by several tokens, so its weights
  * are dequantised once into shared memory and multiplied against all of its
  * tokens on the tensor cores (tcgen05.mma, FP32 accumulation in tensor
- * memory), instead of once per token tile in registers.
+ * memory), instead of once per token tile in registers. Experts that few
+ * tokens chose (up to 16, in calls of up to 512 tokens; the shared expert
+ * while a call has at most 256 tokens) are multiplied on mma.sync tiles of up
+ * to 16 tokens with the weights dequantised in registers instead, where the
+ * tensor-core staging would serve too few columns per weight.
  *
  * Same computation and rounding points as flint_moe_decode (flint_moe.h):
  *   logit = x Wr^T (FP32); sigmoid top-k (ties to the lower index),
@@ -50,7 +54,8 @@ flint_moe_status flint_moe_prefill_workspace_init(const flint_moe_config* cfg, i
  * a no-op). x: bf16 [B][H]; out: bf16 [B][H] (must not overlap x); workspace:
  * workspace_bytes >= flint_moe_prefill_workspace_bytes(cfg, B), 256-byte
  * aligned, initialised once with flint_moe_prefill_workspace_init, not shared
- * with another call in flight. Seven kernels in stream order:
+ * with another call in flight. Seven kernels in stream order (nine in calls of
+ * up to 512 tokens, with the small-tile kernels of steps 5 and 6):
  *   1. router GEMM on the tensor cores (bf16 router rows x tokens, FP32),
  *      split along H into up to 8 ranges while its tiles are fewer than the
  *      SMs (the partial sums live in the y region until step 6);
@@ -58,15 +63,16 @@ flint_moe_status flint_moe_prefill_workspace_init(const flint_moe_config* cfg, i
  *      not depend on timing), sigmoid top-k per token, counting the tokens of
  *      every expert;
  *   3. plan: slots, the first grouped row of every expert, and the (expert,
- *      128-row tile, token tile) work lists;
+ *      128-row tile, token tile) work lists of both tile kinds;
  *   4. per token: its entries of the expert-grouped row lists, and its row in
  *      f16 (times a power of two that keeps every bf16 value exact) at its
  *      grouped rows;
  *   5. gate/up grouped GEMM: NVFP4 tiles dequantised to f16 in shared memory,
  *      tcgen05.mma against the expert's token rows (loaded by TMA), SiLU * up
- *      epilogue writing h (bf16);
+ *      epilogue writing h (bf16); then the small tiles the same way on
+ *      mma.sync;
  *   6. down grouped GEMM on h (bf16 products), epilogue writing w_j * y into
- *      y[B][S + k][H];
+ *      y[B][S + k][H]; then its small tiles;
  *   7. combine: out = bf16(sum over the S + k rows of y), in that fixed order.
  * NVFP4 layers only (FLINT_MOE_EUNSUPPORTED for BF16 weights). Inputs must be
  * finite. x and out 16-byte aligned. */
